@@ -1,0 +1,237 @@
+"""Python access to the plain CPU oracle (oracle.c) through ctypes.
+
+TEST INFRASTRUCTURE ONLY. Tests, the package smoke check and the benchmark's
+CPU-baseline leg may import this module; the product path (the CUDA library
+and its binding) never does. All arrays are numpy arrays on the host.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+BF16, FP8_E4M3_B128, NVFP4_B16, RAW = 0, 1, 2, 3
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (no fast-math, no FMA
+    contraction, no host-specific flags)."""
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
+        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+               "-shared", "-Wall", "-o", _LIB + ".tmp", _SRC, "-lm"]
+        subprocess.check_call(cmd)
+        os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = ctypes.CDLL(_LIB)
+        f32, u8, u16, i32 = ctypes.c_float, ctypes.c_uint8, ctypes.c_uint16, ctypes.c_int
+        _lib.oracle_bf16_to_f32.restype = f32
+        _lib.oracle_bf16_to_f32.argtypes = [u16]
+        _lib.oracle_f32_to_bf16.restype = u16
+        _lib.oracle_f32_to_bf16.argtypes = [f32]
+        _lib.oracle_e4m3_value.restype = f32
+        _lib.oracle_e4m3_value.argtypes = [u8]
+        _lib.oracle_e4m3_encode.restype = u8
+        _lib.oracle_e4m3_encode.argtypes = [f32]
+        _lib.oracle_e2m1_value.restype = f32
+        _lib.oracle_e2m1_value.argtypes = [u8]
+        _lib.oracle_e2m1_encode.restype = u8
+        _lib.oracle_e2m1_encode.argtypes = [f32]
+        _lib.oracle_fp8_group.restype = None
+        _lib.oracle_nvfp4_group.restype = None
+        for name in ("oracle_record_layout", "oracle_layout", "oracle_dispatch",
+                     "oracle_identity_expert", "oracle_combine_topk", "oracle_combine_ranks",
+                     "oracle_combine_topk_ranks", "oracle_combine_topk_f64"):
+            getattr(_lib, name).restype = i32
+    return _lib
+
+
+def _p(a: np.ndarray | None):
+    if a is None:
+        return ctypes.c_void_p(0)
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its arguments (rc={rc})")
+
+
+# ---- number formats --------------------------------------------------------
+
+def bf16_to_f32(b: int) -> float:
+    return _load().oracle_bf16_to_f32(int(b))
+
+
+def f32_to_bf16(f: float) -> int:
+    return _load().oracle_f32_to_bf16(float(np.float32(f)))
+
+
+def e4m3_value(code: int) -> float:
+    return _load().oracle_e4m3_value(int(code))
+
+
+def e4m3_encode(x: float) -> int:
+    return _load().oracle_e4m3_encode(float(np.float32(x)))
+
+
+def e2m1_value(code: int) -> float:
+    return _load().oracle_e2m1_value(int(code))
+
+
+def e2m1_encode(x: float) -> int:
+    return _load().oracle_e2m1_encode(float(np.float32(x)))
+
+
+def bf16_to_f32_array(b: np.ndarray) -> np.ndarray:
+    """Vector form of bf16_to_f32 (an exact widening, used by tests)."""
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16_array(f: np.ndarray) -> np.ndarray:
+    lib = _load()
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    return np.array([lib.oracle_f32_to_bf16(float(v)) for v in f.ravel()],
+                    dtype=np.uint16).reshape(f.shape)
+
+
+def fp8_group(x_bf16: np.ndarray):
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    q = np.zeros(x.size, dtype=np.uint8)
+    sc = np.zeros(1, dtype=np.float32)
+    _load().oracle_fp8_group(_p(x), ctypes.c_int(x.size), _p(q), _p(sc))
+    return q, float(sc[0])
+
+
+def nvfp4_group(x_bf16: np.ndarray):
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    assert x.size % 2 == 0
+    q = np.zeros(x.size // 2, dtype=np.uint8)
+    sc = np.zeros(1, dtype=np.uint8)
+    _load().oracle_nvfp4_group(_p(x), ctypes.c_int(x.size), _p(q), _p(sc))
+    return q, int(sc[0])
+
+
+# ---- record layout -----------------------------------------------------------
+
+def record_layout(topk: int, hidden: int, in_kind: int, out_kind: int,
+                  raw_payload_bytes: int = 0, raw_scale_bytes: int = 0) -> dict:
+    out = np.zeros(7, dtype=np.int32)
+    rc = _load().oracle_record_layout(topk, hidden, in_kind, out_kind, raw_payload_bytes,
+                                      raw_scale_bytes, _p(out))
+    _check(rc, "record_layout")
+    keys = ("record_bytes", "off_ids", "off_weights", "off_payload", "off_scales",
+            "payload_bytes", "scale_bytes")
+    return {k: int(v) for k, v in zip(keys, out)}
+
+
+# ---- layout -------------------------------------------------------------------
+
+def layout(topk_idx: np.ndarray, num_experts: int, num_ranks: int) -> dict:
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    n, k = idx.shape
+    out = dict(
+        tokens_per_expert=np.zeros(num_experts, np.int32),
+        tokens_per_rank=np.zeros(num_ranks, np.int32),
+        is_token_in_rank=np.zeros((n, num_ranks), np.uint8),
+        expert_offset=np.zeros(num_experts + 1, np.int32),
+        rank_offset=np.zeros(num_ranks + 1, np.int32),
+        slot_of=np.zeros((n, k), np.int32),
+        src_of_slot=np.zeros(n * k, np.int32),
+    )
+    rc = _load().oracle_layout(
+        _p(idx), n, k, num_experts, num_ranks, _p(out["tokens_per_expert"]),
+        _p(out["tokens_per_rank"]), _p(out["is_token_in_rank"]), _p(out["expert_offset"]),
+        _p(out["rank_offset"]), _p(out["slot_of"]), _p(out["src_of_slot"]))
+    _check(rc, "layout")
+    out["num_pairs"] = int(out["expert_offset"][-1])
+    return out
+
+
+# ---- dispatch -------------------------------------------------------------------
+
+def dispatch(topk_idx, topk_weights, hidden, scales, slot_of, num_records: int,
+             in_kind: int, out_kind: int, hidden_size: int,
+             raw_payload_bytes: int = 0, raw_scale_bytes: int = 0) -> np.ndarray:
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    n, k = idx.shape
+    lay = record_layout(k, hidden_size, in_kind, out_kind, raw_payload_bytes, raw_scale_bytes)
+    rec = np.zeros((num_records, lay["record_bytes"]), dtype=np.uint8)
+    h = np.ascontiguousarray(hidden)
+    sc = None if scales is None else np.ascontiguousarray(scales)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    rc = _load().oracle_dispatch(_p(idx), _p(w), _p(h), _p(sc), n, k, hidden_size, in_kind,
+                                 out_kind, raw_payload_bytes, raw_scale_bytes, _p(so), _p(rec))
+    _check(rc, "dispatch")
+    return rec
+
+
+def identity_expert(records: np.ndarray, topk: int, hidden_size: int, out_kind: int) -> np.ndarray:
+    rec = np.ascontiguousarray(records, dtype=np.uint8)
+    y = np.zeros((rec.shape[0], hidden_size), dtype=np.uint16)
+    rc = _load().oracle_identity_expert(_p(rec), rec.shape[0], topk, hidden_size, out_kind, _p(y))
+    _check(rc, "identity_expert")
+    return y
+
+
+# ---- combine ----------------------------------------------------------------------
+
+def combine_topk(y, topk_weights, slot_of, hidden_size: int) -> np.ndarray:
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    n, k = so.shape
+    out = np.zeros((n, hidden_size), dtype=np.uint16)
+    _check(_load().oracle_combine_topk(_p(y), _p(w), _p(so), n, k, hidden_size, _p(out)),
+           "combine_topk")
+    return out
+
+
+def combine_ranks(partials) -> np.ndarray:
+    p = np.ascontiguousarray(partials, dtype=np.uint16)
+    r, n, h = p.shape
+    out = np.zeros((n, h), dtype=np.uint16)
+    _check(_load().oracle_combine_ranks(_p(p), r, n, h, _p(out)), "combine_ranks")
+    return out
+
+
+def combine_topk_ranks(y, topk_idx, topk_weights, slot_of, num_experts: int, num_ranks: int,
+                       hidden_size: int) -> np.ndarray:
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    n, k = so.shape
+    out = np.zeros((n, hidden_size), dtype=np.uint16)
+    _check(_load().oracle_combine_topk_ranks(_p(y), _p(idx), _p(w), _p(so), n, k, num_experts,
+                                             num_ranks, hidden_size, _p(out)),
+           "combine_topk_ranks")
+    return out
+
+
+def combine_topk_f64(y, topk_weights, slot_of, hidden_size: int) -> np.ndarray:
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    n, k = so.shape
+    out = np.zeros((n, hidden_size), dtype=np.float64)
+    _check(_load().oracle_combine_topk_f64(_p(y), _p(w), _p(so), n, k, hidden_size, _p(out)),
+           "combine_topk_f64")
+    return out
