@@ -1,0 +1,493 @@
+"""Benchmark of the MoE dispatch + combine hot path on GB300.
+
+One step = moe_layout + moe_dispatch + moe_combine (TOPK_RANKS: the top-k
+weighted reduction grouped by rank and the cross-rank sum) over one batch of
+synthetic input, through the C ABI. Default workload: prefill, N=4096 tokens,
+hidden 7168 BF16 ~N(0,1), 256 experts in 8 groups (top-4 groups, top-8
+experts), R=8 virtual ranks, FP8 e4m3 per-128 dispatch, BF16 combine. Expert
+outputs come from an identity expert (the dequantised records), made once
+before timing: the expert itself is not part of the path.
+
+Prints one JSON line. `--impl reference` times the plain CPU oracle instead
+(rank 0 only), on bounded samples of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload prefill|decode|rs|skewed|tiny]
+Multi-GPU runs (torchrun) are independent replicas: the path has no
+cross-GPU exchange on one-GPU-per-rank hardware here.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and HBM GB/s vs GB300 roofline (1 GPU)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------- workloads --
+
+def workload_spec(name: str) -> dict:
+    """Shapes and algorithmic bytes per token for each kernel of a step."""
+    if name == "prefill":
+        s = dict(num_tokens=4096, hidden=7168, num_experts=256, topk=8, num_ranks=8,
+                 out_kind="fp8", record_bytes=7472,
+                 text="prefill N=4096 H=7168 E=256 (8 groups, top-4 groups) top-8 R=8; "
+                      "FP8 e4m3 per-128 dispatch; BF16 combine grouped by rank")
+    elif name == "skewed":
+        s = dict(num_tokens=16384, hidden=7168, num_experts=256, topk=8, num_ranks=16,
+                 out_kind="fp8", record_bytes=7472,
+                 text="skewed N=16384 H=7168 E=256 Zipf(1.2) top-8 R=16; FP8 dispatch; "
+                      "BF16 combine grouped by rank")
+    elif name == "decode":
+        s = dict(num_tokens=256, hidden=7168, num_experts=256, topk=8, num_ranks=8,
+                 out_kind="raw", record_bytes=4112,
+                 text="decode N=256 top-8 of 256 R=8; raw NVFP4 payload 3584 B + 448 B "
+                      "scales per token; BF16 combine H=7168 grouped by rank")
+    elif name == "rs":
+        s = dict(num_tokens=2048, hidden=8192, num_experts=256, topk=8, num_ranks=4,
+                 out_kind="bf16", record_bytes=16 + 32 + 32 + 16384,
+                 text="reduce-scatter workload R=4 H=8192 512 tokens/rank (8 MiB/rank); "
+                      "BF16 dispatch; top-8 of 256 combine grouped by rank")
+    elif name == "tiny":
+        s = dict(num_tokens=128, hidden=1024, num_experts=16, topk=2, num_ranks=2,
+                 out_kind="bf16", record_bytes=2096,
+                 text="tiny N=128 H=1024 E=16 top-2 R=2; BF16 dispatch and combine")
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    n, h, k, r = s["num_tokens"], s["hidden"], s["topk"], s["num_ranks"]
+    in_row = 3584 + 448 if s["out_kind"] == "raw" else 2 * h
+    # Algorithmic bytes per token: what each step must move at least once.
+    s["bytes_per_token"] = dict(
+        layout=4 * k + 4 * k + 4 * k + r,                     # ids in; slot_of, src_of_slot, mask out
+        dispatch=in_row + 4 * k + 4 * k + 4 * k + k * s["record_bytes"],  # row, ids, w, slots in; k records out
+        combine=k * 2 * h + 4 * k * 3 + 2 * h,                # k expert rows, w, slots, ids in; row out
+    )
+    s["name"] = name
+    return s
+
+
+def make_inputs(spec: dict, seed: int = 0) -> dict:
+    from combine_moe_layout_03_gb300 import synth
+    n = spec["num_tokens"]
+    if spec["name"] == "prefill":
+        return synth.prefill_case(seed=seed, n=n)
+    if spec["name"] == "skewed":
+        return synth.skewed_case(seed=seed, n=n)
+    if spec["name"] == "decode":
+        return synth.decode_case(seed=seed, n=n)
+    if spec["name"] == "rs":
+        c = synth.rs_case(seed=seed, tokens_per_rank=n // 4, with_partials=False,
+                          with_expert_out=False)
+        c["hidden_bf16"] = synth.bf16_normal(synth.rng_for(seed, 9), (n, spec["hidden"]))
+        return c
+    return synth.tiny_case(seed=seed)
+
+
+# ---------------------------------------------------------------- clocks -----
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [[x.strip() for x in line.split(",")] for line in out.splitlines() if line.strip()]
+        rows = [r for r in rows if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = [v for v in sm if smax and v >= 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def gpu_uuid():
+    try:
+        import torch
+        u = str(torch.cuda.get_device_properties(0).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- peaks ------
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def recorded_traffic(kernel: str, workload: str) -> int | None:
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {"combine": "combine.cu", "dispatch": "dispatch.cu", "layout": "layout.cu"}[kernel]
+    with open(os.path.join(ROOT, "combine_moe_layout_03_gb300", "csrc", src), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    for line in open(path):
+        if line.startswith("#") or "=" not in line:
+            continue
+        kv = dict(x.split("=", 1) for x in line.split())
+        if kv.get("kernel") == kernel and kv.get("workload") == workload:
+            return int(kv["bytes_per_launch"]) if kv.get("source_sha256") == sha else None
+    return None
+
+
+# ---------------------------------------------------------------- our arm ----
+
+class Step:
+    """Resident buffers and the three calls of one step."""
+
+    def __init__(self, spec: dict, dev, seed: int = 0):
+        import torch
+        from combine_moe_layout_03_gb300 import moe
+        self.moe = moe
+        self.spec = spec
+        c = make_inputs(spec, seed)
+        n, k, e, r, h = (spec["num_tokens"], spec["topk"], spec["num_experts"],
+                         spec["num_ranks"], spec["hidden"])
+        self.host = c
+        self.ids = torch.from_numpy(c["topk_idx"]).to(dev)
+        self.w = torch.from_numpy(c["topk_weights"]).to(dev)
+        if spec["out_kind"] == "raw":
+            self.x = torch.from_numpy(c["payload"]).to(dev)
+            self.sc = torch.from_numpy(c["scales"]).to(dev)
+            self.desc = moe.MoeDesc(n, k, e, r, h, moe.MOE_PAYLOAD_RAW, moe.MOE_PAYLOAD_RAW,
+                                    3584, 448)
+        else:
+            self.x = torch.from_numpy(c["hidden_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+            self.sc = None
+            kind = moe.MOE_PAYLOAD_FP8_E4M3_B128 if spec["out_kind"] == "fp8" else moe.MOE_PAYLOAD_BF16
+            self.desc = moe.MoeDesc(n, k, e, r, h, moe.MOE_PAYLOAD_BF16, kind)
+        self.cdesc = moe.MoeDesc(n, k, e, r, h)
+        self.lay = moe.layout_outputs(self.desc, dev)
+        self.ws = torch.empty(max(moe.moe_workspace_size(self.desc), 256), dtype=torch.uint8,
+                              device=dev)
+        rl = moe.moe_record_layout(self.desc)
+        assert rl["record_bytes"] == spec["record_bytes"]
+        self.records = torch.empty((n * k, rl["record_bytes"]), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((n, h), dtype=torch.bfloat16, device=dev)
+        # identity expert, once: the records' payload back to BF16 rows
+        self.layout()
+        self.dispatch()
+        torch.cuda.synchronize()
+        if spec["out_kind"] == "fp8":
+            q = self.records[:, rl["off_payload"]:rl["off_payload"] + h].contiguous()
+            s = self.records[:, rl["off_scales"]:rl["off_scales"] + 4 * (h // 128)].contiguous()
+            self.y = (q.view(torch.float8_e4m3fn).float()
+                      * s.view(torch.float32).repeat_interleave(128, dim=1)).to(torch.bfloat16)
+        elif spec["out_kind"] == "bf16":
+            self.y = self.records[:, rl["off_payload"]:rl["off_payload"] + 2 * h].contiguous() \
+                .view(torch.bfloat16)
+        else:  # raw NVFP4 bytes: the expert's output rows are drawn directly
+            from combine_moe_layout_03_gb300 import synth
+            yy = synth.bf16_normal(synth.rng_for(seed, 11), (n * k, h))
+            self.y = torch.from_numpy(yy.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.launches_per_step = (1 if n * k <= 4096 else 2) + 1 + 1
+
+    def layout(self, stream=None):
+        self.moe.moe_layout(self.desc, self.ids, self.lay, self.ws, stream)
+
+    def dispatch(self, stream=None):
+        self.moe.moe_dispatch(self.desc, self.ids, self.w, self.x, self.sc, self.lay["slot_of"],
+                              self.records, stream)
+
+    def combine(self, stream=None):
+        self.moe.moe_combine(self.cdesc, self.moe.MOE_COMBINE_TOPK_RANKS, self.y, self.ids,
+                             self.w, self.lay["slot_of"], self.out, stream)
+
+    def run(self, stream=None):
+        self.layout(stream)
+        self.dispatch(stream)
+        self.combine(stream)
+
+
+def run_ours(args, spec, rank, world):
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    st = Step(spec, dev, seed=rank)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    K, W = args.steps, args.warmup
+    clocks = ClockSampler(gpu_uuid())
+    for _ in range(W):
+        st.run()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush.zero_()                  # L2 flush, outside the timed events
+        e = ev[i]
+        e[0].record(stream)
+        st.layout()
+        e[1].record(stream)
+        st.dispatch()
+        e[2].record(stream)
+        st.combine()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    per = {name: [ev[i][a].elapsed_time(ev[i][b]) for i in range(K)]
+           for name, a, b in (("layout", 0, 1), ("dispatch", 1, 2), ("combine", 2, 3))}
+    step_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(K)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    n = spec["num_tokens"]
+    value = n * K * world / (total_ms / 1e3)
+    peaks = measured_peaks()
+    kern = {name: statistics.mean(v) for name, v in per.items()}
+    dom = max(("dispatch", "combine"), key=lambda x: kern[x])
+    bpt = spec["bytes_per_token"]
+    achieved = {name: bpt[name] * n / (kern[name] / 1e3) / 1e9 for name in kern}
+    step_bytes = sum(bpt.values()) * n
+
+    e2e = measure_e2e(st, spec, dev, K, W) if rank == 0 else None
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in/out, fp32 accumulate, e4m3 records" if spec["out_kind"] == "fp8"
+        else "bf16 in/out, fp32 accumulate",
+        "data": "synthetic (seeded; shapes and distributions of the pages' workloads)",
+        "config": {"workload": spec["text"], "num_tokens": n, "hidden": spec["hidden"],
+                   "num_experts": spec["num_experts"], "topk": spec["topk"],
+                   "num_ranks": spec["num_ranks"], "record_bytes": spec["record_bytes"],
+                   "combine_mode": "TOPK_RANKS",
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside "
+                         f"the timed events); step working set {step_bytes / 1e6:.0f} MB",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved[dom], 1),
+                     "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
+                     "frac": round(achieved[dom] / peaks["hbm_gbs"], 4),
+                     "traffic": recorded_traffic(dom, spec["name"]),
+                     "algorithmic_bytes_per_launch": bpt[dom] * n},
+        "kernels_us": {name: round(v * 1e3, 2) for name, v in kern.items()},
+        "kernels_gbs": {name: round(v, 1) for name, v in achieved.items()},
+        "kernels_frac": {name: round(v / peaks["hbm_gbs"], 4) for name, v in achieved.items()},
+        "step_gbs": round(step_bytes / (total_ms / K / 1e3) / 1e9, 1),
+        "gpu_launches": st.launches_per_step * K,
+        "clocks": clk,
+        "wall_s": round(wall, 3),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec, budget_s=args.cpu_seconds)
+    return line
+
+
+def measure_e2e(st: Step, spec: dict, dev, K: int, W: int) -> dict:
+    """Same step through the public API with inputs copied from pinned host
+    memory every step and the combined output read back every step."""
+    import torch
+    n = spec["num_tokens"]
+    h_ids = st.ids.cpu().pin_memory()
+    h_w = st.w.cpu().pin_memory()
+    h_x = st.x.cpu().pin_memory()
+    h_sc = st.sc.cpu().pin_memory() if st.sc is not None else None
+    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_w, h_x) if t is not None)
+    if h_sc is not None:
+        h2d += h_sc.numel()
+    d2h = h_out.numel() * h_out.element_size()
+
+    def one():
+        st.ids.copy_(h_ids, non_blocking=True)
+        st.w.copy_(h_w, non_blocking=True)
+        st.x.copy_(h_x, non_blocking=True)
+        if h_sc is not None:
+            st.sc.copy_(h_sc, non_blocking=True)
+        st.run()
+        h_out.copy_(st.out, non_blocking=True)
+
+    for _ in range(max(W, 1)):
+        one()
+    torch.cuda.synchronize()
+    k2 = max(1, min(K, 200))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(k2):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / k2
+    return {"value": round(n / (ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": k2, "ms_per_step": round(ms, 4)}
+
+
+# ---------------------------------------------------------------- oracle arm -
+
+def oracle_step(c: dict, spec: dict, t0: int, t1: int):
+    """The oracle's layout + dispatch + combine over tokens [t0, t1)."""
+    import oracle
+    ids, w = c["topk_idx"][t0:t1], c["topk_weights"][t0:t1]
+    e, r, h = spec["num_experts"], spec["num_ranks"], spec["hidden"]
+    lay = oracle.layout(ids, e, r)
+    P = lay["num_pairs"]
+    if spec["out_kind"] == "raw":
+        rec = oracle.dispatch(ids, w, c["payload"][t0:t1], c["scales"][t0:t1], lay["slot_of"], P,
+                              oracle.RAW, oracle.RAW, h, 3584, 448)
+        y = np.zeros((max(P, 1), h), np.uint16)
+    else:
+        kind = oracle.FP8_E4M3_B128 if spec["out_kind"] == "fp8" else oracle.BF16
+        rec = oracle.dispatch(ids, w, c["hidden_bf16"][t0:t1], None, lay["slot_of"], P,
+                              oracle.BF16, kind, h)
+        y = oracle.identity_expert(rec, spec["topk"], h, kind)
+    nt = t1 - t0
+    if nt % r == 0:
+        oracle.combine_topk_ranks(y, ids, w, lay["slot_of"], e, r, h)
+    else:
+        oracle.combine_topk(y, w, lay["slot_of"], h)
+    return rec
+
+
+def cpu_baseline(spec: dict, budget_s: float = 12.0) -> dict:
+    """The oracle as it stands, single-threaded, on a bounded sample."""
+    c = make_inputs(spec, 0)
+    n = spec["num_tokens"]
+    r = spec["num_ranks"]
+    t = time.perf_counter()
+    oracle_step(c, spec, 0, r)
+    per_tok = max((time.perf_counter() - t) / r, 1e-6)
+    sample = int(min(n, max(r, budget_s / per_tok)))
+    sample -= sample % r
+    t = time.perf_counter()
+    oracle_step(c, spec, 0, sample)
+    dt = time.perf_counter() - t
+    return {"value": round(sample / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {sample} of {n} tokens of the {spec['name']} workload, one pass of "
+                      f"layout + dispatch + rank-grouped combine ({dt:.1f} s)"}
+
+
+def run_reference(args, spec) -> dict:
+    c = make_inputs(spec, 0)
+    n, r = spec["num_tokens"], spec["num_ranks"]
+    K, W = args.steps, args.warmup
+    t = time.perf_counter()
+    oracle_step(c, spec, 0, r)
+    per_tok = max((time.perf_counter() - t) / r, 1e-6)
+    budget = args.cpu_seconds * 8  # whole reference run within a few minutes
+    sample = int(min(n, max(r, budget / (K + W) / per_tok)))
+    sample -= sample % r
+    for i in range(W):
+        oracle_step(c, spec, 0, sample)
+    t = time.perf_counter()
+    for i in range(K):
+        oracle_step(c, spec, 0, sample)
+    dt = time.perf_counter() - t
+    value = sample * K / dt
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(dt / K * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 accumulate (CPU oracle)", "data": "synthetic",
+        "config": {"workload": spec["text"], "num_tokens": n, "sample_tokens_per_step": sample},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"first {sample} of {n} tokens per step"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------- main -------
+
+def reduce_replicas(values_ms: list[float]) -> float:
+    """Whole-job time of independent replicas: the slowest rank."""
+    return max(values_ms)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill",
+                    choices=["prefill", "decode", "rs", "skewed", "tiny"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    spec = workload_spec(args.workload)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, spec)), flush=True)
+        return 0
+
+    import __graft_entry__
+    __graft_entry__.build()
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl")
+    line = run_ours(args, spec, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

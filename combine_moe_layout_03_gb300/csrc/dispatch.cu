@@ -1,0 +1,199 @@
+// dispatch.cu -- permute and pack of MoE dispatch on sm_103a.
+//
+// One record per (token, top-k) pair, written to its slot (records grouped by
+// destination rank and expert). Record format: an int4 header, the id and
+// weight rows, the payload and its scales, each segment at a 16-byte
+// boundary (DeepEP repository, csrc/config.hpp LowLatencyLayout message =
+// int4 header + payload + scales; vLLM compare view ds-exp-2...ds-exp-ag,
+// moe_allgather.cu "Host launcher": tensors at 16-byte-aligned offsets).
+//
+// Design: one block per token. The token's row is read once from HBM with
+// 16-byte asynchronous copies (cp.async, all in flight together) into shared
+// memory, quantised there (FP8 e4m3 per 128 channels: a
+// half-warp per group; NVFP4 per 16: a lane pair per group) and the record
+// body (everything after the 16-byte header) is assembled once in shared
+// memory. Then thread j writes pair j's header with one 16-byte store and
+// hands the body to the bulk-copy engine (cp.async.bulk shared -> global), so
+// the k copies of the body cost no register traffic. The token's input is
+// read once and k records are written: the kernel is write-bound.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kDispatchThreads = 256;
+
+// Zero [from, to) of the shared image (byte granularity; few bytes).
+__device__ __forceinline__ void zero_bytes(uint8_t* img, int from, int to) {
+  for (int i = from + threadIdx.x; i < to; i += blockDim.x) img[i] = 0;
+}
+
+// Asynchronous 16-byte copies of n16 vectors global -> shared (cp.async,
+// L1 bypassed). All of them are in flight at once; cp_async_wait_all() waits
+// for this thread's copies in hardware.
+__device__ __forceinline__ void copy_g2s_async(uint8_t* dst, const uint8_t* src, int n16) {
+  for (int i = threadIdx.x; i < n16; i += blockDim.x) {
+    uint32_t sa = (uint32_t)__cvta_generic_to_shared(dst + 16 * i);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(src + 16 * i)
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// FP8 e4m3 with one fp32 scale per 128 channels. A half-warp covers one
+// group: 16 lanes x 8 BF16 values. amax -> a = max(amax, 1e-4) ->
+// scale = a / 448, inv = 448 / a (IEEE divisions) -> q = e4m3(x * inv).
+__device__ __forceinline__ void quant_fp8(const uint8_t* row, int H, uint8_t* pay, float* scl) {
+  // row: the token's BF16 row staged in shared memory
+  const int groups = H / 128;
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int half = (int)(lane_id() >> 4), li = (int)(lane_id() & 15);
+  for (int gp = warp; gp * 2 < groups; gp += nwarps) {
+    const int g = gp * 2 + half;
+    const bool on = g < groups;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (on) v = *reinterpret_cast<const uint4*>(row + g * 256 + li * 16);
+    float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float a = fmaxf(amax, 1e-4f);
+    const float inv = __fdiv_rn(448.0f, a);
+    uint2 q;
+    q.x = cvt_e4m3x2(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv)) |
+          cvt_e4m3x2(__fmul_rn(x[2], inv), __fmul_rn(x[3], inv)) << 16;
+    q.y = cvt_e4m3x2(__fmul_rn(x[4], inv), __fmul_rn(x[5], inv)) |
+          cvt_e4m3x2(__fmul_rn(x[6], inv), __fmul_rn(x[7], inv)) << 16;
+    if (on) {
+      *reinterpret_cast<uint2*>(pay + g * 128 + li * 8) = q;
+      if (li == 0) scl[g] = __fdiv_rn(a, 448.0f);
+    }
+  }
+}
+
+// NVFP4: e2m1 codes with one e4m3 scale byte per 16 channels. A lane pair
+// covers one group: 2 lanes x 8 BF16 values. amax -> sc = e4m3(amax / 6) ->
+// d = value(sc) -> q = d == 0 ? 0 : e2m1(x / d) (IEEE divisions). Byte i of
+// the packed row holds element 2i (low nibble) and 2i+1 (high nibble).
+__device__ __forceinline__ void quant_nvfp4(const uint8_t* row, int H, uint8_t* pay, uint8_t* scl) {
+  // row: the token's BF16 row staged in shared memory
+  const int chunks = H / 8;  // 16-byte input vectors; even since H % 16 == 0
+  for (int cb = (threadIdx.x & ~31); cb < chunks; cb += blockDim.x) {
+    const int c = cb + (int)lane_id();
+    const bool on = c < chunks;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (on) v = *reinterpret_cast<const uint4*>(row + c * 16);
+    float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    const uint32_t sc = cvt_e4m3x2(__fdiv_rn(amax, 6.0f), 0.0f) & 0xffu;
+    const float d = e4m3_to_f32(sc);
+    uint32_t packed = 0;
+    if (d != 0.0f) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        packed |= cvt_e2m1x2(__fdiv_rn(x[2 * i], d), __fdiv_rn(x[2 * i + 1], d)) << (8 * i);
+    }
+    if (on) {
+      *reinterpret_cast<uint32_t*>(pay + c * 4) = packed;
+      if ((c & 1) == 0) scl[c >> 1] = (uint8_t)sc;
+    }
+  }
+}
+
+template <int OUT_KIND>
+__global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p) {
+  // Dynamic shared memory: the record body (record bytes [16, record_bytes)),
+  // then, for the quantising kinds, the staged BF16 input row.
+  extern __shared__ __align__(128) uint8_t img[];
+  __shared__ int s_slot[MOE_MAX_TOPK];
+  __shared__ int s_expert[MOE_MAX_TOPK];
+  const int t = blockIdx.x;
+  const int k = p.topk;
+  const int body = p.record_bytes - 16;
+  const int oi = p.off_ids - 16, ow = p.off_weights - 16, op = p.off_payload - 16,
+            os = p.off_scales - 16;
+  constexpr bool kQuant = OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128 || OUT_KIND == MOE_PAYLOAD_NVFP4_B16;
+  uint8_t* stage = img + body;
+
+  // start the row's copies first so they overlap the small loads below
+  const uint8_t* row = p.hidden + (size_t)t * p.in_row_bytes;
+  if (kQuant) {
+    copy_g2s_async(stage, row, p.in_row_bytes / 16);
+  } else {
+    copy_g2s_async(img + op, row, p.payload_bytes / 16);
+    if (OUT_KIND == MOE_PAYLOAD_RAW && p.scale_bytes > 0)
+      copy_g2s_async(img + os, p.scales + (size_t)t * p.in_scale_bytes, p.scale_bytes / 16);
+  }
+
+  // slots, ids and weights of this token
+  if (threadIdx.x < k) {
+    const int64_t q = (int64_t)t * k + threadIdx.x;
+    const int s = p.slot_of[q];
+    const int e = p.topk_idx[q];
+    s_slot[threadIdx.x] = (s >= 0 && (int64_t)s < p.record_capacity) ? s : -1;
+    s_expert[threadIdx.x] = e;
+    reinterpret_cast<int32_t*>(img + oi)[threadIdx.x] = e;
+    reinterpret_cast<uint32_t*>(img + ow)[threadIdx.x] = __float_as_uint(p.topk_weights[q]);
+  }
+  zero_bytes(img, oi + 4 * k, ow);
+  zero_bytes(img, ow + 4 * k, op);
+  zero_bytes(img, op + p.payload_bytes, os);
+  zero_bytes(img, os + p.scale_bytes, body);
+
+  cp_async_wait_all();
+  __syncthreads();
+  if (OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128) {
+    quant_fp8(stage, p.hidden_size, img + op, reinterpret_cast<float*>(img + os));
+  } else if (OUT_KIND == MOE_PAYLOAD_NVFP4_B16) {
+    quant_nvfp4(stage, p.hidden_size, img + op, img + os);
+  }
+
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  if (threadIdx.x < k) {
+    const int j = threadIdx.x;
+    const int s = s_slot[j];
+    if (s >= 0) {
+      uint8_t* rec = p.records + (size_t)s * p.record_bytes;
+      st_v4(rec, make_uint4((uint32_t)t, (uint32_t)j, (uint32_t)s_expert[j], 0u));
+      bulk_store_s2g(rec + 16, img, (uint32_t)body);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, cudaStream_t s) {
+  (void)in_kind;
+  const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16;
+  const size_t smem = (size_t)(p.record_bytes - 16) + (quant ? (size_t)p.in_row_bytes : 0);
+  const void* fn = nullptr;
+  switch (out_kind) {
+    case MOE_PAYLOAD_BF16: fn = (const void*)k_dispatch<MOE_PAYLOAD_BF16>; break;
+    case MOE_PAYLOAD_FP8_E4M3_B128: fn = (const void*)k_dispatch<MOE_PAYLOAD_FP8_E4M3_B128>; break;
+    case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_dispatch<MOE_PAYLOAD_NVFP4_B16>; break;
+    default: fn = (const void*)k_dispatch<MOE_PAYLOAD_RAW>; break;
+  }
+  if (smem > 48 * 1024) {
+    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  DispatchParams q = p;
+  void* args[] = {&q};
+  return cudaLaunchKernel(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), args, smem, s);
+}
+
+}  // namespace moe

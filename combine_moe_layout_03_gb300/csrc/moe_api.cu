@@ -1,0 +1,281 @@
+// moe_api.cu -- the extern "C" entry points of libmoe.so (declared and
+// documented in include/moe.h): argument validation on the host, then the
+// launches. Nothing here allocates device memory or synchronises, except
+// moe_layout_status.
+#include <string.h>
+
+#include "moe_internal.cuh"
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+inline int pad16(int x) { return (x + 15) / 16 * 16; }
+
+// Shape checks shared by every call. Returns MOE_OK or an error code.
+int check_desc(const moe_desc_t* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->num_tokens < 0 || d->topk < 1 || d->num_experts < 1 || d->num_ranks < 1)
+    return MOE_ERR_SHAPE;
+  if (d->topk > MOE_MAX_TOPK || d->num_experts > MOE_MAX_EXPERTS || d->num_ranks > MOE_MAX_RANKS)
+    return MOE_ERR_SHAPE;
+  if (d->num_experts % d->num_ranks != 0) return MOE_ERR_SHAPE;
+  if ((int64_t)d->num_tokens * d->topk >= ((int64_t)1 << 31)) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+int record_layout(const moe_desc_t* d, moe_record_layout_t* o) {
+  int rc = check_desc(d);
+  if (rc != MOE_OK) return rc;
+  int pb = 0, sb = 0;
+  const int H = d->hidden;
+  if (d->in_kind == MOE_PAYLOAD_RAW && d->out_kind == MOE_PAYLOAD_RAW) {
+    if (d->raw_payload_bytes < 0 || d->raw_scale_bytes < 0) return MOE_ERR_SHAPE;
+    if (d->raw_payload_bytes > MOE_MAX_RAW_BYTES || d->raw_scale_bytes > MOE_MAX_RAW_BYTES)
+      return MOE_ERR_SHAPE;
+    if (d->raw_payload_bytes % 16 || d->raw_scale_bytes % 16) return MOE_ERR_ALIGNMENT;
+    pb = d->raw_payload_bytes;
+    sb = d->raw_scale_bytes;
+  } else if (d->in_kind == MOE_PAYLOAD_BF16) {
+    if (H < 1 || H > MOE_MAX_HIDDEN_DISPATCH) return MOE_ERR_SHAPE;
+    switch (d->out_kind) {
+      case MOE_PAYLOAD_BF16:
+        if (H % 8) return MOE_ERR_SHAPE;
+        pb = 2 * H;
+        break;
+      case MOE_PAYLOAD_FP8_E4M3_B128:
+        if (H % 128) return MOE_ERR_SHAPE;
+        pb = H;
+        sb = H / 128 * 4;
+        break;
+      case MOE_PAYLOAD_NVFP4_B16:
+        if (H % 16) return MOE_ERR_SHAPE;
+        pb = H / 2;
+        sb = H / 16;
+        break;
+      default:
+        return MOE_ERR_INVALID_ARG;
+    }
+  } else {
+    return MOE_ERR_INVALID_ARG;
+  }
+  o->off_ids = 16;
+  o->off_weights = o->off_ids + pad16(4 * d->topk);
+  o->off_payload = o->off_weights + pad16(4 * d->topk);
+  o->off_scales = o->off_payload + pad16(pb);
+  o->record_bytes = o->off_scales + pad16(sb);
+  o->payload_bytes = pb;
+  o->scale_bytes = sb;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_strerror(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, kind or mode)";
+    case MOE_ERR_ALIGNMENT: return "pointer or segment not 16-byte aligned";
+    case MOE_ERR_SHAPE: return "shape outside the supported limits";
+    case MOE_ERR_CAPACITY: return "a caller buffer is too small";
+    case MOE_ERR_CUDA: return "a CUDA launch or copy failed";
+    case MOE_ERR_DEVICE_IDS: return "an expert id was outside [-1, num_experts)";
+    default: return "unknown status";
+  }
+}
+
+int moe_record_layout(const moe_desc_t* desc, moe_record_layout_t* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  return record_layout(desc, out);
+}
+
+size_t moe_workspace_size(const moe_desc_t* desc) {
+  if (check_desc(desc) != MOE_OK) return 0;
+  return moe::layout_workspace_bytes(desc->num_tokens, desc->num_experts, desc->num_ranks);
+}
+
+int moe_layout(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* tokens_per_expert,
+               int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
+               int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot, void* workspace,
+               size_t ws_bytes, moe_stream_t stream) {
+  int rc = check_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens, E = desc->num_experts, R = desc->num_ranks;
+  if (!tokens_per_expert || !tokens_per_rank || !expert_offset || !rank_offset || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!topk_idx || !is_token_in_rank || !slot_of)) return MOE_ERR_INVALID_ARG;
+  const void* ints[] = {topk_idx, tokens_per_expert, tokens_per_rank, expert_offset,
+                        rank_offset, slot_of, src_of_slot};
+  for (const void* q : ints)
+    if (!aligned(q, 4)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(workspace, 256)) return MOE_ERR_ALIGNMENT;
+  const size_t need = moe::layout_workspace_bytes(N, E, R);
+  if (ws_bytes < need) return MOE_ERR_CAPACITY;
+  cudaStream_t s = (cudaStream_t)stream;
+
+  uint8_t* ws = (uint8_t*)workspace;
+  if (N == 0) {  // nothing routed: zero counts and offsets
+    cudaError_t e = cudaMemsetAsync(tokens_per_expert, 0, (size_t)E * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(tokens_per_rank, 0, (size_t)R * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(expert_offset, 0, (size_t)(E + 1) * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(rank_offset, 0, (size_t)(R + 1) * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, 4, s);  // status = MOE_OK
+    return cuda_status(e);
+  }
+  moe::LayoutParams p;
+  p.topk_idx = topk_idx;
+  p.tokens_per_expert = tokens_per_expert;
+  p.tokens_per_rank = tokens_per_rank;
+  p.is_token_in_rank = is_token_in_rank;
+  p.expert_offset = expert_offset;
+  p.rank_offset = rank_offset;
+  p.slot_of = slot_of;
+  p.src_of_slot = src_of_slot;
+  p.num_tokens = N;
+  p.topk = desc->topk;
+  p.num_experts = E;
+  p.num_ranks = R;
+  p.experts_per_rank = E / R;
+  p.tokens_per_chunk = moe::kLayoutTokensPerChunk;
+  p.num_chunks = (N + moe::kLayoutTokensPerChunk - 1) / moe::kLayoutTokensPerChunk;
+  p.status = (int32_t*)ws;
+  p.chunk_hist = (int32_t*)(ws + 256);
+  p.chunk_rank = p.chunk_hist + (size_t)p.num_chunks * E;
+  p.chunk_flag = p.chunk_rank + (size_t)p.num_chunks * R;
+  return cuda_status(moe::launch_layout(p, s));
+}
+
+int moe_layout_status(const void* workspace, int32_t* status, moe_stream_t stream) {
+  if (!workspace || !status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t v = MOE_OK;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  *status = v;
+  return MOE_OK;
+}
+
+int moe_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* topk_weights,
+                 const void* hidden, const void* scales, const int32_t* slot_of, void* records,
+                 size_t records_bytes, moe_stream_t stream) {
+  moe_record_layout_t lay;
+  int rc = record_layout(desc, &lay);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens;
+  if (N == 0) return MOE_OK;
+  const bool raw = desc->out_kind == MOE_PAYLOAD_RAW;
+  if (!topk_idx || !topk_weights || !hidden || !slot_of || !records) return MOE_ERR_INVALID_ARG;
+  if (raw && lay.scale_bytes > 0 && !scales) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 4) || !aligned(topk_weights, 4) || !aligned(slot_of, 4))
+    return MOE_ERR_ALIGNMENT;
+  if (!aligned(hidden, 16) || !aligned(records, 16) || (raw && scales && !aligned(scales, 16)))
+    return MOE_ERR_ALIGNMENT;
+  if (records_bytes < (size_t)lay.record_bytes) return MOE_ERR_CAPACITY;
+  moe::DispatchParams p;
+  p.topk_idx = topk_idx;
+  p.topk_weights = topk_weights;
+  p.hidden = (const uint8_t*)hidden;
+  p.scales = (const uint8_t*)scales;
+  p.slot_of = slot_of;
+  p.records = (uint8_t*)records;
+  p.record_capacity = (int64_t)(records_bytes / (size_t)lay.record_bytes);
+  p.num_tokens = N;
+  p.topk = desc->topk;
+  p.hidden_size = desc->hidden;
+  p.in_row_bytes = raw ? desc->raw_payload_bytes : 2 * desc->hidden;
+  p.in_scale_bytes = raw ? desc->raw_scale_bytes : 0;
+  p.record_bytes = lay.record_bytes;
+  p.off_ids = lay.off_ids;
+  p.off_weights = lay.off_weights;
+  p.off_payload = lay.off_payload;
+  p.off_scales = lay.off_scales;
+  p.payload_bytes = lay.payload_bytes;
+  p.scale_bytes = lay.scale_bytes;
+  return cuda_status(moe::launch_dispatch(p, desc->in_kind, desc->out_kind, (cudaStream_t)stream));
+}
+
+int moe_combine(const moe_desc_t* desc, int mode, const void* expert_out, int64_t expert_out_rows,
+                const int32_t* topk_idx, const float* topk_weights, const int32_t* slot_of,
+                void* out, moe_stream_t stream) {
+  int rc = check_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens, H = desc->hidden, R = desc->num_ranks;
+  if (mode != MOE_COMBINE_TOPK && mode != MOE_COMBINE_RANKS && mode != MOE_COMBINE_TOPK_RANKS)
+    return MOE_ERR_INVALID_ARG;
+  if (H < 8 || H % 8) return MOE_ERR_SHAPE;
+  if (mode != MOE_COMBINE_TOPK && N % R) return MOE_ERR_SHAPE;
+  if ((int64_t)H / 8 > (int64_t)65535 * 128) return MOE_ERR_SHAPE;
+  if (N == 0) return MOE_OK;
+  if (!expert_out || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(expert_out, 16) || !aligned(out, 16)) return MOE_ERR_ALIGNMENT;
+  if (expert_out_rows < 0) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (mode == MOE_COMBINE_RANKS) {
+    if (expert_out_rows < (int64_t)R * N) return MOE_ERR_CAPACITY;
+    return cuda_status(moe::launch_combine_ranks((const uint8_t*)expert_out, (uint8_t*)out,
+                                                 (int64_t)N, H, R, s));
+  }
+  if (!topk_weights || !slot_of) return MOE_ERR_INVALID_ARG;
+  if (mode == MOE_COMBINE_TOPK_RANKS && !topk_idx) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_weights, 4) || !aligned(slot_of, 4) || !aligned(topk_idx, 4))
+    return MOE_ERR_ALIGNMENT;
+  moe::CombineParams p;
+  p.expert_out = (const uint8_t*)expert_out;
+  p.expert_out_rows = expert_out_rows;
+  p.topk_idx = topk_idx;
+  p.topk_weights = topk_weights;
+  p.slot_of = slot_of;
+  p.out = (uint8_t*)out;
+  p.num_tokens = N;
+  p.topk = desc->topk;
+  p.hidden_size = H;
+  p.num_ranks = R;
+  p.experts_per_rank = desc->num_experts / R;
+  p.group_by_rank = mode == MOE_COMBINE_TOPK_RANKS;
+  return cuda_status(moe::launch_combine_topk(p, s));
+}
+
+int moe_pack_record(const moe_desc_t* desc, int32_t src_token, int32_t slot_j, int32_t expert,
+                    const int32_t* ids_row, const float* w_row, const void* payload_row,
+                    const void* scales_row, void* record) {
+  moe_record_layout_t lay;
+  int rc = record_layout(desc, &lay);
+  if (rc != MOE_OK) return rc;
+  if (!ids_row || !w_row || !payload_row || !record) return MOE_ERR_INVALID_ARG;
+  if (lay.scale_bytes > 0 && !scales_row) return MOE_ERR_INVALID_ARG;
+  uint8_t* r = (uint8_t*)record;
+  memset(r, 0, (size_t)lay.record_bytes);
+  const int32_t hdr[4] = {src_token, slot_j, expert, 0};
+  memcpy(r, hdr, 16);
+  memcpy(r + lay.off_ids, ids_row, (size_t)desc->topk * 4);
+  memcpy(r + lay.off_weights, w_row, (size_t)desc->topk * 4);
+  memcpy(r + lay.off_payload, payload_row, (size_t)lay.payload_bytes);
+  if (lay.scale_bytes > 0) memcpy(r + lay.off_scales, scales_row, (size_t)lay.scale_bytes);
+  return MOE_OK;
+}
+
+int moe_unpack_record(const moe_desc_t* desc, const void* record, int32_t* src_token,
+                      int32_t* slot_j, int32_t* expert, int32_t* ids_row, float* w_row,
+                      void* payload_row, void* scales_row) {
+  moe_record_layout_t lay;
+  int rc = record_layout(desc, &lay);
+  if (rc != MOE_OK) return rc;
+  if (!record) return MOE_ERR_INVALID_ARG;
+  const uint8_t* r = (const uint8_t*)record;
+  int32_t hdr[4];
+  memcpy(hdr, r, 16);
+  if (src_token) *src_token = hdr[0];
+  if (slot_j) *slot_j = hdr[1];
+  if (expert) *expert = hdr[2];
+  if (ids_row) memcpy(ids_row, r + lay.off_ids, (size_t)desc->topk * 4);
+  if (w_row) memcpy(w_row, r + lay.off_weights, (size_t)desc->topk * 4);
+  if (payload_row) memcpy(payload_row, r + lay.off_payload, (size_t)lay.payload_bytes);
+  if (scales_row && lay.scale_bytes > 0) memcpy(scales_row, r + lay.off_scales, (size_t)lay.scale_bytes);
+  return MOE_OK;
+}
+
+}  // extern "C"

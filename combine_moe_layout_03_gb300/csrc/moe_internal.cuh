@@ -1,0 +1,190 @@
+// moe_internal.cuh -- device helpers and launcher declarations shared by the
+// CUDA translation units of libmoe.so. Internal: not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Launch parameter blocks (host fills, kernels read by value).
+// ---------------------------------------------------------------------------
+
+struct LayoutParams {
+  const int32_t* topk_idx;
+  int32_t* tokens_per_expert;
+  int32_t* tokens_per_rank;
+  uint8_t* is_token_in_rank;
+  int32_t* expert_offset;
+  int32_t* rank_offset;
+  int32_t* slot_of;
+  int32_t* src_of_slot;  // may be null
+  int32_t* status;       // workspace status word
+  int32_t* chunk_hist;   // [chunks][E] per-chunk expert counts
+  int32_t* chunk_rank;   // [chunks][R] per-chunk token-in-rank counts
+  int32_t* chunk_flag;   // [chunks] invalid-id flags
+  int num_tokens, topk, num_experts, num_ranks, experts_per_rank;
+  int tokens_per_chunk, num_chunks;
+};
+
+struct DispatchParams {
+  const int32_t* topk_idx;
+  const float* topk_weights;
+  const uint8_t* hidden;  // bf16 rows or raw payload rows
+  const uint8_t* scales;  // raw scale rows (RAW only)
+  const int32_t* slot_of;
+  uint8_t* records;
+  int64_t record_capacity;  // records the caller's buffer holds
+  int num_tokens, topk, hidden_size;
+  int in_row_bytes;   // bytes of one hidden row
+  int in_scale_bytes; // bytes of one raw scale row (RAW)
+  // record layout
+  int record_bytes, off_ids, off_weights, off_payload, off_scales, payload_bytes, scale_bytes;
+};
+
+struct CombineParams {
+  const uint8_t* expert_out;
+  int64_t expert_out_rows;
+  const int32_t* topk_idx;
+  const float* topk_weights;
+  const int32_t* slot_of;
+  uint8_t* out;
+  int num_tokens, topk, hidden_size, num_ranks, experts_per_rank;
+  int group_by_rank;  // 1: TOPK_RANKS, 0: TOPK
+};
+
+// Workspace carving shared by moe_workspace_size and moe_layout.
+constexpr int kLayoutTokensPerChunk = 128;
+constexpr int kSmallLayoutMaxPairs = 4096;
+size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s);
+cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, cudaStream_t s);
+cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s);
+cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t rows,
+                                 int hidden_size, int num_ranks, cudaStream_t s);
+
+#ifdef __CUDACC__
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+// 16-byte read-only streaming load: data read once, do not keep it in L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// BF16 <-> fp32. Widening is exact (BF16 is the top half of an fp32 pattern).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two fp32 -> packed BF16x2, round to nearest even (lo in bits 0-15).
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 -> packed e4m3x2, round to nearest even, saturating to +-448
+// (lo in bits 0-7).
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+// One e4m3 code -> its exact value (e4m3 values are exact in f16 and f32).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  uint32_t h2;
+  uint16_t in = (uint16_t)(code & 0xffu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(f)
+      : "r"(h2));
+  return f;
+}
+
+// Two fp32 -> packed e2m1x2 byte, round to nearest even, saturating to +-6
+// (lo in bits 0-3, hi in bits 4-7).
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Bulk asynchronous copy shared -> global (no tensor map). Both addresses
+// 16-byte aligned, size a multiple of 16. Tracked in the issuing thread's
+// bulk group.
+__device__ __forceinline__ void bulk_store_s2g(void* gdst, const void* ssrc, uint32_t bytes) {
+  uint32_t sa = (uint32_t)__cvta_generic_to_shared(ssrc);
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(sa),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the issuing thread's bulk copies have finished reading shared
+// memory (the shared buffer may then be reused or the block may exit).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Make generic-proxy writes to shared memory visible to the async proxy.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Inclusive warp scan of an int.
+__device__ __forceinline__ int warp_inclusive_scan(int v) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, v, o);
+    if ((int)lane_id() >= o) v += n;
+  }
+  return v;
+}
+
+// Exclusive prefix sum of the per-thread values v over the block (all threads
+// must call). scratch holds >= 33 ints of shared memory. Returns the
+// exclusive prefix; *total gets the block sum.
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  constexpr int NW = NT / 32;
+  const int warp = threadIdx.x >> 5;
+  int inc = warp_inclusive_scan(v);
+  if (lane_id() == 31) scratch[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane_id() < NW) ? scratch[lane_id()] : 0;
+    int wi = warp_inclusive_scan(w);
+    if (lane_id() < NW) scratch[lane_id()] = wi - w;
+    if (lane_id() == NW - 1) scratch[32] = wi;
+  }
+  __syncthreads();
+  int ex = scratch[warp] + inc - v;
+  *total = scratch[32];
+  __syncthreads();
+  return ex;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace moe

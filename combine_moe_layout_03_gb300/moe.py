@@ -1,0 +1,246 @@
+"""Thin Python binding of libmoe.so (include/moe.h) through ctypes.
+
+Argument marshalling only: every step of layout, dispatch and combine runs in
+the library's CUDA kernels. PyTorch supplies device memory and the current
+stream. There is no fallback: if libmoe.so is missing, importing this module
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_ALIGNMENT = -2
+MOE_ERR_SHAPE = -3
+MOE_ERR_CAPACITY = -4
+MOE_ERR_CUDA = -5
+MOE_ERR_DEVICE_IDS = -6
+
+MOE_PAYLOAD_BF16 = 0
+MOE_PAYLOAD_FP8_E4M3_B128 = 1
+MOE_PAYLOAD_NVFP4_B16 = 2
+MOE_PAYLOAD_RAW = 3
+
+MOE_COMBINE_TOPK = 0
+MOE_COMBINE_RANKS = 1
+MOE_COMBINE_TOPK_RANKS = 2
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"` "
+        "(there is no CPU fallback)")
+_lib = ctypes.CDLL(LIB_PATH)
+
+_i32, _i64, _sz, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [("num_tokens", _i32), ("topk", _i32), ("num_experts", _i32), ("num_ranks", _i32),
+                ("hidden", _i32), ("in_kind", _i32), ("out_kind", _i32),
+                ("raw_payload_bytes", _i32), ("raw_scale_bytes", _i32)]
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [("record_bytes", _i32), ("off_ids", _i32), ("off_weights", _i32),
+                ("off_payload", _i32), ("off_scales", _i32), ("payload_bytes", _i32),
+                ("scale_bytes", _i32)]
+
+
+_D = ctypes.POINTER(_Desc)
+_lib.moe_strerror.restype = ctypes.c_char_p
+_lib.moe_strerror.argtypes = [ctypes.c_int]
+_lib.moe_record_layout.restype = ctypes.c_int
+_lib.moe_record_layout.argtypes = [_D, ctypes.POINTER(_Layout)]
+_lib.moe_workspace_size.restype = _sz
+_lib.moe_workspace_size.argtypes = [_D]
+_lib.moe_layout.restype = ctypes.c_int
+_lib.moe_layout.argtypes = [_D] + [_vp] * 9 + [_sz, _vp]
+_lib.moe_layout_status.restype = ctypes.c_int
+_lib.moe_layout_status.argtypes = [_vp, ctypes.POINTER(_i32), _vp]
+_lib.moe_dispatch.restype = ctypes.c_int
+_lib.moe_dispatch.argtypes = [_D] + [_vp] * 6 + [_sz, _vp]
+_lib.moe_combine.restype = ctypes.c_int
+_lib.moe_combine.argtypes = [_D, ctypes.c_int, _vp, _i64, _vp, _vp, _vp, _vp, _vp]
+_lib.moe_pack_record.restype = ctypes.c_int
+_lib.moe_pack_record.argtypes = [_D, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
+_lib.moe_unpack_record.restype = ctypes.c_int
+_lib.moe_unpack_record.argtypes = [_D, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {moe_strerror(code)} ({code})")
+        self.code = code
+
+
+@dataclass
+class MoeDesc:
+    """Shape and format of one call (moe_desc_t)."""
+    num_tokens: int
+    topk: int
+    num_experts: int
+    num_ranks: int
+    hidden: int
+    in_kind: int = MOE_PAYLOAD_BF16
+    out_kind: int = MOE_PAYLOAD_BF16
+    raw_payload_bytes: int = 0
+    raw_scale_bytes: int = 0
+
+    def c(self) -> _Desc:
+        return _Desc(self.num_tokens, self.topk, self.num_experts, self.num_ranks, self.hidden,
+                     self.in_kind, self.out_kind, self.raw_payload_bytes, self.raw_scale_bytes)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return t.data_ptr() if t.numel() else None
+    return t
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc: int, what: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, what)
+
+
+def moe_strerror(code: int) -> str:
+    return _lib.moe_strerror(int(code)).decode()
+
+
+def moe_record_layout(desc: MoeDesc) -> dict:
+    lay = _Layout()
+    _check(_lib.moe_record_layout(ctypes.byref(desc.c()), ctypes.byref(lay)), "moe_record_layout")
+    return {name: getattr(lay, name) for name, _ in _Layout._fields_}
+
+
+def moe_workspace_size(desc: MoeDesc) -> int:
+    return int(_lib.moe_workspace_size(ctypes.byref(desc.c())))
+
+
+def layout_outputs(desc: MoeDesc, device) -> dict:
+    """Allocates the output tensors of moe_layout (torch device memory)."""
+    n, k, e, r = desc.num_tokens, desc.topk, desc.num_experts, desc.num_ranks
+    i32 = dict(dtype=torch.int32, device=device)
+    return dict(
+        tokens_per_expert=torch.empty(e, **i32),
+        tokens_per_rank=torch.empty(r, **i32),
+        is_token_in_rank=torch.empty((n, r), dtype=torch.uint8, device=device),
+        expert_offset=torch.empty(e + 1, **i32),
+        rank_offset=torch.empty(r + 1, **i32),
+        slot_of=torch.empty((n, k), **i32),
+        src_of_slot=torch.empty(n * k, **i32),
+    )
+
+
+def moe_layout(desc: MoeDesc, topk_idx: torch.Tensor, out: dict | None = None,
+               workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Routing layout (see include/moe.h). Returns the dict of output tensors
+    (plus 'workspace')."""
+    if out is None:
+        out = layout_outputs(desc, topk_idx.device)
+    if workspace is None:
+        workspace = torch.empty(max(moe_workspace_size(desc), 256), dtype=torch.uint8,
+                                device=topk_idx.device)
+    rc = _lib.moe_layout(ctypes.byref(desc.c()), _ptr(topk_idx), _ptr(out["tokens_per_expert"]),
+                         _ptr(out["tokens_per_rank"]), _ptr(out["is_token_in_rank"]),
+                         _ptr(out["expert_offset"]), _ptr(out["rank_offset"]),
+                         _ptr(out["slot_of"]), _ptr(out.get("src_of_slot")), _ptr(workspace),
+                         workspace.numel(), _stream(stream))
+    _check(rc, "moe_layout")
+    out["workspace"] = workspace
+    return out
+
+
+def moe_layout_status(workspace: torch.Tensor, stream=None) -> int:
+    """Status word of the last moe_layout on this workspace (synchronises)."""
+    v = _i32(0)
+    _check(_lib.moe_layout_status(_ptr(workspace), ctypes.byref(v), _stream(stream)),
+           "moe_layout_status")
+    return v.value
+
+
+def moe_dispatch(desc: MoeDesc, topk_idx: torch.Tensor, topk_weights: torch.Tensor,
+                 hidden: torch.Tensor, scales: torch.Tensor | None, slot_of: torch.Tensor,
+                 records: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Permute and pack: writes one record per routed pair into `records`
+    (uint8 [N*k, record_bytes] when allocated here)."""
+    lay = moe_record_layout(desc)
+    if records is None:
+        records = torch.empty((desc.num_tokens * desc.topk, lay["record_bytes"]),
+                              dtype=torch.uint8, device=topk_idx.device)
+    nbytes = records.numel() * records.element_size()
+    rc = _lib.moe_dispatch(ctypes.byref(desc.c()), _ptr(topk_idx), _ptr(topk_weights),
+                           _ptr(hidden), _ptr(scales), _ptr(slot_of), _ptr(records), nbytes,
+                           _stream(stream))
+    _check(rc, "moe_dispatch")
+    return records
+
+
+def moe_combine(desc: MoeDesc, mode: int, expert_out: torch.Tensor,
+                topk_idx: torch.Tensor | None, topk_weights: torch.Tensor | None,
+                slot_of: torch.Tensor | None, out: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """Combine (see include/moe.h): returns bf16 [N, H]."""
+    if out is None:
+        out = torch.empty((desc.num_tokens, desc.hidden), dtype=torch.bfloat16,
+                          device=expert_out.device)
+    rows = expert_out.numel() // max(desc.hidden, 1)
+    rc = _lib.moe_combine(ctypes.byref(desc.c()), int(mode), _ptr(expert_out), rows,
+                          _ptr(topk_idx), _ptr(topk_weights), _ptr(slot_of), _ptr(out),
+                          _stream(stream))
+    _check(rc, "moe_combine")
+    return out
+
+
+def moe_pack_record(desc: MoeDesc, src_token: int, slot_j: int, expert: int, ids_row, w_row,
+                    payload_row, scales_row):
+    """Host-only: builds one record (numpy uint8) from host numpy rows."""
+    import numpy as np
+    lay = moe_record_layout(desc)
+    rec = np.zeros(lay["record_bytes"], dtype=np.uint8)
+    arrs = [np.ascontiguousarray(a) if a is not None else None
+            for a in (ids_row, w_row, payload_row, scales_row)]
+    p = [a.ctypes.data if a is not None else None for a in arrs]
+    _check(_lib.moe_pack_record(ctypes.byref(desc.c()), src_token, slot_j, expert, p[0], p[1],
+                                p[2], p[3], rec.ctypes.data), "moe_pack_record")
+    return rec
+
+
+def moe_unpack_record(desc: MoeDesc, record):
+    """Host-only: splits one record (numpy uint8) into its fields."""
+    import numpy as np
+    lay = moe_record_layout(desc)
+    rec = np.ascontiguousarray(record, dtype=np.uint8)
+    t, j, e = _i32(), _i32(), _i32()
+    ids = np.zeros(desc.topk, np.int32)
+    w = np.zeros(desc.topk, np.float32)
+    pay = np.zeros(lay["payload_bytes"], np.uint8)
+    sc = np.zeros(lay["scale_bytes"], np.uint8)
+    _check(_lib.moe_unpack_record(ctypes.byref(desc.c()), rec.ctypes.data, ctypes.byref(t),
+                                  ctypes.byref(j), ctypes.byref(e), ids.ctypes.data,
+                                  w.ctypes.data, pay.ctypes.data,
+                                  sc.ctypes.data if sc.size else None),
+           "moe_unpack_record")
+    return dict(src_token=t.value, slot_j=j.value, expert=e.value, ids=ids, weights=w,
+                payload=pay, scales=sc)
+
+
+def exported_symbols() -> list[str]:
+    return ["moe_strerror", "moe_record_layout", "moe_workspace_size", "moe_layout",
+            "moe_layout_status", "moe_dispatch", "moe_combine", "moe_pack_record",
+            "moe_unpack_record"]

@@ -1,0 +1,231 @@
+/*
+ * moe.h -- C ABI of libmoe.so: MoE token dispatch and combine on one GPU.
+ *
+ * The library computes the data-parallel hot path of Mixture-of-Experts token
+ * routing with expert-parallel ranks emulated as R regions of one GPU's
+ * memory:
+ *
+ *   moe_layout    routing layout: per-expert and per-rank counts, prefix
+ *                 offsets, the token-in-rank mask and a stable slot map
+ *                 (DeepEP repository, csrc/deep_ep.cpp,
+ *                 Buffer::get_dispatch_layout);
+ *   moe_dispatch  one 16-byte-aligned record per (token, top-k) pair, grouped
+ *                 by destination rank and expert, with the payload optionally
+ *                 quantised to FP8 e4m3 per 128 channels or NVFP4 per 16
+ *                 (DeepEP csrc/config.hpp LowLatencyLayout message: int4
+ *                 header + payload + scales; Buffer::low_latency_dispatch
+ *                 FP8 cast; vLLM compare view ds-exp-2...ds-exp-ag,
+ *                 moe_allgather.cu "Host launcher": tensors packed at
+ *                 16-byte-aligned offsets);
+ *   moe_combine   the top-k weighted BF16 reduction back to token order and
+ *                 the cross-rank sum a reduce-scatter performs (DeepEP
+ *                 Buffer::low_latency_combine; ds-exp-ag moe_reduce_scatter.cu
+ *                 "Lamport reduce-scatter kernel" phase 3; vLLM PR
+ *                 "Eliminate staging from NCCL symmetric reduce-scatter",
+ *                 Implementation).
+ *
+ * Conventions
+ *  - Every function returns an int status: MOE_OK (0) or a negative MOE_ERR_*
+ *    code; moe_strerror() names it. Nothing throws, aborts or traps. Argument
+ *    errors are found on the host before anything is launched.
+ *  - All buffers belong to the caller. Device pointers are allocated and freed
+ *    by the caller; the library allocates nothing, keeps no state between
+ *    calls and never synchronises the stream (except moe_layout_status, which
+ *    says so). Work is enqueued on the caller's stream.
+ *  - moe_stream_t is a cudaStream_t passed as void*; NULL is the legacy
+ *    default stream.
+ *  - Integers in records are little-endian.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1) /* NULL pointer, bad kind or mode, size < needed */
+#define MOE_ERR_ALIGNMENT (-2)   /* pointer or segment not 16-byte aligned */
+#define MOE_ERR_SHAPE (-3)       /* shape outside the supported limits below */
+#define MOE_ERR_CAPACITY (-4)    /* a caller buffer is too small */
+#define MOE_ERR_CUDA (-5)        /* a CUDA launch or copy failed */
+#define MOE_ERR_DEVICE_IDS (-6)  /* (from moe_layout_status) an id was outside [-1, E) */
+
+typedef void* moe_stream_t;
+
+/* ---- payload kinds ------------------------------------------------------- */
+/* What the caller's hidden rows are (in_kind) and what records carry
+ * (out_kind). Valid pairs: (BF16, BF16), (BF16, FP8_E4M3_B128),
+ * (BF16, NVFP4_B16), (RAW, RAW). */
+#define MOE_PAYLOAD_BF16 0          /* bf16 [H] per token, H*2 bytes */
+#define MOE_PAYLOAD_FP8_E4M3_B128 1 /* e4m3 [H] + fp32 scale per 128 channels */
+#define MOE_PAYLOAD_NVFP4_B16 2     /* e2m1 [H/2 bytes] + e4m3 scale byte per 16 */
+#define MOE_PAYLOAD_RAW 3           /* opaque bytes copied as they are */
+
+/* ---- combine modes -------------------------------------------------------- */
+#define MOE_COMBINE_TOPK 0       /* top-k weighted reduction to token order */
+#define MOE_COMBINE_RANKS 1      /* cross-rank sum of R BF16 partials */
+#define MOE_COMBINE_TOPK_RANKS 2 /* top-k reduction grouped by rank, then summed */
+
+/* ---- limits ----------------------------------------------------------------- */
+#define MOE_MAX_TOPK 32
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_RANKS 64
+#define MOE_MAX_HIDDEN_DISPATCH 16384 /* BF16/FP8/NVFP4 dispatch */
+#define MOE_MAX_RAW_BYTES 65536       /* RAW payload and scale bytes each */
+
+/* Shape and format of one call. num_tokens N >= 0; topk k in [1, 32];
+ * num_experts E in [1, 1024]; num_ranks R in [1, 64] with E % R == 0; expert e
+ * lives on rank e / (E/R) (DeepEP Buffer::low_latency_dispatch: E % R == 0,
+ * E/R local experts per rank). N * k < 2^31.
+ * hidden H: channels per token. BF16 rows need H % 8 == 0 (16-byte rows);
+ * FP8 needs H % 128 == 0; NVFP4 needs H % 32 == 0 (16-byte packed rows).
+ * For RAW, raw_payload_bytes and raw_scale_bytes are the bytes per token of
+ * the caller's two tensors; each must be a multiple of 16 (ds-exp-ag
+ * moe_allgather.cu make_desc rejects other sizes) and <= MOE_MAX_RAW_BYTES;
+ * raw_scale_bytes may be 0 (no scales). H is then only informational. */
+typedef struct {
+  int32_t num_tokens;
+  int32_t topk;
+  int32_t num_experts;
+  int32_t num_ranks;
+  int32_t hidden;
+  int32_t in_kind;
+  int32_t out_kind;
+  int32_t raw_payload_bytes;
+  int32_t raw_scale_bytes;
+} moe_desc_t;
+
+/* Byte layout of one record. Every offset and record_bytes is a multiple of
+ * 16; padding bytes are zero.
+ *   [0, 16)                 header: int32 src_token, int32 j, int32 expert, int32 0
+ *   [off_ids, +4k)          the token's whole top-k id row (int32)
+ *   [off_weights, +4k)      the token's fp32 weight row
+ *   [off_payload, +payload_bytes)  BF16 row | e4m3 bytes | packed e2m1 | raw
+ *   [off_scales, +scale_bytes)     none | fp32 per 128 | e4m3 byte per 16 | raw
+ * NVFP4 packing: byte i holds element 2i in bits 0-3 and element 2i+1 in bits
+ * 4-7; e2m1 code = sign << 3 | magnitude index into {0,.5,1,1.5,2,3,4,6}. */
+typedef struct {
+  int32_t record_bytes;
+  int32_t off_ids;
+  int32_t off_weights;
+  int32_t off_payload;
+  int32_t off_scales;
+  int32_t payload_bytes;
+  int32_t scale_bytes;
+} moe_record_layout_t;
+
+/* Text for a status code (static storage, never NULL). */
+const char* moe_strerror(int status);
+
+/* Host only. Fills *out for the record format of desc. Errors:
+ * INVALID_ARG (NULL, bad kind pair), SHAPE (limits above). */
+int moe_record_layout(const moe_desc_t* desc, moe_record_layout_t* out);
+
+/* Host only. Bytes of device scratch that moe_layout needs for desc (0 if desc
+ * is invalid). The workspace must be 256-byte aligned. Its contents need no
+ * initialisation and are meaningful only to the library; the status word of
+ * the last moe_layout call lives in it. */
+size_t moe_workspace_size(const moe_desc_t* desc);
+
+/* Routing layout (DeepEP Buffer::get_dispatch_layout outputs plus the slot
+ * map of the pairs; -1 ids mean "no expert", as vLLM's mask_topk_ids writes
+ * for padded tokens on the ds-exp-ag page).
+ * Inputs (device): topk_idx int32 [N, k], row-major.
+ * Outputs (device, caller-allocated, fully written):
+ *   tokens_per_expert int32 [E]   pairs routed to each expert
+ *   tokens_per_rank   int32 [R]   tokens with at least one pair on the rank
+ *   is_token_in_rank  uint8 [N,R] 1/0
+ *   expert_offset     int32 [E+1] exclusive prefix sum of tokens_per_expert;
+ *                                 expert_offset[E] = P, the number of records
+ *   rank_offset       int32 [R+1] expert_offset[r * E/R]; rank r's records are
+ *                                 slots [rank_offset[r], rank_offset[r+1])
+ *   slot_of           int32 [N,k] record slot of pair (t, j), -1 for id -1.
+ *                                 Inside an expert's region slots follow
+ *                                 ascending (t, j): a stable counting sort.
+ *   src_of_slot       int32 [N*k] t*k+j of the pair in slot s, -1 for s >= P.
+ *                                 May be NULL.
+ * workspace: device, >= moe_workspace_size(desc) bytes, 256-byte aligned.
+ * An id outside [-1, E) is treated as -1 and recorded in the workspace's
+ * status word; read it with moe_layout_status. All int pointers must be
+ * 4-byte aligned. Errors: INVALID_ARG, SHAPE, ALIGNMENT, CAPACITY (ws_bytes),
+ * CUDA. */
+int moe_layout(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* tokens_per_expert,
+               int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
+               int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot, void* workspace,
+               size_t ws_bytes, moe_stream_t stream);
+
+/* Copies the status word of the last moe_layout that used this workspace to
+ * *status (MOE_OK or MOE_ERR_DEVICE_IDS) after synchronising the stream.
+ * This is the only call that waits for the device. Errors: INVALID_ARG, CUDA. */
+int moe_layout_status(const void* workspace, int32_t* status, moe_stream_t stream);
+
+/* Permute and pack (dispatch). For every pair (t, j) with slot_of[t, j] >= 0
+ * writes one record (moe_record_layout) to
+ * records + slot_of[t, j] * record_bytes. The payload of a token is computed
+ * once and copied into each of its records.
+ * Inputs (device): topk_idx int32 [N,k]; topk_weights fp32 [N,k];
+ *   hidden: bf16 [N,H] (in_kind BF16) or uint8 [N, raw_payload_bytes] (RAW);
+ *   scales: uint8 [N, raw_scale_bytes] for RAW with raw_scale_bytes > 0, else
+ *   ignored (may be NULL); slot_of int32 [N,k] from moe_layout.
+ * Output (device): records, at least P * record_bytes bytes
+ *   (records_bytes says how many the caller has; N*k*record_bytes is always
+ *   enough). Slots not named by slot_of are not touched.
+ * FP8 per 128 channels (the pages give no formula; reading): amax = max|x|,
+ *   a = max(amax, 1e-4), scale = a/448, q = e4m3_rn_satfinite(x * (448/a)),
+ *   both divisions IEEE fp32; stored scale is fp32.
+ * NVFP4 per 16 (reading, no global scale): sc = e4m3_rn_satfinite(amax/6),
+ *   d = value(sc), q = d == 0 ? 0 : e2m1_rn_satfinite(x / d).
+ * hidden, scales and records must be 16-byte aligned. Errors: INVALID_ARG,
+ * SHAPE, ALIGNMENT, CAPACITY, CUDA. */
+int moe_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* topk_weights,
+                 const void* hidden, const void* scales, const int32_t* slot_of, void* records,
+                 size_t records_bytes, moe_stream_t stream);
+
+/* Combine.
+ * MOE_COMBINE_TOPK: expert_out bf16 [P, H] holds the expert outputs in slot
+ *   order; out bf16 [N, H] with
+ *     out[t] = bf16_rn( fp32 fma chain over j ascending, slot_of[t,j] >= 0,
+ *                       of topk_weights[t,j] * expert_out[slot_of[t,j]] )
+ *   (fp32 accumulation and round-to-nearest-even BF16 output as in the
+ *   ds-exp-ag reduce-scatter; ascending j is the reading taken).
+ *   topk_idx may be NULL.
+ * MOE_COMBINE_RANKS: expert_out bf16 [R][N][H] holds R partials; out bf16
+ *   [N, H] = bf16_rn(sum over r ascending of float(partial_r)), fp32
+ *   accumulation; rank q's reduce-scatter output is rows [qN/R, (q+1)N/R).
+ *   Needs N % R == 0. topk_idx, topk_weights, slot_of may be NULL.
+ * MOE_COMBINE_TOPK_RANKS: as TOPK, but for each rank r (ascending) the fp32
+ *   partial over the pairs whose expert lives on rank r (fma chain, ascending
+ *   j) is formed first and the partials are summed in fp32, ascending r, with
+ *   one BF16 rounding at the end. Needs N % R == 0 and topk_idx.
+ * expert_out and out must be 16-byte aligned; H % 8 == 0. expert_out_rows is
+ *   the number of rows the caller's expert_out holds (P for the TOPK modes,
+ *   R*N for RANKS); a slot outside it is a caller error that the kernels
+ *   skip. Errors: INVALID_ARG, SHAPE, ALIGNMENT, CAPACITY, CUDA. */
+int moe_combine(const moe_desc_t* desc, int mode, const void* expert_out, int64_t expert_out_rows,
+                const int32_t* topk_idx, const float* topk_weights, const int32_t* slot_of,
+                void* out, moe_stream_t stream);
+
+/* Host only: builds one record in host memory `record` (record_bytes bytes)
+ * from host rows: ids_row int32 [k], w_row fp32 [k], payload_row
+ * (payload_bytes, already in the out_kind format), scales_row (scale_bytes,
+ * may be NULL when scale_bytes is 0). Padding is zeroed. Errors: INVALID_ARG,
+ * SHAPE. */
+int moe_pack_record(const moe_desc_t* desc, int32_t src_token, int32_t slot_j, int32_t expert,
+                    const int32_t* ids_row, const float* w_row, const void* payload_row,
+                    const void* scales_row, void* record);
+
+/* Host only: the inverse of moe_pack_record. Any output pointer may be NULL to
+ * skip that field. Errors: INVALID_ARG, SHAPE. */
+int moe_unpack_record(const moe_desc_t* desc, const void* record, int32_t* src_token,
+                      int32_t* slot_j, int32_t* expert, int32_t* ids_row, float* w_row,
+                      void* payload_row, void* scales_row);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */
