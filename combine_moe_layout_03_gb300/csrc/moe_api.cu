@@ -83,6 +83,7 @@ const char* moe_strerror(int status) {
     case MOE_ERR_CAPACITY: return "a caller buffer is too small";
     case MOE_ERR_CUDA: return "a CUDA launch or copy failed";
     case MOE_ERR_DEVICE_IDS: return "an expert id was outside [-1, num_experts)";
+    case MOE_ERR_TOO_LARGE: return "shape needs more scratch than moe_layout_noalloc's fixed array";
     default: return "unknown status";
   }
 }

@@ -23,6 +23,8 @@ MOE_ERR_SHAPE = -3
 MOE_ERR_CAPACITY = -4
 MOE_ERR_CUDA = -5
 MOE_ERR_DEVICE_IDS = -6
+MOE_ERR_TOO_LARGE = -7
+MOE_NOALLOC_SCRATCH_BYTES = 2 << 20
 
 MOE_PAYLOAD_BF16 = 0
 MOE_PAYLOAD_FP8_E4M3_B128 = 1
@@ -63,6 +65,8 @@ _lib.moe_workspace_size.restype = _sz
 _lib.moe_workspace_size.argtypes = [_D]
 _lib.moe_layout.restype = ctypes.c_int
 _lib.moe_layout.argtypes = [_D] + [_vp] * 9 + [_sz, _vp]
+_lib.moe_layout_noalloc.restype = ctypes.c_int
+_lib.moe_layout_noalloc.argtypes = [_D] + [_vp] * 10
 _lib.moe_layout_status.restype = ctypes.c_int
 _lib.moe_layout_status.argtypes = [_vp, ctypes.POINTER(_i32), _vp]
 _lib.moe_dispatch.restype = ctypes.c_int
@@ -166,6 +170,24 @@ def moe_layout(desc: MoeDesc, topk_idx: torch.Tensor, out: dict | None = None,
     return out
 
 
+def moe_layout_noalloc(desc: MoeDesc, topk_idx: torch.Tensor, out: dict | None = None,
+                       status: torch.Tensor | None = None, stream=None) -> dict:
+    """Routing layout without a workspace, for callers that cannot provide
+    device scratch: the library uses its own fixed 2 MiB device array instead
+    (see include/moe.h for the size limit and the rule that calls overlapping
+    on the GPU race). `status` (int32 [1] on the device) receives this call's
+    status word."""
+    if out is None:
+        out = layout_outputs(desc, topk_idx.device)
+    rc = _lib.moe_layout_noalloc(ctypes.byref(desc.c()), _ptr(topk_idx),
+                                 _ptr(out["tokens_per_expert"]), _ptr(out["tokens_per_rank"]),
+                                 _ptr(out["is_token_in_rank"]), _ptr(out["expert_offset"]),
+                                 _ptr(out["rank_offset"]), _ptr(out["slot_of"]),
+                                 _ptr(out.get("src_of_slot")), _ptr(status), _stream(stream))
+    _check(rc, "moe_layout_noalloc")
+    return out
+
+
 def moe_layout_status(workspace: torch.Tensor, stream=None) -> int:
     """Status word of the last moe_layout on this workspace (synchronises)."""
     v = _i32(0)
@@ -243,4 +265,4 @@ def moe_unpack_record(desc: MoeDesc, record):
 def exported_symbols() -> list[str]:
     return ["moe_strerror", "moe_record_layout", "moe_workspace_size", "moe_layout",
             "moe_layout_status", "moe_dispatch", "moe_combine", "moe_pack_record",
-            "moe_unpack_record"]
+            "moe_unpack_record", "moe_layout_noalloc"]

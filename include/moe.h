@@ -54,6 +54,7 @@ extern "C" {
 #define MOE_ERR_CAPACITY (-4)    /* a caller buffer is too small */
 #define MOE_ERR_CUDA (-5)        /* a CUDA launch or copy failed */
 #define MOE_ERR_DEVICE_IDS (-6)  /* (from moe_layout_status) an id was outside [-1, E) */
+#define MOE_ERR_TOO_LARGE (-7)   /* moe_layout_noalloc: the shape needs more scratch than it has */
 
 typedef void* moe_stream_t;
 
@@ -209,6 +210,35 @@ int moe_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* t
 int moe_combine(const moe_desc_t* desc, int mode, const void* expert_out, int64_t expert_out_rows,
                 const int32_t* topk_idx, const float* topk_weights, const int32_t* slot_of,
                 void* out, moe_stream_t stream);
+
+/* Allocation-free routing layout. The pages have no counterpart to this entry
+ * point: it is the same computation as moe_layout for callers that cannot
+ * give the library device memory for scratch -- for example a plugin inside a
+ * host program that owns every device allocation through its own pool, or a
+ * service that fixes its device footprint at start-up and must not call
+ * cudaMalloc afterwards.
+ * Instead of a workspace it uses a fixed array of MOE_NOALLOC_SCRATCH_BYTES
+ * (2 MiB) inside the library's device image. That array exists on every GPU
+ * that loads the library and is held until the process exits. The call
+ * allocates nothing.
+ * Arguments and outputs are those of moe_layout, without workspace and
+ * ws_bytes. status (device int32, may be NULL) receives MOE_OK or
+ * MOE_ERR_DEVICE_IDS for this call, written on the stream.
+ * Limit: the layout needs 256 + ceil(N/128) * (E + R + 1) * 4 bytes of
+ * scratch (moe_workspace_size); larger shapes return MOE_ERR_TOO_LARGE. For
+ * E = 256, R = 8 that allows N up to about 253,000 tokens.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call shares the one array and overwrites
+ * what it reads, so nothing needs clearing, but calls that overlap on the GPU
+ * (different streams, or unordered host threads) race on it.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, TOO_LARGE, CUDA. */
+#define MOE_NOALLOC_SCRATCH_BYTES (2u << 20)
+int moe_layout_noalloc(const moe_desc_t* desc, const int32_t* topk_idx,
+                       int32_t* tokens_per_expert, int32_t* tokens_per_rank,
+                       uint8_t* is_token_in_rank, int32_t* expert_offset, int32_t* rank_offset,
+                       int32_t* slot_of, int32_t* src_of_slot, int32_t* status,
+                       moe_stream_t stream);
 
 /* Host only: builds one record in host memory `record` (record_bytes bytes)
  * from host rows: ids_row int32 [k], w_row fp32 [k], payload_row

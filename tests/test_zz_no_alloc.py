@@ -1,0 +1,88 @@
+"""moe_layout_noalloc, the routing layout for callers that cannot allocate.
+
+Some callers of this library cannot give it device scratch memory: a plugin
+inside a host program that owns every device allocation through its own pool
+and forbids direct cudaMalloc, or a service that fixes its device footprint at
+start-up. moe_layout_noalloc serves them with a fixed scratch array inside the
+library's device image instead of a caller workspace.
+
+These tests call it through the C ABI (ctypes, no binding helper) twice in a
+row on different inputs -- so the second call runs on scratch the first one
+left behind -- and compare every output with the existing moe_layout's,
+exactly, since all layout outputs are integers. The file is named to be
+collected last; it also passes when run alone in a fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from combine_moe_layout_03_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+KEYS = ("tokens_per_expert", "tokens_per_rank", "is_token_in_rank", "expert_offset",
+        "rank_offset", "slot_of", "src_of_slot")
+
+
+def _noalloc(moe, desc, ids):
+    out = moe.layout_outputs(desc, ids.device)
+    for t in out.values():
+        t.fill_(0x55)  # stale values the call must overwrite
+    status = torch.full((1,), 12345, dtype=torch.int32, device=ids.device)
+    rc = moe._lib.moe_layout_noalloc(
+        ctypes.byref(desc.c()), ids.data_ptr(), out["tokens_per_expert"].data_ptr(),
+        out["tokens_per_rank"].data_ptr(), out["is_token_in_rank"].data_ptr(),
+        out["expert_offset"].data_ptr(), out["rank_offset"].data_ptr(), out["slot_of"].data_ptr(),
+        out["src_of_slot"].data_ptr(), status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == moe.MOE_OK, moe.moe_strerror(rc)
+    return out, status
+
+
+def _compare(moe, desc, ids):
+    got, status = _noalloc(moe, desc, ids)
+    ref = moe.moe_layout(desc, ids)  # the existing entry point, with its own workspace
+    torch.cuda.synchronize()
+    for key in KEYS:
+        assert torch.equal(got[key], ref[key]), key
+    return int(status.item()), int(moe.moe_layout_status(ref["workspace"]))
+
+
+def test_noalloc_matches_moe_layout_on_two_calls_in_a_row():
+    from combine_moe_layout_03_gb300 import moe
+    dev = torch.device("cuda:0")
+    # call 1: prefill routing (multi-block path, 32 chunks of scratch)
+    c = synth.prefill_case(seed=11)
+    ids = torch.from_numpy(c["topk_idx"]).to(dev)
+    st, ref_st = _compare(moe, moe.MoeDesc(4096, 8, 256, 8, 7168), ids)
+    assert st == ref_st == moe.MOE_OK
+    # call 2, right after, on a ragged shape with padding ids and fewer chunks
+    g = np.random.default_rng(12)
+    ids2 = g.integers(-1, 64, size=(1000, 6)).astype(np.int32)
+    st, ref_st = _compare(moe, moe.MoeDesc(1000, 6, 64, 4, 8), torch.from_numpy(ids2).to(dev))
+    assert st == ref_st == moe.MOE_OK
+
+
+def test_noalloc_status_and_small_path():
+    from combine_moe_layout_03_gb300 import moe
+    dev = torch.device("cuda:0")
+    ids = synth.decode_case(seed=3, n=64)["topk_idx"].copy()
+    ids[5, 1] = 300  # outside [-1, E): reported, treated as -1
+    st, ref_st = _compare(moe, moe.MoeDesc(64, 8, 256, 8, 8), torch.from_numpy(ids).to(dev))
+    assert st == ref_st == moe.MOE_ERR_DEVICE_IDS
+    ids[5, 1] = 7
+    st, ref_st = _compare(moe, moe.MoeDesc(64, 8, 256, 8, 8), torch.from_numpy(ids).to(dev))
+    assert st == ref_st == moe.MOE_OK
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    from combine_moe_layout_03_gb300 import moe
+    n = 300_000  # needs about 2.4 MiB of scratch at E=256, R=8
+    desc = moe.MoeDesc(n, 8, 256, 8, 8)
+    assert moe.moe_workspace_size(desc) > moe.MOE_NOALLOC_SCRATCH_BYTES
+    rc = moe._lib.moe_layout_noalloc(ctypes.byref(desc.c()), 16, 16, 16, 16, 16, 16, 16, None,
+                                     None, None)
+    assert rc == moe.MOE_ERR_TOO_LARGE
+    ok = moe.MoeDesc(250_000, 8, 256, 8, 8)
+    assert moe.moe_workspace_size(ok) <= moe.MOE_NOALLOC_SCRATCH_BYTES
