@@ -13,27 +13,25 @@
 //   kernel" phase 3: fp32 accumulation over ranks in ascending order, one
 //   BF16 round-to-nearest-even).
 //
-// Design: HBM-bound gathers. A block of 128 threads covers one token and
-// 128 16-byte column chunks of it (grid.y walks the hidden dimension), so
-// every thread owns 8 columns. A thread first issues the loads of all its
-// pairs' rows (up to 8 at a time, read-only, no L1 allocation: each expert
-// row is read exactly once), then runs the fp32 fma chain in the fixed
-// order. No shared-memory staging: each loaded byte is used once.
+// Design: HBM-bound gathers. The work is cut into units of (token, slice of
+// its 16-byte column chunks); one warp owns one unit at a time and walks the
+// units of a persistent grid sized to the SMs (grid-stride over units). For
+// its unit the warp loads the token's k (slot, weight, expert) with lanes
+// 0..k-1, orders the valid pairs by (rank, j) with warp shuffles (no block
+// barrier, no serial thread), and keeps the ordered list spread across the
+// lanes. Each lane then owns one 16-byte column chunk per step: it issues the
+// loads of up to 8 expert rows at once (read-only, no L1 allocation: every
+// expert row is read exactly once) and runs the fp32 fma chain in the fixed
+// order. The next unit's pair info is fetched while the current unit
+// streams, so its latency is hidden.
 #include "moe_internal.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kCombineThreads = 128;
-constexpr int kBatch = 8;  // rows in flight per thread
-
-struct PairOrder {
-  int slot[MOE_MAX_TOPK];
-  float w[MOE_MAX_TOPK];
-  int last[MOE_MAX_TOPK];  // 1 if this pair closes its rank group
-  int n;
-};
+constexpr int kCombineWarps = 8;  // 256 threads per block
+constexpr int kBatch = 8;         // expert rows in flight per lane
 
 __device__ __forceinline__ void fma8(float* acc, float w, uint4 v) {
   acc[0] = __fmaf_rn(w, bf16_lo(v.x), acc[0]);
@@ -46,75 +44,116 @@ __device__ __forceinline__ void fma8(float* acc, float w, uint4 v) {
   acc[7] = __fmaf_rn(w, bf16_hi(v.w), acc[7]);
 }
 
-__global__ void __launch_bounds__(kCombineThreads) k_combine_topk(CombineParams p) {
-  __shared__ PairOrder po;
-  const int t = blockIdx.x;
+__device__ __forceinline__ uint4 pack8(const float* a) {
+  uint4 o;
+  o.x = pack_bf16x2_rn(a[0], a[1]);
+  o.y = pack_bf16x2_rn(a[2], a[3]);
+  o.z = pack_bf16x2_rn(a[4], a[5]);
+  o.w = pack_bf16x2_rn(a[6], a[7]);
+  return o;
+}
+
+// GROUP = false: out = bf16(fma chain over j ascending)            (TOPK)
+// GROUP = true:  out = bf16(sum over ranks ascending of the rank's
+//                fma chain over its pairs, j ascending)             (TOPK_RANKS)
+template <bool GROUP>
+__global__ void __launch_bounds__(kCombineWarps * 32, 3)
+    k_combine_topk(CombineParams p, int units_per_token, int chunks_per_unit, int64_t num_units) {
+  const int lane = (int)lane_id();
   const int k = p.topk;
-  if (threadIdx.x == 0) {
-    // Valid pairs sorted by (rank, j) when grouping by rank, else by j: an
-    // insertion sort of at most 32 keys. A pair closes its group when the
-    // next pair has another rank (always true for the last pair).
-    int key[MOE_MAX_TOPK];
-    int n = 0;
-    for (int j = 0; j < k; ++j) {
-      const int64_t q = (int64_t)t * k + j;
-      const int s = p.slot_of[q];
-      if (s < 0 || (int64_t)s >= p.expert_out_rows) continue;
-      const int r = p.group_by_rank ? p.topk_idx[q] / p.experts_per_rank : 0;
-      const float w = p.topk_weights[q];
-      int i = n++;
-      while (i > 0 && key[i - 1] > r) {  // stable: equal ranks keep j order
-        key[i] = key[i - 1];
-        po.slot[i] = po.slot[i - 1];
-        po.w[i] = po.w[i - 1];
-        --i;
-      }
-      key[i] = r;
-      po.slot[i] = s;
-      po.w[i] = w;
-    }
-    for (int i = 0; i < n; ++i) po.last[i] = (i == n - 1) || (key[i + 1] != key[i]);
-    po.n = n;
-  }
-  __syncthreads();
-
   const int chunks = p.hidden_size / 8;
-  const int c = blockIdx.y * kCombineThreads + threadIdx.x;
-  if (c >= chunks) return;
   const size_t row_bytes = (size_t)p.hidden_size * 2;
-  const uint8_t* base = p.expert_out + (size_t)c * 16;
-  const int n = po.n;
+  const int64_t stride = (int64_t)gridDim.x * kCombineWarps;
+  int64_t u = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
 
-  float total[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int m0 = 0; m0 < n; m0 += kBatch) {
-    uint4 v[kBatch];
+  // pair info of unit uu's token in lanes 0..k-1
+  int nslot = -1, nidx = 0;
+  float nw = 0.0f;
+  auto fetch = [&](int64_t uu) {
+    nslot = -1;
+    if (uu < num_units && lane < k) {
+      const int64_t q = (uu / units_per_token) * k + lane;
+      nslot = p.slot_of[q];
+      nw = p.topk_weights[q];
+      if (GROUP) nidx = p.topk_idx[q];
+    }
+  };
+  fetch(u);
+
+  for (; u < num_units; u += stride) {
+    const int slot = nslot, idx = nidx;
+    const float w = nw;
+    fetch(u + stride);  // in flight while this unit streams
+
+    const int64_t t = u / units_per_token;
+    const int c0 = (int)(u % units_per_token) * chunks_per_unit;
+    const int c1 = min(c0 + chunks_per_unit, chunks);
+
+    const bool valid = slot >= 0 && (int64_t)slot < p.expert_out_rows;
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+    const int n = __popc(vmask);
+    const int key = GROUP ? (valid ? idx / p.experts_per_rank : 0) : 0;
+    // position of this lane's pair in (key, j) order among the valid pairs
+    int pos;
+    if (GROUP) {
+      pos = 0;
+      for (int l = 0; l < k; ++l) {
+        const int kl = __shfl_sync(0xffffffffu, key, l);
+        pos += ((vmask >> l) & 1u) && (kl < key || (kl == key && l < lane));
+      }
+    } else {
+      pos = __popc(vmask & ((1u << lane) - 1u));
+    }
+    // lane m takes the pair at position m
+    int src = 0;
+    for (int l = 0; l < k; ++l) {
+      const int pl = __shfl_sync(0xffffffffu, pos, l);
+      if (((vmask >> l) & 1u) && pl == lane) src = l;
+    }
+    const int o_slot = __shfl_sync(0xffffffffu, slot, src);
+    const float o_w = __shfl_sync(0xffffffffu, w, src);
+    unsigned lastmask = 0;
+    if (GROUP) {
+      const int o_key = __shfl_sync(0xffffffffu, key, src);
+      const int next_key = __shfl_down_sync(0xffffffffu, o_key, 1);
+      lastmask = __ballot_sync(0xffffffffu, lane < n && (lane == n - 1 || next_key != o_key));
+    }
+
+    for (int cb = c0; cb < c1; cb += 32) {
+      const int c = cb + lane;
+      const bool on = c < c1;
+      const uint8_t* col = p.expert_out + (size_t)c * 16;
+      float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      float total[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int m0 = 0; m0 < n; m0 += kBatch) {
+        uint4 v[kBatch];
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b)
-      if (m0 + b < n) v[b] = ld_stream_v4(base + (size_t)po.slot[m0 + b] * row_bytes);
+        for (int b = 0; b < kBatch; ++b) {
+          v[b] = make_uint4(0, 0, 0, 0);
+          if (m0 + b < n) {
+            const int sl = __shfl_sync(0xffffffffu, o_slot, m0 + b);
+            if (on) v[b] = ld_stream_v4(col + (size_t)sl * row_bytes);
+          }
+        }
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      if (m0 + b < n) {
-        fma8(part, po.w[m0 + b], v[b]);
-        if (po.last[m0 + b]) {
-          // TOPK rounds its single chain as it is (a chain that underflows
-          // to -0 stays -0); TOPK_RANKS adds each rank's partial to the
-          // running total, starting from +0.
+        for (int b = 0; b < kBatch; ++b) {
+          if (m0 + b < n) {
+            fma8(part, __shfl_sync(0xffffffffu, o_w, m0 + b), v[b]);
+            if (GROUP && ((lastmask >> (m0 + b)) & 1u)) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            total[i] = p.group_by_rank ? __fadd_rn(total[i], part[i]) : part[i];
-            part[i] = 0.0f;
+              for (int i = 0; i < 8; ++i) {
+                total[i] = __fadd_rn(total[i], part[i]);
+                part[i] = 0.0f;
+              }
+            }
           }
         }
       }
+      // TOPK rounds its single chain as it is (a chain that underflows to -0
+      // stays -0); TOPK_RANKS rounds the sum of the rank partials.
+      if (on) st_v4(p.out + (size_t)t * row_bytes + (size_t)c * 16, pack8(GROUP ? total : part));
     }
   }
-  uint4 o;
-  o.x = pack_bf16x2_rn(total[0], total[1]);
-  o.y = pack_bf16x2_rn(total[2], total[3]);
-  o.z = pack_bf16x2_rn(total[4], total[5]);
-  o.w = pack_bf16x2_rn(total[6], total[7]);
-  st_v4(p.out + (size_t)t * row_bytes + (size_t)c * 16, o);
 }
 
 // Cross-rank sum: out[i] = bf16(sum_r float(P_r[i])), i over 16-byte chunks.
@@ -156,21 +195,67 @@ __global__ void __launch_bounds__(256) k_combine_ranks(const uint8_t* partials, 
 
 }  // namespace
 
+namespace {
+
+// SM count and resident blocks of each kernel, looked up once per device.
+struct DeviceInfo {
+  int sms = 0;
+  int topk_blocks[2] = {0, 0};
+};
+DeviceInfo g_info[64];
+
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  DeviceInfo& d = g_info[dev];
+  if (d.sms == 0) {
+    int sms = 0, b0 = 0, b1 = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_combine_topk<false>, kCombineWarps * 32, 0) != cudaSuccess)
+      return nullptr;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_combine_topk<true>, kCombineWarps * 32, 0) != cudaSuccess)
+      return nullptr;
+    d.topk_blocks[0] = b0 > 0 ? b0 : 1;
+    d.topk_blocks[1] = b1 > 0 ? b1 : 1;
+    d.sms = sms;
+  }
+  return &d;
+}
+
+}  // namespace
+
 cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
+  const DeviceInfo* di = device_info();
+  if (!di) return cudaErrorInvalidDevice;
   const int chunks = p.hidden_size / 8;
-  dim3 grid((unsigned)p.num_tokens, (unsigned)((chunks + kCombineThreads - 1) / kCombineThreads));
-  k_combine_topk<<<grid, kCombineThreads, 0, s>>>(p);
+  const int steps_per_token = (chunks + 31) / 32;  // warp steps of 32 chunks
+  const int g = p.group_by_rank ? 1 : 0;
+  const int64_t resident_warps = (int64_t)di->sms * di->topk_blocks[g] * kCombineWarps;
+  // about 4 units per resident warp, so the grid-stride loop balances well,
+  // but as few units per token as that allows (each unit pays one prologue)
+  int64_t per_unit = (int64_t)p.num_tokens * steps_per_token / (resident_warps * 4);
+  if (per_unit < 1) per_unit = 1;
+  if (per_unit > steps_per_token) per_unit = steps_per_token;
+  const int chunks_per_unit = (int)per_unit * 32;
+  const int units_per_token = (chunks + chunks_per_unit - 1) / chunks_per_unit;
+  const int64_t num_units = (int64_t)p.num_tokens * units_per_token;
+  int64_t blocks = (num_units + kCombineWarps - 1) / kCombineWarps;
+  const int64_t cap = (int64_t)di->sms * di->topk_blocks[g];
+  if (blocks > cap) blocks = cap;
+  if (p.group_by_rank)
+    k_combine_topk<true><<<(unsigned)blocks, kCombineWarps * 32, 0, s>>>(p, units_per_token, chunks_per_unit, num_units);
+  else
+    k_combine_topk<false><<<(unsigned)blocks, kCombineWarps * 32, 0, s>>>(p, units_per_token, chunks_per_unit, num_units);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t rows,
                                  int hidden_size, int num_ranks, cudaStream_t s) {
+  const DeviceInfo* di = device_info();
+  if (!di) return cudaErrorInvalidDevice;
   const int64_t chunks = rows * (hidden_size / 8);
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int64_t blocks = (chunks + 255) / 256;
-  const int64_t cap = (int64_t)sms * 8;
+  const int64_t cap = (int64_t)di->sms * 8;
   if (blocks > cap) blocks = cap;
   k_combine_ranks<4><<<(unsigned)blocks, 256, 0, s>>>(partials, out, chunks, num_ranks);
   return cudaGetLastError();

@@ -32,8 +32,7 @@ constexpr int kCountThreads = 128;   // one thread per token of a chunk
 constexpr int kAssignThreads = 256;  // 8 warps
 constexpr int kSmallThreads = 512;   // 16 warps
 
-__device__ __forceinline__ int load_id(const int32_t* idx, int64_t p, int E, int* bad) {
-  int e = idx[p];
+__device__ __forceinline__ int checked_id(int e, int E, int* bad) {
   if (e < -1 || e >= E) {
     *bad = 1;
     e = -1;
@@ -41,20 +40,44 @@ __device__ __forceinline__ int load_id(const int32_t* idx, int64_t p, int E, int
   return e;
 }
 
-// Phase A over tokens [t0, t1): expert histogram (cnt[E], shared), per-rank
-// token counts (rcnt[R], shared), the is_token_in_rank rows, invalid-id flag.
-// Every thread of the block must call it.
-__device__ void count_tokens(const LayoutParams& p, int t0, int t1, int* cnt, int* rcnt,
-                             int* flag) {
-  const int k = p.topk, E = p.num_experts, R = p.num_ranks, EPR = p.experts_per_rank;
+// Copies topk_idx[p0, p1) into shared sids[0, p1 - p0) with every invalid id
+// replaced by -1 (and *bad set). 16-byte loads when the start is aligned, so
+// the block pays one round of memory latency for all its ids.
+__device__ void stage_ids(const LayoutParams& p, int64_t p0, int64_t p1, int* sids, int* bad) {
+  const int E = p.num_experts;
+  const int len = (int)(p1 - p0);
+  const int32_t* src = p.topk_idx + p0;
+  int b = 0;
+  if ((((uintptr_t)src) & 15) == 0) {
+    const int nv = len / 4;
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+      int4 v = __ldcg(reinterpret_cast<const int4*>(src) + i);
+      sids[4 * i + 0] = checked_id(v.x, E, &b);
+      sids[4 * i + 1] = checked_id(v.y, E, &b);
+      sids[4 * i + 2] = checked_id(v.z, E, &b);
+      sids[4 * i + 3] = checked_id(v.w, E, &b);
+    }
+    for (int i = 4 * nv + threadIdx.x; i < len; i += blockDim.x) sids[i] = checked_id(src[i], E, &b);
+  } else {
+    for (int i = threadIdx.x; i < len; i += blockDim.x) sids[i] = checked_id(src[i], E, &b);
+  }
+  if (b) *bad = 1;
+}
+
+// Phase A over tokens [t0, t1) whose ids are staged in sids (token t0 first):
+// expert histogram (cnt[E], shared), per-rank token counts (rcnt[R], shared)
+// and the is_token_in_rank rows. Every thread of the block must call it.
+__device__ void count_tokens(const LayoutParams& p, int t0, int t1, const int* sids, int* cnt,
+                             int* rcnt) {
+  const int k = p.topk, R = p.num_ranks, EPR = p.experts_per_rank;
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  int bad = 0;
   for (int tb = t0 + warp * 32; tb < t1; tb += nwarps * 32) {
     const int t = tb + (int)lane_id();
     uint64_t mask = 0;
     if (t < t1) {
+      const int* row_ids = sids + (t - t0) * k;
       for (int j = 0; j < k; ++j) {
-        int e = load_id(p.topk_idx, (int64_t)t * k + j, E, &bad);
+        const int e = row_ids[j];
         if (e >= 0) {
           atomicAdd(&cnt[e], 1);
           mask |= 1ull << (e / EPR);
@@ -77,31 +100,30 @@ __device__ void count_tokens(const LayoutParams& p, int t0, int t1, int* cnt, in
       if (lane_id() == 0 && b) atomicAdd(&rcnt[r], __popc(b));
     }
   }
-  if (bad) atomicOr(flag, 1);
 }
 
-// Phase C over pairs [p0, p1) of one block: base[e] is the first slot of the
-// block's pairs of expert e. whist is [nwarps][E] shared scratch. Writes
-// slot_of and src_of_slot. Every thread of the block must call it.
-__device__ void assign_slots(const LayoutParams& p, int64_t p0, int64_t p1, const int* base,
-                             int* whist) {
+// Phase C over pairs [p0, p1) of one block, ids staged in sids (pair p0
+// first): base[e] is the first slot of the block's pairs of expert e. whist is
+// [nwarps][E] shared scratch. Writes slot_of and src_of_slot. Every thread of
+// the block must call it.
+__device__ void assign_slots(const LayoutParams& p, int64_t p0, int64_t p1, const int* sids,
+                             const int* base, int* whist) {
   const int E = p.num_experts;
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const unsigned lane = lane_id();
   const unsigned lt = (1u << lane) - 1u;
-  const int64_t len = p1 - p0;
-  const int64_t per = (len + nwarps - 1) / nwarps;
-  const int64_t w0 = p0 + per * warp;
-  const int64_t w1 = (w0 + per < p1) ? w0 + per : p1;
+  const int len = (int)(p1 - p0);
+  const int per = (len + nwarps - 1) / nwarps;
+  const int w0 = per * warp;
+  const int w1 = min(w0 + per, len);
   int* wh = whist + warp * E;
-  int dummy = 0;
 
   for (int e = threadIdx.x; e < nwarps * E; e += blockDim.x) whist[e] = 0;
   __syncthreads();
   // pass 1: this warp's count per expert
-  for (int64_t pb = w0; pb < w1; pb += 32) {
-    const int64_t q = pb + lane;
-    const int e = (q < w1) ? load_id(p.topk_idx, q, E, &dummy) : -1;
+  for (int qb = w0; qb < w1; qb += 32) {
+    const int q = qb + (int)lane;
+    const int e = (q < w1) ? sids[q] : -1;
     const unsigned m = __match_any_sync(0xffffffffu, e);
     if (e >= 0 && (m & lt) == 0) wh[e] += __popc(m);
   }
@@ -117,9 +139,9 @@ __device__ void assign_slots(const LayoutParams& p, int64_t p0, int64_t p1, cons
   }
   __syncthreads();
   // pass 2: slots
-  for (int64_t pb = w0; pb < w1; pb += 32) {
-    const int64_t q = pb + lane;
-    const int e = (q < w1) ? load_id(p.topk_idx, q, E, &dummy) : -1;
+  for (int qb = w0; qb < w1; qb += 32) {
+    const int q = qb + (int)lane;
+    const int e = (q < w1) ? sids[q] : -1;
     const unsigned m = __match_any_sync(0xffffffffu, e);
     int slot = -1;
     if (e >= 0) slot = wh[e] + __popc(m & lt);
@@ -127,8 +149,8 @@ __device__ void assign_slots(const LayoutParams& p, int64_t p0, int64_t p1, cons
     if (e >= 0 && (m & lt) == 0) wh[e] += __popc(m);
     __syncwarp();
     if (q < w1) {
-      p.slot_of[q] = slot;
-      if (p.src_of_slot && slot >= 0) p.src_of_slot[slot] = (int32_t)q;
+      p.slot_of[p0 + q] = slot;
+      if (p.src_of_slot && slot >= 0) p.src_of_slot[slot] = (int32_t)(p0 + q);
     }
   }
 }
@@ -148,12 +170,15 @@ __global__ void __launch_bounds__(kCountThreads) k_layout_count(LayoutParams p) 
   int* cnt = smem;
   int* rcnt = smem + E;
   int* flag = rcnt + R;
+  int* sids = flag + 1;  // [tokens_per_chunk * k]
   for (int i = threadIdx.x; i < E + R + 1; i += blockDim.x) smem[i] = 0;
-  __syncthreads();
   const int c = blockIdx.x;
   const int t0 = c * p.tokens_per_chunk;
   const int t1 = min(t0 + p.tokens_per_chunk, p.num_tokens);
-  count_tokens(p, t0, t1, cnt, rcnt, flag);
+  __syncthreads();
+  stage_ids(p, (int64_t)t0 * p.topk, (int64_t)t1 * p.topk, sids, flag);
+  __syncthreads();
+  count_tokens(p, t0, t1, sids, cnt, rcnt);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) p.chunk_hist[(int64_t)c * E + e] = cnt[e];
   for (int r = threadIdx.x; r < R; r += blockDim.x) p.chunk_rank[(int64_t)c * R + r] = rcnt[r];
@@ -173,10 +198,16 @@ __device__ int64_t scan_chunks(const LayoutParams& p, int c, int* base, int* scr
     const int e = e0 + i;
     if (e >= E) break;
     int tot = 0, pre = 0;
-    for (int c2 = 0; c2 < C; ++c2) {
-      const int v = __ldcg(&p.chunk_hist[(int64_t)c2 * E + e]);
-      tot += v;
-      pre += (c2 < c) ? v : 0;
+    for (int c0 = 0; c0 < C; c0 += 8) {  // 8 independent loads in flight
+      int v[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b)
+        v[b] = (c0 + b < C) ? __ldcg(&p.chunk_hist[(int64_t)(c0 + b) * E + e]) : 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        tot += v[b];
+        pre += (c0 + b < c) ? v[b] : 0;
+      }
     }
     base[e] = pre;       // within-expert prefix of this chunk, for now
     base[E + e] = tot;   // expert total
@@ -217,14 +248,18 @@ __device__ int64_t scan_chunks(const LayoutParams& p, int c, int* base, int* scr
 __global__ void __launch_bounds__(kAssignThreads) k_layout_assign(LayoutParams p) {
   extern __shared__ int smem[];
   const int E = p.num_experts;
-  int* scratch = smem;            // 33
+  int* scratch = smem;            // 33 (+3 pad)
   int* base = smem + 36;          // [2E]
   int* whist = base + 2 * E;      // [8][E]
+  int* sids = whist + (kAssignThreads / 32) * E;  // [tokens_per_chunk * k]
   const int c = blockIdx.x;
-  const int64_t P = scan_chunks<kAssignThreads>(p, c, base, scratch);
   const int t0 = c * p.tokens_per_chunk;
   const int t1 = min(t0 + p.tokens_per_chunk, p.num_tokens);
-  assign_slots(p, (int64_t)t0 * p.topk, (int64_t)t1 * p.topk, base, whist);
+  const int64_t p0 = (int64_t)t0 * p.topk, p1 = (int64_t)t1 * p.topk;
+  int dummy = 0;
+  stage_ids(p, p0, p1, sids, &dummy);  // in flight during the scan below
+  const int64_t P = scan_chunks<kAssignThreads>(p, c, base, scratch);
+  assign_slots(p, p0, p1, sids, base, whist);
   clear_src_tail(p, P);
 }
 
@@ -238,9 +273,13 @@ __global__ void __launch_bounds__(kSmallThreads) k_layout_small(LayoutParams p) 
   int* flag = rcnt + R;         // [1]
   int* base = flag + 1;         // [E]
   int* whist = base + E;        // [16][E]
+  int* sids = whist + (kSmallThreads / 32) * E;  // [N * k]
+  const int64_t pairs = (int64_t)p.num_tokens * p.topk;
   for (int i = threadIdx.x; i < E + R + 1; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
-  count_tokens(p, 0, p.num_tokens, cnt, rcnt, flag);
+  stage_ids(p, 0, pairs, sids, flag);
+  __syncthreads();
+  count_tokens(p, 0, p.num_tokens, sids, cnt, rcnt);
   __syncthreads();
   // exclusive scan of the expert counts
   const int ept = (E + kSmallThreads - 1) / kSmallThreads;
@@ -264,7 +303,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_layout_small(LayoutParams p) 
     *p.status = *flag ? MOE_ERR_DEVICE_IDS : MOE_OK;
   }
   __syncthreads();
-  assign_slots(p, 0, (int64_t)p.num_tokens * p.topk, base, whist);
+  assign_slots(p, 0, pairs, sids, base, whist);
   clear_src_tail(p, total);
 }
 
@@ -288,17 +327,20 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s) {
   const int E = p.num_experts, R = p.num_ranks;
   const int64_t pairs = (int64_t)p.num_tokens * p.topk;
   if (pairs <= kSmallLayoutMaxPairs) {
-    const size_t smem = (size_t)(36 + E + R + 1 + E + (kSmallThreads / 32) * E) * 4;
+    const size_t smem = (size_t)(36 + E + R + 1 + E + (kSmallThreads / 32) * E + pairs) * 4;
     cudaError_t err = set_smem((const void*)k_layout_small, smem);
     if (err != cudaSuccess) return err;
     k_layout_small<<<1, kSmallThreads, smem, s>>>(p);
     return cudaGetLastError();
   }
-  const size_t smem_count = (size_t)(E + R + 1) * 4;
-  k_layout_count<<<p.num_chunks, kCountThreads, smem_count, s>>>(p);
-  cudaError_t err = cudaGetLastError();
+  const size_t chunk_ids = (size_t)p.tokens_per_chunk * p.topk;
+  const size_t smem_count = (size_t)(E + R + 1) * 4 + chunk_ids * 4;
+  cudaError_t err = set_smem((const void*)k_layout_count, smem_count);
   if (err != cudaSuccess) return err;
-  const size_t smem_assign = (size_t)(36 + 2 * E + (kAssignThreads / 32) * E) * 4;
+  k_layout_count<<<p.num_chunks, kCountThreads, smem_count, s>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t smem_assign = (size_t)(36 + 2 * E + (kAssignThreads / 32) * E) * 4 + chunk_ids * 4;
   err = set_smem((const void*)k_layout_assign, smem_assign);
   if (err != cudaSuccess) return err;
   k_layout_assign<<<p.num_chunks, kAssignThreads, smem_assign, s>>>(p);
