@@ -14,7 +14,10 @@
 // body (everything after the 16-byte header) is assembled once in shared
 // memory. Then thread j writes pair j's header with one 16-byte store and
 // hands the body to the bulk-copy engine (cp.async.bulk shared -> global), so
-// the k copies of the body cost no register traffic. The token's input is
+// the k copies of the body cost no register traffic. The stores carry an L2
+// evict-first policy: records are written once here and read by another
+// kernel later, so they should not linger dirty in L2 for the next kernel to
+// write back. The token's input is
 // read once and k records are written: the kernel is write-bound.
 #include "moe_internal.cuh"
 
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p)
     if (s >= 0) {
       uint8_t* rec = p.records + (size_t)s * p.record_bytes;
       st_v4(rec, make_uint4((uint32_t)t, (uint32_t)j, (uint32_t)s_expert[j], 0u));
-      bulk_store_s2g(rec + 16, img, (uint32_t)body);
+      bulk_store_s2g_evict_first(rec + 16, img, (uint32_t)body, l2_evict_first_policy());
       bulk_commit();
       bulk_wait_read_all();
     }

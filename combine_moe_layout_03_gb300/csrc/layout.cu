@@ -6,22 +6,25 @@
 // that dispatch and combine use.
 //
 // Design (all integer work, latency- not bandwidth-bound):
-//  * Pairs are cut into chunks of kLayoutTokensPerChunk tokens.
-//  * k_layout_count: one block per chunk. One thread per token reads its k
-//    ids, counts them into a shared-memory histogram, builds the token's rank
-//    bitmask, writes its is_token_in_rank row and counts tokens per rank with
-//    warp ballots. The chunk's histogram goes to the workspace.
-//  * k_layout_assign: one block per chunk. Each block scans the per-chunk
-//    histograms itself (redundantly, from L2), so no grid-wide barrier, atomic
-//    counter or third kernel is needed. Inside the chunk, each warp owns a
-//    contiguous run of pairs; per-warp histograms and a scan over warps give
-//    every warp its starting slot per expert; within a warp the rank of a
-//    pair among equal experts is popc(match_any mask & lanes below). Slots
-//    thus follow ascending (t, j) inside every expert: deterministic, no
-//    global atomics.
-//  * Small inputs (N*k <= kSmallLayoutMaxPairs, e.g. decode) run all phases in
-//    one block: one launch.
+//  * Up to 8 * 4096 pairs (every workload of the pages): one launch of a
+//    thread-block cluster of up to 8 blocks of 1024 threads (k_layout_cluster).
+//    Each block stages its run of ids in shared memory with 16-byte loads,
+//    builds its expert histogram, rank-mask rows and per-warp histograms
+//    there, and after a hardware cluster barrier reads the other blocks'
+//    histograms through distributed shared memory to get the expert totals
+//    and its own prefix. Each block then ranks its pairs: per-warp starting
+//    slots from a scan over warps, and within a warp the rank of a pair among
+//    equal experts is popc(match_any mask & lanes below). Slots follow
+//    ascending (t, j) inside every expert: deterministic, no global atomics,
+//    no workspace except the status word.
+//  * Larger inputs: k_layout_count (one block per 128-token chunk, chunk
+//    histograms to the workspace), then k_layout_assign, where every block
+//    scans the chunk histograms itself (redundantly, from L2), so no
+//    grid-wide barrier or atomic counter is needed, and ranks its pairs as
+//    above.
 // Ids outside [-1, E) count as -1 and raise the status word.
+#include <cooperative_groups.h>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -30,7 +33,10 @@ namespace {
 
 constexpr int kCountThreads = 128;   // one thread per token of a chunk
 constexpr int kAssignThreads = 256;  // 8 warps
-constexpr int kSmallThreads = 512;   // 16 warps
+constexpr int kClusterThreads = 1024;  // 32 warps
+constexpr int kClusterMaxBlocks = 8;   // portable cluster size
+constexpr int kPairsPerClusterBlock = 4096;
+constexpr size_t kClusterMaxSmem = 200 * 1024;
 
 __device__ __forceinline__ int checked_id(int e, int E, int* bad) {
   if (e < -1 || e >= E) {
@@ -65,22 +71,29 @@ __device__ void stage_ids(const LayoutParams& p, int64_t p0, int64_t p1, int* si
 }
 
 // Phase A over tokens [t0, t1) whose ids are staged in sids (token t0 first):
-// expert histogram (cnt[E], shared), per-rank token counts (rcnt[R], shared)
-// and the is_token_in_rank rows. Every thread of the block must call it.
-__device__ void count_tokens(const LayoutParams& p, int t0, int t1, const int* sids, int* cnt,
-                             int* rcnt) {
-  const int k = p.topk, R = p.num_ranks, EPR = p.experts_per_rank;
+// per-rank token counts (rcnt[R], shared), the is_token_in_rank rows and, if
+// COUNT_EXPERTS, the expert histogram (cnt[E], shared). Every thread of the
+// block must call it.
+template <bool COUNT_EXPERTS>
+__device__ void count_tokens(const LayoutParams& p, int t0, int t1, const int* sids,
+                             const int* rank_of, int* cnt, int* rcnt) {
+  const int k = p.topk, R = p.num_ranks;
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int tb = t0 + warp * 32; tb < t1; tb += nwarps * 32) {
     const int t = tb + (int)lane_id();
     uint64_t mask = 0;
     if (t < t1) {
       const int* row_ids = sids + (t - t0) * k;
-      for (int j = 0; j < k; ++j) {
-        const int e = row_ids[j];
-        if (e >= 0) {
-          atomicAdd(&cnt[e], 1);
-          mask |= 1ull << (e / EPR);
+      for (int j0 = 0; j0 < k; j0 += 8) {  // 8 independent reads at a time
+        int ev[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) ev[b] = (j0 + b < k) ? row_ids[j0 + b] : -1;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (ev[b] >= 0) {
+            if (COUNT_EXPERTS) atomicAdd(&cnt[ev[b]], 1);
+            mask |= 1ull << rank_of[ev[b]];
+          }
         }
       }
       uint8_t* row = p.is_token_in_rank + (int64_t)t * R;
@@ -102,57 +115,106 @@ __device__ void count_tokens(const LayoutParams& p, int t0, int t1, const int* s
   }
 }
 
-// Phase C over pairs [p0, p1) of one block, ids staged in sids (pair p0
-// first): base[e] is the first slot of the block's pairs of expert e. whist is
-// [nwarps][E] shared scratch. Writes slot_of and src_of_slot. Every thread of
-// the block must call it.
-__device__ void assign_slots(const LayoutParams& p, int64_t p0, int64_t p1, const int* sids,
-                             const int* base, int* whist) {
-  const int E = p.num_experts;
+// rank_of[e] = e / (E/R) for e < E, in shared memory (no division per pair).
+__device__ __forceinline__ void fill_rank_of(const LayoutParams& p, int* rank_of) {
+  for (int e = threadIdx.x; e < p.num_experts; e += blockDim.x) rank_of[e] = e / p.experts_per_rank;
+}
+
+// Bits for expert keys 0..E-1 plus the "no expert" key 2^nbits - 1 >= E.
+__device__ __forceinline__ int key_bits(int E) { return 32 - __clz(E); }
+
+// Phase C, part 1, over the len pairs staged in sids: each warp owns a
+// contiguous run of them, counts its run per expert into whist[warp][E] and
+// replaces each staged id by (rank of the pair among the run's pairs of the
+// same expert, in order) << 11 | (id + 1). Every thread of the block must
+// call it; ends with a barrier.
+__device__ void warp_histograms(int E, int len, int* sids, int* whist) {
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const unsigned lane = lane_id();
   const unsigned lt = (1u << lane) - 1u;
-  const int len = (int)(p1 - p0);
   const int per = (len + nwarps - 1) / nwarps;
   const int w0 = per * warp;
   const int w1 = min(w0 + per, len);
+  const int nb = key_bits(E);
+  const int none = (1 << nb) - 1;
   int* wh = whist + warp * E;
-
   for (int e = threadIdx.x; e < nwarps * E; e += blockDim.x) whist[e] = 0;
   __syncthreads();
-  // pass 1: this warp's count per expert
-  for (int qb = w0; qb < w1; qb += 32) {
-    const int q = qb + (int)lane;
-    const int e = (q < w1) ? sids[q] : -1;
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && (m & lt) == 0) wh[e] += __popc(m);
+  constexpr int S = 4;  // steps of 32 pairs whose masks are built together
+  for (int qb = w0; qb < w1; qb += 32 * S) {
+    int e[S], key[S];
+    unsigned m[S];
+#pragma unroll
+    for (int st = 0; st < S; ++st) {
+      const int q = qb + 32 * st + (int)lane;
+      e[st] = (q < w1) ? sids[q] : -1;
+      key[st] = e[st] >= 0 ? e[st] : none;
+      m[st] = 0xffffffffu;
+    }
+    for (int b = 0; b < nb; ++b) {
+#pragma unroll
+      for (int st = 0; st < S; ++st) {
+        const unsigned bit = (key[st] >> b) & 1u;
+        const unsigned v = __ballot_sync(0xffffffffu, bit);
+        m[st] &= bit ? v : ~v;
+      }
+    }
+#pragma unroll
+    for (int st = 0; st < S; ++st) {  // in pair order: counts carry over
+      const int q = qb + 32 * st + (int)lane;
+      int rank = 0;
+      if (e[st] >= 0) rank = wh[e[st]] + __popc(m[st] & lt);
+      __syncwarp();
+      if (e[st] >= 0 && (m[st] & lt) == 0) wh[e[st]] += __popc(m[st]);
+      __syncwarp();
+      if (q < w1) sids[q] = (rank << 11) | (e[st] + 1);
+    }
   }
   __syncthreads();
-  // scan over warps per expert, offset by the block's base
+}
+
+// Phase C, part 2: base[e] is the first slot of the block's pairs of expert
+// e; a scan over warps turns whist into each warp's first slot per expert and
+// every pair's slot is that plus its rank from part 1. Writes
+// slot_of[p0 + q] and src_of_slot. Every thread of the block must call it.
+template <int NW>
+__device__ void assign_from_histograms(const LayoutParams& p, int64_t p0, int len,
+                                       const int* sids, const int* base, int* whist) {
+  const int E = p.num_experts;
+  const int warp = threadIdx.x >> 5;
+  const unsigned lane = lane_id();
+  const int per = (len + NW - 1) / NW;
+  const int w0 = per * warp;
+  const int w1 = min(w0 + per, len);
+  const int* wh = whist + warp * E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = base[e];
-    for (int w = 0; w < nwarps; ++w) {
-      int c = whist[w * E + e];
-      whist[w * E + e] = run;
-      run += c;
+#pragma unroll
+    for (int g0 = 0; g0 < NW; g0 += 8) {  // 8 loads in flight at a time
+      int c[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) c[w] = whist[(g0 + w) * E + e];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        whist[(g0 + w) * E + e] = run;
+        run += c[w];
+      }
     }
   }
   __syncthreads();
-  // pass 2: slots
-  for (int qb = w0; qb < w1; qb += 32) {
-    const int q = qb + (int)lane;
-    const int e = (q < w1) ? sids[q] : -1;
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    int slot = -1;
-    if (e >= 0) slot = wh[e] + __popc(m & lt);
-    __syncwarp();
-    if (e >= 0 && (m & lt) == 0) wh[e] += __popc(m);
-    __syncwarp();
-    if (q < w1) {
-      p.slot_of[p0 + q] = slot;
-      if (p.src_of_slot && slot >= 0) p.src_of_slot[slot] = (int32_t)(p0 + q);
-    }
+  for (int q = w0 + (int)lane; q < w1; q += 32) {
+    const int v = sids[q];
+    const int e = (v & 2047) - 1;
+    const int slot = e >= 0 ? wh[e] + (v >> 11) : -1;
+    p.slot_of[p0 + q] = slot;
+    if (p.src_of_slot && slot >= 0) p.src_of_slot[slot] = (int32_t)(p0 + q);
   }
+}
+
+__device__ void assign_slots(const LayoutParams& p, int64_t p0, int64_t p1, int* sids,
+                             const int* base, int* whist) {
+  warp_histograms(p.num_experts, (int)(p1 - p0), sids, whist);
+  assign_from_histograms<kAssignThreads / 32>(p, p0, (int)(p1 - p0), sids, base, whist);
 }
 
 // src_of_slot[s] = -1 for s in [P, N*k), spread over the grid.
@@ -170,15 +232,17 @@ __global__ void __launch_bounds__(kCountThreads) k_layout_count(LayoutParams p) 
   int* cnt = smem;
   int* rcnt = smem + E;
   int* flag = rcnt + R;
-  int* sids = flag + 1;  // [tokens_per_chunk * k]
+  int* rank_of = flag + 1;  // [E]
+  int* sids = rank_of + E;  // [tokens_per_chunk * k]
   for (int i = threadIdx.x; i < E + R + 1; i += blockDim.x) smem[i] = 0;
+  fill_rank_of(p, rank_of);
   const int c = blockIdx.x;
   const int t0 = c * p.tokens_per_chunk;
   const int t1 = min(t0 + p.tokens_per_chunk, p.num_tokens);
   __syncthreads();
   stage_ids(p, (int64_t)t0 * p.topk, (int64_t)t1 * p.topk, sids, flag);
   __syncthreads();
-  count_tokens(p, t0, t1, sids, cnt, rcnt);
+  count_tokens<true>(p, t0, t1, sids, rank_of, cnt, rcnt);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) p.chunk_hist[(int64_t)c * E + e] = cnt[e];
   for (int r = threadIdx.x; r < R; r += blockDim.x) p.chunk_rank[(int64_t)c * R + r] = rcnt[r];
@@ -263,48 +327,107 @@ __global__ void __launch_bounds__(kAssignThreads) k_layout_assign(LayoutParams p
   clear_src_tail(p, P);
 }
 
-// Everything in one block (small inputs).
-__global__ void __launch_bounds__(kSmallThreads) k_layout_small(LayoutParams p) {
+// Everything in one launch: a cluster of G blocks (G <= 8), block c owning a
+// contiguous run of tokens. Each block stages its ids, counts them (shared
+// histogram, rank mask rows, per-warp histograms), then after a cluster
+// barrier reads the other blocks' histograms through distributed shared
+// memory to get the expert totals and its own prefix; one scan gives the
+// offsets, and the block ranks its pairs. No workspace is used except the
+// status word. A final cluster barrier keeps every block's shared memory
+// alive until the others have read it.
+__global__ void __launch_bounds__(kClusterThreads) k_layout_cluster(LayoutParams p, int tokens_per_block) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ int smem[];
-  const int E = p.num_experts, R = p.num_ranks;
+  const int E = p.num_experts, R = p.num_ranks, k = p.topk;
+  const int G = (int)cluster.num_blocks();
+  const int c = (int)cluster.block_rank();
   int* scratch = smem;          // 33 (+3 pad)
-  int* cnt = smem + 36;         // [E]
-  int* rcnt = cnt + E;          // [R]
-  int* flag = rcnt + R;         // [1]
+  int* cnt = smem + 36;         // [E] this block's expert counts
+  int* rcnt = cnt + E;          // [R] this block's token-in-rank counts
+  int* flag = rcnt + R;         // [1] invalid ids seen
   int* base = flag + 1;         // [E]
-  int* whist = base + E;        // [16][E]
-  int* sids = whist + (kSmallThreads / 32) * E;  // [N * k]
-  const int64_t pairs = (int64_t)p.num_tokens * p.topk;
+  int* rank_of = base + E;      // [E]
+  int* whist = rank_of + E;     // [32][E]
+  int* sids = whist + (kClusterThreads / 32) * E;  // [tokens_per_block * k]
+  const int t0 = min(c * tokens_per_block, p.num_tokens);
+  const int t1 = min(t0 + tokens_per_block, p.num_tokens);
+  const int64_t p0 = (int64_t)t0 * k;
+  const int len = (t1 - t0) * k;
+
   for (int i = threadIdx.x; i < E + R + 1; i += blockDim.x) cnt[i] = 0;
+  fill_rank_of(p, rank_of);
   __syncthreads();
-  stage_ids(p, 0, pairs, sids, flag);
+  stage_ids(p, p0, p0 + len, sids, flag);
   __syncthreads();
-  count_tokens(p, 0, p.num_tokens, sids, cnt, rcnt);
-  __syncthreads();
-  // exclusive scan of the expert counts
-  const int ept = (E + kSmallThreads - 1) / kSmallThreads;
-  const int e0 = threadIdx.x * ept;
-  int mine = 0;
-  for (int i = 0; i < ept && e0 + i < E; ++i) mine += cnt[e0 + i];
+  count_tokens<false>(p, t0, t1, sids, rank_of, cnt, rcnt);
+  warp_histograms(E, len, sids, whist);  // starts and ends with a barrier
+  if (threadIdx.x < E) {                 // the block's expert counts
+    int sum = 0;
+#pragma unroll
+    for (int g0 = 0; g0 < kClusterThreads / 32; g0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) v[w] = whist[(g0 + w) * E + threadIdx.x];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) sum += v[w];
+    }
+    cnt[threadIdx.x] = sum;
+  }
+  cluster.sync();  // every block's cnt/rcnt/flag is final
+
+  // Expert totals and this block's prefix from all blocks' counts: thread e
+  // owns expert e (E <= 1024 = blockDim) and issues its (at most 8) remote
+  // loads together, so the exchange costs one distributed-shared-memory round
+  // trip.
+  const int e = threadIdx.x;
+  int tot = 0, pre = 0;
+  if (e < E) {
+    int v[kClusterMaxBlocks];
+#pragma unroll
+    for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(cnt + e, b) : 0;
+#pragma unroll
+    for (int b = 0; b < kClusterMaxBlocks; ++b) {
+      tot += v[b];
+      pre += (b < c) ? v[b] : 0;
+    }
+  }
   int total;
-  int ex = block_exclusive_scan<kSmallThreads>(mine, scratch, &total);
-  for (int i = 0; i < ept && e0 + i < E; ++i) {
-    const int e = e0 + i;
-    p.tokens_per_expert[e] = cnt[e];
-    p.expert_offset[e] = ex;
-    if (e % p.experts_per_rank == 0) p.rank_offset[e / p.experts_per_rank] = ex;
-    base[e] = ex;
-    ex += cnt[e];
+  const int ex = block_exclusive_scan<kClusterThreads>(tot, scratch, &total);
+  if (e < E) {
+    base[e] = ex + pre;
+    if (c == 0) {
+      p.tokens_per_expert[e] = tot;
+      p.expert_offset[e] = ex;
+      if (e % p.experts_per_rank == 0) p.rank_offset[e / p.experts_per_rank] = ex;
+    }
   }
-  for (int r = threadIdx.x; r < R; r += blockDim.x) p.tokens_per_rank[r] = rcnt[r];
-  if (threadIdx.x == 0) {
-    p.expert_offset[E] = total;
-    p.rank_offset[R] = total;
-    *p.status = *flag ? MOE_ERR_DEVICE_IDS : MOE_OK;
+  if (c == 0) {
+    if (e < R) {
+      int v[kClusterMaxBlocks];
+#pragma unroll
+      for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(rcnt + e, b) : 0;
+      int sum = 0;
+#pragma unroll
+      for (int b = 0; b < kClusterMaxBlocks; ++b) sum += v[b];
+      p.tokens_per_rank[e] = sum;
+    }
+    if (e == 0) {
+      int v[kClusterMaxBlocks];
+#pragma unroll
+      for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(flag, b) : 0;
+      int f = 0;
+#pragma unroll
+      for (int b = 0; b < kClusterMaxBlocks; ++b) f |= v[b];
+      p.expert_offset[E] = total;
+      p.rank_offset[R] = total;
+      *p.status = f ? MOE_ERR_DEVICE_IDS : MOE_OK;
+    }
   }
   __syncthreads();
-  assign_slots(p, 0, pairs, sids, base, whist);
+  assign_from_histograms<kClusterThreads / 32>(p, p0, len, sids, base, whist);
   clear_src_tail(p, total);
+  cluster.sync();  // no block leaves while another may still read its counts
 }
 
 }  // namespace
@@ -323,18 +446,45 @@ static cudaError_t set_smem(const void* fn, size_t bytes) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+static bool layout_fits_cluster(int num_tokens, int topk, int num_experts, int num_ranks) {
+  const int64_t pairs = (int64_t)num_tokens * topk;
+  int g = (int)((pairs + kPairsPerClusterBlock - 1) / kPairsPerClusterBlock);
+  g = g < 1 ? 1 : (g > kClusterMaxBlocks ? kClusterMaxBlocks : g);
+  int tpb = (num_tokens + g - 1) / g;
+  tpb = (tpb + 3) / 4 * 4;
+  const size_t smem = (size_t)(36 + 3 * num_experts + num_ranks + 1 +
+                               (kClusterThreads / 32) * num_experts) * 4 + (size_t)tpb * topk * 4;
+  return smem <= kClusterMaxSmem;
+}
+
 cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s) {
   const int E = p.num_experts, R = p.num_ranks;
   const int64_t pairs = (int64_t)p.num_tokens * p.topk;
-  if (pairs <= kSmallLayoutMaxPairs) {
-    const size_t smem = (size_t)(36 + E + R + 1 + E + (kSmallThreads / 32) * E + pairs) * 4;
-    cudaError_t err = set_smem((const void*)k_layout_small, smem);
+  if (layout_fits_cluster(p.num_tokens, p.topk, E, R)) {
+    int g = (int)((pairs + kPairsPerClusterBlock - 1) / kPairsPerClusterBlock);
+    g = g < 1 ? 1 : (g > kClusterMaxBlocks ? kClusterMaxBlocks : g);
+    int tpb = (p.num_tokens + g - 1) / g;
+    tpb = (tpb + 3) / 4 * 4;  // 16-byte aligned id runs per block
+    const size_t smem = (size_t)(36 + 3 * E + R + 1 + (kClusterThreads / 32) * E) * 4 +
+                        (size_t)tpb * p.topk * 4;
+    cudaError_t err = set_smem((const void*)k_layout_cluster, smem);
     if (err != cudaSuccess) return err;
-    k_layout_small<<<1, kSmallThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)g);
+    cfg.blockDim = dim3(kClusterThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)g;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_layout_cluster, p, tpb);
   }
   const size_t chunk_ids = (size_t)p.tokens_per_chunk * p.topk;
-  const size_t smem_count = (size_t)(E + R + 1) * 4 + chunk_ids * 4;
+  const size_t smem_count = (size_t)(2 * E + R + 1) * 4 + chunk_ids * 4;
   cudaError_t err = set_smem((const void*)k_layout_count, smem_count);
   if (err != cudaSuccess) return err;
   k_layout_count<<<p.num_chunks, kCountThreads, smem_count, s>>>(p);

@@ -58,7 +58,6 @@ struct CombineParams {
 
 // Workspace carving shared by moe_workspace_size and moe_layout.
 constexpr int kLayoutTokensPerChunk = 128;
-constexpr int kSmallLayoutMaxPairs = 4096;
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 
 // Launchers (return cudaError_t of the launch).
@@ -139,6 +138,21 @@ __device__ __forceinline__ void bulk_store_s2g(void* gdst, const void* ssrc, uin
   uint32_t sa = (uint32_t)__cvta_generic_to_shared(ssrc);
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(sa),
                "r"(bytes)
+               : "memory");
+}
+// Same, with an L2 evict-first policy: data written once and not read again
+// soon leaves L2 early instead of staying dirty for later kernels to write
+// back.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_store_s2g_evict_first(void* gdst, const void* ssrc,
+                                                           uint32_t bytes, uint64_t pol) {
+  uint32_t sa = (uint32_t)__cvta_generic_to_shared(ssrc);
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
+               "r"(sa), "r"(bytes), "l"(pol)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

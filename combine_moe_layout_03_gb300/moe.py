@@ -262,6 +262,57 @@ def moe_unpack_record(desc: MoeDesc, record):
                 payload=pay, scales=sc)
 
 
+class Prepared:
+    """One libmoe call with its arguments marshalled once, for repeated
+    launches on the same buffers and stream (argument marshalling only; each
+    call of the object enqueues the library's kernels again)."""
+
+    def __init__(self, name: str, args: tuple, keep: tuple):
+        self._fn = getattr(_lib, name)
+        self._name = name
+        self._args = args
+        self._keep = keep  # ctypes structs and tensors the arguments point into
+
+    def __call__(self):
+        rc = self._fn(*self._args)
+        if rc != MOE_OK:
+            raise MoeError(rc, self._name)
+
+
+def _vps(*ts):
+    return tuple(ctypes.c_void_p(_ptr(t)) for t in ts)
+
+
+def prepare_layout(desc: MoeDesc, topk_idx, out: dict, workspace, stream=None) -> Prepared:
+    d = desc.c()
+    ptrs = _vps(topk_idx, out["tokens_per_expert"], out["tokens_per_rank"],
+                out["is_token_in_rank"], out["expert_offset"], out["rank_offset"], out["slot_of"],
+                out.get("src_of_slot"), workspace)
+    args = (ctypes.byref(d), *ptrs, ctypes.c_size_t(workspace.numel()),
+            ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_layout", args, (d, topk_idx, out, workspace))
+
+
+def prepare_dispatch(desc: MoeDesc, topk_idx, topk_weights, hidden, scales, slot_of, records,
+                     stream=None) -> Prepared:
+    d = desc.c()
+    ptrs = _vps(topk_idx, topk_weights, hidden, scales, slot_of, records)
+    args = (ctypes.byref(d), *ptrs, ctypes.c_size_t(records.numel() * records.element_size()),
+            ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_dispatch", args, (d, topk_idx, topk_weights, hidden, scales, slot_of,
+                                           records))
+
+
+def prepare_combine(desc: MoeDesc, mode: int, expert_out, topk_idx, topk_weights, slot_of, out,
+                    stream=None) -> Prepared:
+    d = desc.c()
+    rows = expert_out.numel() // max(desc.hidden, 1)
+    ptrs = _vps(topk_idx, topk_weights, slot_of, out)
+    args = (ctypes.byref(d), ctypes.c_int(mode), ctypes.c_void_p(_ptr(expert_out)),
+            ctypes.c_int64(rows), *ptrs, ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_combine", args, (d, expert_out, topk_idx, topk_weights, slot_of, out))
+
+
 def exported_symbols() -> list[str]:
     return ["moe_strerror", "moe_record_layout", "moe_workspace_size", "moe_layout",
             "moe_layout_status", "moe_dispatch", "moe_combine", "moe_pack_record",

@@ -151,3 +151,33 @@ def test_empty_combine_is_a_no_op():
     out = moe.moe_combine(d, moe.MOE_COMBINE_TOPK, torch.empty((1, 64), dtype=torch.bfloat16,
                                                                device=DEV), e, e.float(), e)
     assert out.shape == (0, 64)
+
+
+def test_prepared_calls_match_direct_calls():
+    """The binding's pre-marshalled calls launch the same kernels on the same
+    buffers: repeated calls give the direct calls' results."""
+    from combine_moe_layout_03_gb300 import moe
+    c = synth.prefill_case(seed=8, n=512)
+    n, k, e, r, h = 512, 8, 256, 8, 7168
+    d = moe.MoeDesc(n, k, e, r, h, moe.MOE_PAYLOAD_BF16, moe.MOE_PAYLOAD_FP8_E4M3_B128)
+    ids, w, x = dev_i32(c["topk_idx"]), dev_f32(c["topk_weights"]), dev_bf16(c["hidden_bf16"])
+    ref_lay = moe.moe_layout(d, ids)
+    ref_rec = moe.moe_dispatch(d, ids, w, x, None, ref_lay["slot_of"])
+    y = dev_bf16(synth.bf16_normal(synth.rng_for(1), (n * k, h)))
+    cd = moe.MoeDesc(n, k, e, r, h)
+    ref_out = moe.moe_combine(cd, moe.MOE_COMBINE_TOPK_RANKS, y, ids, w, ref_lay["slot_of"])
+    lay = moe.layout_outputs(d, DEV)
+    ws = torch.empty(moe.moe_workspace_size(d), dtype=torch.uint8, device=DEV)
+    rec = torch.zeros_like(ref_rec)
+    out = torch.zeros_like(ref_out)
+    pl = moe.prepare_layout(d, ids, lay, ws)
+    pd = moe.prepare_dispatch(d, ids, w, x, None, lay["slot_of"], rec)
+    pc = moe.prepare_combine(cd, moe.MOE_COMBINE_TOPK_RANKS, y, ids, w, lay["slot_of"], out)
+    for _ in range(2):
+        pl()
+        pd()
+        pc()
+    torch.cuda.synchronize()
+    assert torch.equal(lay["slot_of"], ref_lay["slot_of"])
+    assert torch.equal(rec, ref_rec)
+    assert torch.equal(out, ref_out)

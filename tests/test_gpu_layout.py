@@ -72,8 +72,11 @@ def test_rs_sizes(t):
     (700, 32, 64, 1),      # largest k, one rank
     (3000, 3, 7, 7),       # one expert per rank
     (129, 2, 2, 2),
-    (600, 8, 1024, 8),     # the single-block path limit is crossed at N*k > 4096
-    (512, 8, 1024, 8),     # exactly at the single-block limit
+    (600, 8, 1024, 8),     # two cluster blocks
+    (512, 8, 1024, 8),     # exactly one cluster block of 4096 pairs
+    (50000, 8, 256, 8),    # ids of a cluster block exceed shared memory: two-kernel path
+    (20000, 8, 1024, 16),  # large E: two-kernel path
+    (33000, 3, 64, 4),     # eight cluster blocks of 12376 pairs
 ])
 def test_ragged_and_extreme_shapes(n, k, e, r):
     g = np.random.default_rng(n * 31 + k)

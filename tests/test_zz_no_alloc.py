@@ -52,15 +52,28 @@ def _compare(moe, desc, ids):
 def test_noalloc_matches_moe_layout_on_two_calls_in_a_row():
     from combine_moe_layout_03_gb300 import moe
     dev = torch.device("cuda:0")
-    # call 1: prefill routing (multi-block path, 32 chunks of scratch)
-    c = synth.prefill_case(seed=11)
-    ids = torch.from_numpy(c["topk_idx"]).to(dev)
-    st, ref_st = _compare(moe, moe.MoeDesc(4096, 8, 256, 8, 7168), ids)
-    assert st == ref_st == moe.MOE_OK
-    # call 2, right after, on a ragged shape with padding ids and fewer chunks
+    # Two calls in a row on shapes large enough for the layout to keep
+    # per-chunk counts in scratch (the two-kernel path): the second call runs
+    # on the scratch the first one left behind, with fewer chunks and other E.
     g = np.random.default_rng(12)
-    ids2 = g.integers(-1, 64, size=(1000, 6)).astype(np.int32)
-    st, ref_st = _compare(moe, moe.MoeDesc(1000, 6, 64, 4, 8), torch.from_numpy(ids2).to(dev))
+    ids1 = synth.route_uniform(g, 50000, 256, 8)
+    st, ref_st = _compare(moe, moe.MoeDesc(50000, 8, 256, 8, 8), torch.from_numpy(ids1).to(dev))
+    assert st == ref_st == moe.MOE_OK
+    ids2 = g.integers(-1, 96, size=(70000, 6)).astype(np.int32)
+    st, ref_st = _compare(moe, moe.MoeDesc(70000, 6, 96, 12, 8), torch.from_numpy(ids2).to(dev))
+    assert st == ref_st == moe.MOE_OK
+
+
+def test_noalloc_matches_moe_layout_on_the_pages_workloads():
+    from combine_moe_layout_03_gb300 import moe
+    dev = torch.device("cuda:0")
+    c = synth.prefill_case(seed=11)
+    st, ref_st = _compare(moe, moe.MoeDesc(4096, 8, 256, 8, 7168),
+                          torch.from_numpy(c["topk_idx"]).to(dev))
+    assert st == ref_st == moe.MOE_OK
+    c = synth.skewed_case(seed=4)
+    st, ref_st = _compare(moe, moe.MoeDesc(16384, 8, 256, 16, 7168),
+                          torch.from_numpy(c["topk_idx"]).to(dev))
     assert st == ref_st == moe.MOE_OK
 
 
