@@ -61,6 +61,11 @@ def workload_spec(name: str) -> dict:
                  out_kind="bf16", record_bytes=16 + 32 + 32 + 16384,
                  text="reduce-scatter workload R=4 H=8192 512 tokens/rank (8 MiB/rank); "
                       "BF16 dispatch; top-8 of 256 combine grouped by rank")
+    elif name == "prefill_norm":
+        s = dict(num_tokens=4096, hidden=7168, num_experts=256, topk=8, num_ranks=8,
+                 out_kind="fp8", record_bytes=7472, norm=True,
+                 text="prefill N=4096 H=7168 E=256 top-8 R=8; FP8 dispatch; BF16 combine "
+                      "grouped by rank fused with residual add and RMSNorm")
     elif name == "tiny":
         s = dict(num_tokens=128, hidden=1024, num_experts=16, topk=2, num_ranks=2,
                  out_kind="bf16", record_bytes=2096,
@@ -75,6 +80,8 @@ def workload_spec(name: str) -> dict:
         dispatch=in_row + 4 * k + 4 * k + 4 * k + k * s["record_bytes"],  # row, ids, w, slots in; k records out
         combine=k * 2 * h + 4 * k * 3 + 2 * h,                # k expert rows, w, slots, ids in; row out
     )
+    if s.get("norm"):  # + residual in, normed and new residual out
+        s["bytes_per_token"]["combine"] += 2 * 2 * h
     s["name"] = name
     return s
 
@@ -82,7 +89,7 @@ def workload_spec(name: str) -> dict:
 def make_inputs(spec: dict, seed: int = 0) -> dict:
     from combine_moe_layout_03_gb300 import synth
     n = spec["num_tokens"]
-    if spec["name"] == "prefill":
+    if spec["name"] in ("prefill", "prefill_norm"):
         return synth.prefill_case(seed=seed, n=n)
     if spec["name"] == "skewed":
         return synth.skewed_case(seed=seed, n=n)
@@ -247,8 +254,19 @@ class Step:
         self.layout = moe.prepare_layout(self.desc, self.ids, self.lay, self.ws)
         self.dispatch = moe.prepare_dispatch(self.desc, self.ids, self.w, self.x, self.sc,
                                              self.lay["slot_of"], self.records)
-        self.combine = moe.prepare_combine(self.cdesc, moe.MOE_COMBINE_TOPK_RANKS, self.y,
-                                           self.ids, self.w, self.lay["slot_of"], self.out)
+        if spec.get("norm"):
+            from combine_moe_layout_03_gb300 import synth
+            self.residual = torch.from_numpy(synth.bf16_normal(synth.rng_for(seed, 12), (n, h))
+                                             .view(np.int16)).to(dev).view(torch.bfloat16)
+            self.gamma = torch.from_numpy(synth.bf16_normal(synth.rng_for(seed, 13), (h,))
+                                          .view(np.int16)).to(dev).view(torch.bfloat16)
+            self.residual_out = torch.empty_like(self.out)
+            self.combine = moe.prepare_combine_norm(
+                self.cdesc, moe.MOE_COMBINE_TOPK_RANKS, self.y, self.ids, self.w,
+                self.lay["slot_of"], self.residual, self.gamma, 1e-6, self.out, self.residual_out)
+        else:
+            self.combine = moe.prepare_combine(self.cdesc, moe.MOE_COMBINE_TOPK_RANKS, self.y,
+                                               self.ids, self.w, self.lay["slot_of"], self.out)
 
     def run(self):
         self.layout()
@@ -322,7 +340,8 @@ def run_ours(args, spec, rank, world):
         "config": {"workload": spec["text"], "num_tokens": n, "hidden": spec["hidden"],
                    "num_experts": spec["num_experts"], "topk": spec["topk"],
                    "num_ranks": spec["num_ranks"], "record_bytes": spec["record_bytes"],
-                   "combine_mode": "TOPK_RANKS",
+                   "combine_mode": "TOPK_RANKS + residual + RMSNorm" if spec.get("norm")
+                   else "TOPK_RANKS",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, then "
                          f"{L2_FLUSH_BYTES >> 20} MiB read, outside the timed events); step "
                          f"working set {step_bytes / 1e6:.0f} MB",
@@ -475,7 +494,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill",
-                    choices=["prefill", "decode", "rs", "skewed", "tiny"])
+                    choices=["prefill", "decode", "rs", "skewed", "tiny", "prefill_norm"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

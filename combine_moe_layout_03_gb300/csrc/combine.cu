@@ -53,6 +53,91 @@ __device__ __forceinline__ uint4 pack8(const float* a) {
   return o;
 }
 
+// The valid pairs of one token, ordered by (rank, j) when GROUP (else by j),
+// spread over the warp: lane m holds the m-th pair's slot and weight; bit m of
+// lastmask says whether pair m closes its rank group. Lanes 0..k-1 bring the
+// token's (slot, weight, expert) in j order. All lanes must call it.
+struct PairList {
+  int slot;
+  float w;
+  unsigned lastmask;
+  int n;
+};
+
+template <bool GROUP>
+__device__ __forceinline__ PairList order_pairs(int slot, float w, int idx, int k, int64_t rows,
+                                                int experts_per_rank) {
+  const int lane = (int)lane_id();
+  const bool valid = lane < k && slot >= 0 && (int64_t)slot < rows;
+  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+  PairList out;
+  out.n = __popc(vmask);
+  const int key = GROUP ? (valid ? idx / experts_per_rank : 0) : 0;
+  // position of this lane's pair in (key, j) order among the valid pairs
+  int pos;
+  if (GROUP) {
+    pos = 0;
+    for (int l = 0; l < k; ++l) {
+      const int kl = __shfl_sync(0xffffffffu, key, l);
+      pos += ((vmask >> l) & 1u) && (kl < key || (kl == key && l < lane));
+    }
+  } else {
+    pos = __popc(vmask & ((1u << lane) - 1u));
+  }
+  // lane m takes the pair at position m
+  int src = 0;
+  for (int l = 0; l < k; ++l) {
+    const int pl = __shfl_sync(0xffffffffu, pos, l);
+    if (((vmask >> l) & 1u) && pl == lane) src = l;
+  }
+  out.slot = __shfl_sync(0xffffffffu, slot, src);
+  out.w = __shfl_sync(0xffffffffu, w, src);
+  out.lastmask = 0;
+  if (GROUP) {
+    const int o_key = __shfl_sync(0xffffffffu, key, src);
+    const int next_key = __shfl_down_sync(0xffffffffu, o_key, 1);
+    out.lastmask = __ballot_sync(0xffffffffu, lane < out.n && (lane == out.n - 1 || next_key != o_key));
+  }
+  return out;
+}
+
+// One 16-byte column chunk of a token's combine, in fp32 (before rounding):
+// GROUP = false: the fma chain over the ordered pairs; GROUP = true: the sum
+// of the rank groups' chains. col points at the chunk's column in row 0 of
+// expert_out. All lanes must call it (on = whether this lane's chunk exists).
+template <bool GROUP>
+__device__ __forceinline__ void combine_chunk(const PairList& pl, const uint8_t* col,
+                                              size_t row_bytes, bool on, float* res) {
+  float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float total[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int m0 = 0; m0 < pl.n; m0 += kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      v[b] = make_uint4(0, 0, 0, 0);
+      if (m0 + b < pl.n) {
+        const int sl = __shfl_sync(0xffffffffu, pl.slot, m0 + b);
+        if (on) v[b] = ld_stream_v4(col + (size_t)sl * row_bytes);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (m0 + b < pl.n) {
+        fma8(part, __shfl_sync(0xffffffffu, pl.w, m0 + b), v[b]);
+        if (GROUP && ((pl.lastmask >> (m0 + b)) & 1u)) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            total[i] = __fadd_rn(total[i], part[i]);
+            part[i] = 0.0f;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) res[i] = GROUP ? total[i] : part[i];
+}
+
 // GROUP = false: out = bf16(fma chain over j ascending)            (TOPK)
 // GROUP = true:  out = bf16(sum over ranks ascending of the rank's
 //                fma chain over its pairs, j ascending)             (TOPK_RANKS)
@@ -89,69 +174,128 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 3)
     const int c0 = (int)(u % units_per_token) * chunks_per_unit;
     const int c1 = min(c0 + chunks_per_unit, chunks);
 
-    const bool valid = slot >= 0 && (int64_t)slot < p.expert_out_rows;
-    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-    const int n = __popc(vmask);
-    const int key = GROUP ? (valid ? idx / p.experts_per_rank : 0) : 0;
-    // position of this lane's pair in (key, j) order among the valid pairs
-    int pos;
-    if (GROUP) {
-      pos = 0;
-      for (int l = 0; l < k; ++l) {
-        const int kl = __shfl_sync(0xffffffffu, key, l);
-        pos += ((vmask >> l) & 1u) && (kl < key || (kl == key && l < lane));
-      }
-    } else {
-      pos = __popc(vmask & ((1u << lane) - 1u));
-    }
-    // lane m takes the pair at position m
-    int src = 0;
-    for (int l = 0; l < k; ++l) {
-      const int pl = __shfl_sync(0xffffffffu, pos, l);
-      if (((vmask >> l) & 1u) && pl == lane) src = l;
-    }
-    const int o_slot = __shfl_sync(0xffffffffu, slot, src);
-    const float o_w = __shfl_sync(0xffffffffu, w, src);
-    unsigned lastmask = 0;
-    if (GROUP) {
-      const int o_key = __shfl_sync(0xffffffffu, key, src);
-      const int next_key = __shfl_down_sync(0xffffffffu, o_key, 1);
-      lastmask = __ballot_sync(0xffffffffu, lane < n && (lane == n - 1 || next_key != o_key));
-    }
-
+    const PairList pl = order_pairs<GROUP>(slot, w, idx, k, p.expert_out_rows, p.experts_per_rank);
     for (int cb = c0; cb < c1; cb += 32) {
       const int c = cb + lane;
       const bool on = c < c1;
-      const uint8_t* col = p.expert_out + (size_t)c * 16;
-      float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      float total[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int m0 = 0; m0 < n; m0 += kBatch) {
-        uint4 v[kBatch];
+      float res[8];
+      combine_chunk<GROUP>(pl, p.expert_out + (size_t)c * 16, row_bytes, on, res);
+      // TOPK rounds its single chain as it is (a chain that underflows to -0
+      // stays -0); TOPK_RANKS rounds the sum of the rank partials.
+      if (on) st_v4(p.out + (size_t)t * row_bytes + (size_t)c * 16, pack8(res));
+    }
+  }
+}
+
+
+// Combine fused with the residual add and RMSNorm that follow it (vLLM
+// compare view ds-exp-2...ds-exp-ag, moe_rs_fused.cu: reduce-scatter + residual
+// + RMSNorm in one kernel). One block per token. For every 16-byte chunk of
+// the row: x = (the combine of MODE in fp32, before rounding) + residual;
+// residual_out = bf16(x); the thread keeps x in registers. One block
+// reduction gives sum(x^2); normed = bf16((x * rsqrt(sum/H + eps)) * gamma).
+constexpr int kNormThreads = 256;
+
+template <int CPT, int MODE>
+__global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams q) {
+  const CombineParams& p = q.c;
+  __shared__ float red[kNormThreads / 32];
+  const int t = blockIdx.x;
+  const int lane = (int)lane_id(), warp = threadIdx.x >> 5;
+  const int k = p.topk;
+  const int chunks = p.hidden_size / 8;
+  const size_t row_bytes = (size_t)p.hidden_size * 2;
+  constexpr bool GROUP = MODE == MOE_COMBINE_TOPK_RANKS;
+
+  PairList pl;
+  pl.n = 0;
+  pl.slot = -1;
+  pl.w = 0.0f;
+  pl.lastmask = 0;
+  if (MODE != MOE_COMBINE_RANKS) {
+    int slot = -1, idx = 0;
+    float w = 0.0f;
+    if (lane < k) {
+      const int64_t qq = (int64_t)t * k + lane;
+      slot = p.slot_of[qq];
+      w = p.topk_weights[qq];
+      if (GROUP) idx = p.topk_idx[qq];
+    }
+    pl = order_pairs<GROUP>(slot, w, idx, k, p.expert_out_rows, p.experts_per_rank);
+  }
+
+  float xs[CPT][8];
+  float ss = 0.0f;
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
+  for (int i = 0; i < CPT; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    const bool on = c < chunks;
+    float* x = xs[i];
+    if (MODE == MOE_COMBINE_RANKS) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+      const size_t rank_stride = (size_t)p.num_tokens * row_bytes;
+      const uint8_t* src = p.expert_out + (size_t)t * row_bytes + (size_t)c * 16;
+      for (int r0 = 0; r0 < p.num_ranks; r0 += 4) {
+        uint4 v[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
           v[b] = make_uint4(0, 0, 0, 0);
-          if (m0 + b < n) {
-            const int sl = __shfl_sync(0xffffffffu, o_slot, m0 + b);
-            if (on) v[b] = ld_stream_v4(col + (size_t)sl * row_bytes);
-          }
+          if (on && r0 + b < p.num_ranks) v[b] = ld_stream_v4(src + (size_t)(r0 + b) * rank_stride);
         }
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          if (m0 + b < n) {
-            fma8(part, __shfl_sync(0xffffffffu, o_w, m0 + b), v[b]);
-            if (GROUP && ((lastmask >> (m0 + b)) & 1u)) {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                total[i] = __fadd_rn(total[i], part[i]);
-                part[i] = 0.0f;
-              }
-            }
+        for (int b = 0; b < 4; ++b) {
+          if (r0 + b < p.num_ranks) {
+            x[0] = __fadd_rn(x[0], bf16_lo(v[b].x));
+            x[1] = __fadd_rn(x[1], bf16_hi(v[b].x));
+            x[2] = __fadd_rn(x[2], bf16_lo(v[b].y));
+            x[3] = __fadd_rn(x[3], bf16_hi(v[b].y));
+            x[4] = __fadd_rn(x[4], bf16_lo(v[b].z));
+            x[5] = __fadd_rn(x[5], bf16_hi(v[b].z));
+            x[6] = __fadd_rn(x[6], bf16_lo(v[b].w));
+            x[7] = __fadd_rn(x[7], bf16_hi(v[b].w));
           }
         }
       }
-      // TOPK rounds its single chain as it is (a chain that underflows to -0
-      // stays -0); TOPK_RANKS rounds the sum of the rank partials.
-      if (on) st_v4(p.out + (size_t)t * row_bytes + (size_t)c * 16, pack8(GROUP ? total : part));
+    } else {
+      combine_chunk<GROUP>(pl, p.expert_out + (size_t)c * 16, row_bytes, on, x);
+    }
+    uint4 rv = make_uint4(0, 0, 0, 0);
+    if (on) rv = ld_stream_v4(q.residual_in + (size_t)t * row_bytes + (size_t)c * 16);
+    x[0] = __fadd_rn(x[0], bf16_lo(rv.x));
+    x[1] = __fadd_rn(x[1], bf16_hi(rv.x));
+    x[2] = __fadd_rn(x[2], bf16_lo(rv.y));
+    x[3] = __fadd_rn(x[3], bf16_hi(rv.y));
+    x[4] = __fadd_rn(x[4], bf16_lo(rv.z));
+    x[5] = __fadd_rn(x[5], bf16_hi(rv.z));
+    x[6] = __fadd_rn(x[6], bf16_lo(rv.w));
+    x[7] = __fadd_rn(x[7], bf16_hi(rv.w));
+    if (on) {
+      st_v4(q.residual_out + (size_t)t * row_bytes + (size_t)c * 16, pack8(x));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = __fmaf_rn(x[j], x[j], ss);
+    }
+  }
+  // block sum of squares
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  float tot = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+  const float scale = rsqrtf(__fadd_rn(__fdiv_rn(tot, (float)p.hidden_size), q.eps));
+#pragma unroll
+  for (int i = 0; i < CPT; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    if (c < chunks) {
+      const uint4 g = *reinterpret_cast<const uint4*>(q.gamma + (size_t)c * 16);
+      const float gv[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
+                           bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
+      float y[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(__fmul_rn(xs[i][j], scale), gv[j]);
+      st_v4(q.normed_out + (size_t)t * row_bytes + (size_t)c * 16, pack8(y));
     }
   }
 }
@@ -258,6 +402,27 @@ cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t 
   const int64_t cap = (int64_t)di->sms * 8;
   if (blocks > cap) blocks = cap;
   k_combine_ranks<4><<<(unsigned)blocks, 256, 0, s>>>(partials, out, chunks, num_ranks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_norm(const CombineNormParams& p, cudaStream_t s) {
+  const int chunks = p.c.hidden_size / 8;
+  const int cpt = (chunks + kNormThreads - 1) / kNormThreads;
+  const dim3 grid((unsigned)p.c.num_tokens), block(kNormThreads);
+#define MOE_NORM_LAUNCH(C)                                                                  \
+  do {                                                                                      \
+    if (p.mode == MOE_COMBINE_TOPK)                                                         \
+      k_combine_norm<C, MOE_COMBINE_TOPK><<<grid, block, 0, s>>>(p);                        \
+    else if (p.mode == MOE_COMBINE_RANKS)                                                   \
+      k_combine_norm<C, MOE_COMBINE_RANKS><<<grid, block, 0, s>>>(p);                       \
+    else                                                                                    \
+      k_combine_norm<C, MOE_COMBINE_TOPK_RANKS><<<grid, block, 0, s>>>(p);                  \
+  } while (0)
+  if (cpt <= 1) MOE_NORM_LAUNCH(1);
+  else if (cpt <= 2) MOE_NORM_LAUNCH(2);
+  else if (cpt <= 4) MOE_NORM_LAUNCH(4);
+  else MOE_NORM_LAUNCH(8);
+#undef MOE_NORM_LAUNCH
   return cudaGetLastError();
 }
 

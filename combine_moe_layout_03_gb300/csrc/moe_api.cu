@@ -240,6 +240,54 @@ int moe_combine(const moe_desc_t* desc, int mode, const void* expert_out, int64_
   return cuda_status(moe::launch_combine_topk(p, s));
 }
 
+int moe_combine_norm(const moe_desc_t* desc, int mode, const void* expert_out,
+                     int64_t expert_out_rows, const int32_t* topk_idx, const float* topk_weights,
+                     const int32_t* slot_of, const void* residual_in, const void* gamma, float eps,
+                     void* normed_out, void* residual_out, moe_stream_t stream) {
+  int rc = check_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens, H = desc->hidden, R = desc->num_ranks;
+  if (mode != MOE_COMBINE_TOPK && mode != MOE_COMBINE_RANKS && mode != MOE_COMBINE_TOPK_RANKS)
+    return MOE_ERR_INVALID_ARG;
+  if (H < 8 || H % 8 || H > moe::kMaxHiddenNorm) return MOE_ERR_SHAPE;
+  if (mode != MOE_COMBINE_TOPK && N % R) return MOE_ERR_SHAPE;
+  if (!(eps >= 0.0f) || eps > 3.0e38f) return MOE_ERR_INVALID_ARG;
+  if (N == 0) return MOE_OK;
+  if (!expert_out || !residual_in || !gamma || !normed_out || !residual_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(expert_out, 16) || !aligned(residual_in, 16) || !aligned(gamma, 16) ||
+      !aligned(normed_out, 16) || !aligned(residual_out, 16))
+    return MOE_ERR_ALIGNMENT;
+  if (expert_out_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (mode == MOE_COMBINE_RANKS) {
+    if (expert_out_rows < (int64_t)R * N) return MOE_ERR_CAPACITY;
+  } else {
+    if (!topk_weights || !slot_of) return MOE_ERR_INVALID_ARG;
+    if (mode == MOE_COMBINE_TOPK_RANKS && !topk_idx) return MOE_ERR_INVALID_ARG;
+    if (!aligned(topk_weights, 4) || !aligned(slot_of, 4) || !aligned(topk_idx, 4))
+      return MOE_ERR_ALIGNMENT;
+  }
+  moe::CombineNormParams p;
+  p.c.expert_out = (const uint8_t*)expert_out;
+  p.c.expert_out_rows = expert_out_rows;
+  p.c.topk_idx = topk_idx;
+  p.c.topk_weights = topk_weights;
+  p.c.slot_of = slot_of;
+  p.c.out = nullptr;
+  p.c.num_tokens = N;
+  p.c.topk = desc->topk;
+  p.c.hidden_size = H;
+  p.c.num_ranks = R;
+  p.c.experts_per_rank = desc->num_experts / R;
+  p.c.group_by_rank = mode == MOE_COMBINE_TOPK_RANKS;
+  p.mode = mode;
+  p.residual_in = (const uint8_t*)residual_in;
+  p.gamma = (const uint8_t*)gamma;
+  p.normed_out = (uint8_t*)normed_out;
+  p.residual_out = (uint8_t*)residual_out;
+  p.eps = eps;
+  return cuda_status(moe::launch_combine_norm(p, (cudaStream_t)stream));
+}
+
 int moe_pack_record(const moe_desc_t* desc, int32_t src_token, int32_t slot_j, int32_t expert,
                     const int32_t* ids_row, const float* w_row, const void* payload_row,
                     const void* scales_row, void* record) {

@@ -56,6 +56,16 @@ struct CombineParams {
   int group_by_rank;  // 1: TOPK_RANKS, 0: TOPK
 };
 
+struct CombineNormParams {
+  CombineParams c;  // expert rows (or rank partials), pairs, shapes; c.out unused
+  int mode;         // MOE_COMBINE_TOPK, MOE_COMBINE_RANKS or MOE_COMBINE_TOPK_RANKS
+  const uint8_t* residual_in;  // bf16 [N, H]
+  const uint8_t* gamma;        // bf16 [H]
+  uint8_t* normed_out;         // bf16 [N, H]
+  uint8_t* residual_out;       // bf16 [N, H]
+  float eps;
+};
+
 // Workspace carving shared by moe_workspace_size and moe_layout.
 constexpr int kLayoutTokensPerChunk = 128;
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
@@ -66,6 +76,8 @@ cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, 
 cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t rows,
                                  int hidden_size, int num_ranks, cudaStream_t s);
+cudaError_t launch_combine_norm(const CombineNormParams& p, cudaStream_t s);
+constexpr int kMaxHiddenNorm = 16384;
 
 #ifdef __CUDACC__
 

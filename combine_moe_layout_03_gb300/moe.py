@@ -73,6 +73,9 @@ _lib.moe_dispatch.restype = ctypes.c_int
 _lib.moe_dispatch.argtypes = [_D] + [_vp] * 6 + [_sz, _vp]
 _lib.moe_combine.restype = ctypes.c_int
 _lib.moe_combine.argtypes = [_D, ctypes.c_int, _vp, _i64, _vp, _vp, _vp, _vp, _vp]
+_lib.moe_combine_norm.restype = ctypes.c_int
+_lib.moe_combine_norm.argtypes = [_D, ctypes.c_int, _vp, _i64, _vp, _vp, _vp, _vp, _vp,
+                                  ctypes.c_float, _vp, _vp, _vp]
 _lib.moe_pack_record.restype = ctypes.c_int
 _lib.moe_pack_record.argtypes = [_D, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
 _lib.moe_unpack_record.restype = ctypes.c_int
@@ -229,6 +232,27 @@ def moe_combine(desc: MoeDesc, mode: int, expert_out: torch.Tensor,
     return out
 
 
+def moe_combine_norm(desc: MoeDesc, mode: int, expert_out: torch.Tensor,
+                     topk_idx: torch.Tensor | None, topk_weights: torch.Tensor | None,
+                     slot_of: torch.Tensor | None, residual_in: torch.Tensor,
+                     gamma: torch.Tensor, eps: float, normed_out: torch.Tensor | None = None,
+                     residual_out: torch.Tensor | None = None, stream=None):
+    """Combine fused with residual add and RMSNorm (see include/moe.h).
+    Returns (normed_out, residual_out), both bf16 [N, H]."""
+    shape = (desc.num_tokens, desc.hidden)
+    if normed_out is None:
+        normed_out = torch.empty(shape, dtype=torch.bfloat16, device=expert_out.device)
+    if residual_out is None:
+        residual_out = torch.empty(shape, dtype=torch.bfloat16, device=expert_out.device)
+    rows = expert_out.numel() // max(desc.hidden, 1)
+    rc = _lib.moe_combine_norm(ctypes.byref(desc.c()), int(mode), _ptr(expert_out), rows,
+                               _ptr(topk_idx), _ptr(topk_weights), _ptr(slot_of),
+                               _ptr(residual_in), _ptr(gamma), float(eps), _ptr(normed_out),
+                               _ptr(residual_out), _stream(stream))
+    _check(rc, "moe_combine_norm")
+    return normed_out, residual_out
+
+
 def moe_pack_record(desc: MoeDesc, src_token: int, slot_j: int, expert: int, ids_row, w_row,
                     payload_row, scales_row):
     """Host-only: builds one record (numpy uint8) from host numpy rows."""
@@ -313,7 +337,19 @@ def prepare_combine(desc: MoeDesc, mode: int, expert_out, topk_idx, topk_weights
     return Prepared("moe_combine", args, (d, expert_out, topk_idx, topk_weights, slot_of, out))
 
 
+def prepare_combine_norm(desc: MoeDesc, mode: int, expert_out, topk_idx, topk_weights, slot_of,
+                         residual_in, gamma, eps: float, normed_out, residual_out,
+                         stream=None) -> Prepared:
+    d = desc.c()
+    rows = expert_out.numel() // max(desc.hidden, 1)
+    args = (ctypes.byref(d), ctypes.c_int(mode), ctypes.c_void_p(_ptr(expert_out)),
+            ctypes.c_int64(rows), *_vps(topk_idx, topk_weights, slot_of, residual_in, gamma),
+            ctypes.c_float(eps), *_vps(normed_out, residual_out), ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_combine_norm", args, (d, expert_out, topk_idx, topk_weights, slot_of,
+                                               residual_in, gamma, normed_out, residual_out))
+
+
 def exported_symbols() -> list[str]:
     return ["moe_strerror", "moe_record_layout", "moe_workspace_size", "moe_layout",
             "moe_layout_status", "moe_dispatch", "moe_combine", "moe_pack_record",
-            "moe_unpack_record", "moe_layout_noalloc"]
+            "moe_unpack_record", "moe_layout_noalloc", "moe_combine_norm"]

@@ -240,6 +240,26 @@ int moe_layout_noalloc(const moe_desc_t* desc, const int32_t* topk_idx,
                        int32_t* slot_of, int32_t* src_of_slot, int32_t* status,
                        moe_stream_t stream);
 
+/* Combine fused with the residual add and RMSNorm that follow it in the layer
+ * (vLLM compare view ds-exp-2...ds-exp-ag, moe_rs_fused.cu: reduce-scatter,
+ * residual add and RMSNorm in one kernel; test_rs_fused.py rms_norm_ref).
+ * mode and expert_out, expert_out_rows, topk_idx, topk_weights, slot_of are as
+ * in moe_combine. For every token t and channel h:
+ *   x[t,h]            = s[t,h] + float(residual_in[t,h])   (fp32)
+ *   residual_out[t,h] = bf16_rn(x[t,h])
+ *   normed_out[t,h]   = bf16_rn((x[t,h] * rsqrt(sum_h x[t,h]^2 / H + eps)) * gamma[h])
+ * where s is the mode's combine in fp32 before its final rounding (the value
+ * moe_combine would round). residual_out is exact; the normed output carries
+ * the rounding of an fp32 sum of squares and of rsqrt (fp32, products in the
+ * order written).
+ * residual_in, normed_out, residual_out: bf16 [N, H]; gamma: bf16 [H]; all
+ * device, 16-byte aligned. eps >= 0. H % 8 == 0 and H <= 16384.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, CAPACITY, CUDA. */
+int moe_combine_norm(const moe_desc_t* desc, int mode, const void* expert_out,
+                     int64_t expert_out_rows, const int32_t* topk_idx, const float* topk_weights,
+                     const int32_t* slot_of, const void* residual_in, const void* gamma, float eps,
+                     void* normed_out, void* residual_out, moe_stream_t stream);
+
 /* Host only: builds one record in host memory `record` (record_bytes bytes)
  * from host rows: ids_row int32 [k], w_row fp32 [k], payload_row
  * (payload_bytes, already in the out_kind format), scales_row (scale_bytes,

@@ -58,6 +58,9 @@ def _load():
                      "oracle_identity_expert", "oracle_combine_topk", "oracle_combine_ranks",
                      "oracle_combine_topk_ranks", "oracle_combine_topk_f64"):
             getattr(_lib, name).restype = i32
+        _lib.oracle_combine_norm.restype = i32
+        _lib.oracle_combine_norm.argtypes = [i32] + [ctypes.c_void_p] * 4 + [i32] * 5 + \
+            [ctypes.c_void_p, ctypes.c_void_p, f32, ctypes.c_void_p, ctypes.c_void_p]
     return _lib
 
 
@@ -235,3 +238,28 @@ def combine_topk_f64(y, topk_weights, slot_of, hidden_size: int) -> np.ndarray:
     _check(_load().oracle_combine_topk_f64(_p(y), _p(w), _p(so), n, k, hidden_size, _p(out)),
            "combine_topk_f64")
     return out
+
+
+def combine_norm(mode: int, y, topk_idx, topk_weights, slot_of, residual, gamma, eps: float,
+                 num_experts: int, num_ranks: int, hidden_size: int):
+    """mode 0 top-k, 1 rank sum (y = partials [R, N, H]), 2 top-k grouped by rank.
+    Returns (normed, residual_out), uint16 BF16 patterns [N, H]."""
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    res = np.ascontiguousarray(residual, dtype=np.uint16)
+    g = np.ascontiguousarray(gamma, dtype=np.uint16)
+    n = res.shape[0]
+    if mode == 1:
+        idx = w = so = None
+        k = 1
+    else:
+        idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+        w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+        so = np.ascontiguousarray(slot_of, dtype=np.int32)
+        k = so.shape[1]
+    normed = np.zeros((n, hidden_size), dtype=np.uint16)
+    rout = np.zeros((n, hidden_size), dtype=np.uint16)
+    rc = _load().oracle_combine_norm(mode, _p(y), _p(idx), _p(w), _p(so), n, k, num_experts,
+                                     num_ranks, hidden_size, _p(res), _p(g), float(eps),
+                                     _p(normed), _p(rout))
+    _check(rc, "combine_norm")
+    return normed, rout

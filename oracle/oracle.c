@@ -481,3 +481,79 @@ int oracle_combine_topk_f64(const uint16_t* y, const float* topk_weights,
   }
   return 0;
 }
+
+/* Combine fused with the residual add and RMSNorm ([AG] moe_rs_fused.cu:
+ * reduce-scatter sum in fp32, add the residual, RMSNorm over the row;
+ * test_rs_fused.py rms_norm_ref: x * rsqrt(mean(x^2) + eps) * gamma in fp32).
+ * For each token t:
+ *   s[h]     = the mode's combine in fp32 before its final rounding, with the
+ *              same operation order as oracle_combine_topk / _ranks /
+ *              _topk_ranks
+ *   x[h]     = s[h] + residual[t,h]                      (fp32 add)
+ *   residual_out[t,h] = bf16(x[h])
+ *   ms       = (sum over h of x[h]^2) / H                (fp64)
+ *   r        = fp32(1 / sqrt(ms + eps))                  (fp64, rounded once)
+ *   normed[t,h] = bf16((x[h] * r) * gamma[h])            (two fp32 products)
+ * Reading: the pages sum the squares in fp32 in a tree order and use rsqrtf;
+ * the oracle takes the exact-as-fp64 mean and one rounding of the scale, so
+ * the normed output agrees with them only within rounding. */
+int oracle_combine_norm(int mode, const uint16_t* y, const int32_t* topk_idx,
+                        const float* topk_weights, const int32_t* slot_of, int num_tokens,
+                        int topk, int num_experts, int num_ranks, int hidden_size,
+                        const uint16_t* residual, const uint16_t* gamma, float eps,
+                        uint16_t* normed, uint16_t* residual_out) {
+  if (mode < 0 || mode > 2 || num_ranks < 1 || hidden_size < 1) return -1;
+  if (mode != 0 && (num_tokens % num_ranks)) return -1;
+  if (mode == 2 && num_experts % num_ranks) return -1;
+  const int per_rank = mode == 2 ? num_experts / num_ranks : 1;
+  const size_t hs = (size_t)hidden_size;
+  float* x = (float*)malloc(sizeof(float) * hs);
+  float* part = (float*)malloc(sizeof(float) * hs);
+  if (!x || !part) {
+    free(x);
+    free(part);
+    return -2;
+  }
+  for (int t = 0; t < num_tokens; ++t) {
+    for (int h = 0; h < hidden_size; ++h) x[h] = 0.0f;
+    if (mode == 0) {
+      for (int j = 0; j < topk; ++j) {
+        long p = (long)t * topk + j;
+        int s = slot_of[p];
+        if (s < 0) continue;
+        float w = topk_weights[p];
+        const uint16_t* row = y + (size_t)s * hs;
+        for (int h = 0; h < hidden_size; ++h) x[h] = fmaf(w, oracle_bf16_to_f32(row[h]), x[h]);
+      }
+    } else if (mode == 1) {
+      for (int r = 0; r < num_ranks; ++r)
+        for (int h = 0; h < hidden_size; ++h)
+          x[h] = x[h] + oracle_bf16_to_f32(y[((size_t)r * num_tokens + t) * hs + h]);
+    } else {
+      for (int r = 0; r < num_ranks; ++r) {
+        for (int h = 0; h < hidden_size; ++h) part[h] = 0.0f;
+        for (int j = 0; j < topk; ++j) {
+          long p = (long)t * topk + j;
+          int s = slot_of[p];
+          if (s < 0 || topk_idx[p] / per_rank != r) continue;
+          float w = topk_weights[p];
+          const uint16_t* row = y + (size_t)s * hs;
+          for (int h = 0; h < hidden_size; ++h) part[h] = fmaf(w, oracle_bf16_to_f32(row[h]), part[h]);
+        }
+        for (int h = 0; h < hidden_size; ++h) x[h] = x[h] + part[h];
+      }
+    }
+    double sumsq = 0.0;
+    for (int h = 0; h < hidden_size; ++h) {
+      x[h] = x[h] + oracle_bf16_to_f32(residual[(size_t)t * hs + h]);
+      residual_out[(size_t)t * hs + h] = oracle_f32_to_bf16(x[h]);
+      sumsq += (double)x[h] * (double)x[h];
+    }
+    float r = (float)(1.0 / sqrt(sumsq / hidden_size + (double)eps));
+    for (int h = 0; h < hidden_size; ++h)
+      normed[(size_t)t * hs + h] = oracle_f32_to_bf16((x[h] * r) * oracle_bf16_to_f32(gamma[h]));
+  }
+  free(x);
+  free(part);
+  return 0;
+}

@@ -68,6 +68,13 @@ int oracle_combine_topk_ranks(const uint16_t* y, const int32_t* topk_idx,
                               const float* topk_weights, const int32_t* slot_of,
                               int num_tokens, int topk, int num_experts, int num_ranks,
                               int hidden_size, uint16_t* out);
+/* Combine + residual add + RMSNorm. mode 0 = top-k (y [P,H]), 1 = rank sum
+ * (y = partials [R][N][H]), 2 = top-k grouped by rank. */
+int oracle_combine_norm(int mode, const uint16_t* y, const int32_t* topk_idx,
+                        const float* topk_weights, const int32_t* slot_of, int num_tokens,
+                        int topk, int num_experts, int num_ranks, int hidden_size,
+                        const uint16_t* residual, const uint16_t* gamma, float eps,
+                        uint16_t* normed, uint16_t* residual_out);
 /* fp64 references, used only to bound the error of the fp32 routines */
 int oracle_combine_topk_f64(const uint16_t* y, const float* topk_weights,
                             const int32_t* slot_of, int num_tokens, int topk,

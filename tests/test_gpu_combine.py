@@ -181,3 +181,61 @@ def test_prepared_calls_match_direct_calls():
     assert torch.equal(lay["slot_of"], ref_lay["slot_of"])
     assert torch.equal(rec, ref_rec)
     assert torch.equal(out, ref_out)
+
+
+def _check_norm(mode, n, k, e, r, h, seed, ranges=None):
+    """Fused combine + residual + RMSNorm against the oracle: residual_out
+    bit-exact, normed within the contract tolerance and at most one BF16 step
+    apart (the sum of squares and rsqrt round differently)."""
+    from combine_moe_layout_03_gb300 import moe
+    g = np.random.default_rng(seed)
+    res = synth.bf16_normal(g, (n, h))
+    gamma = synth.bf16_normal(g, (h,))
+    eps = 1e-6
+    d = moe.MoeDesc(n, k, e, r, h)
+    if mode == moe.MOE_COMBINE_RANKS:
+        y = synth.bf16_normal(g, (r, n, h))
+        ids = w = None
+        so_d = ids_d = w_d = None
+        so = None
+    else:
+        ids = synth.route_uniform(g, n, e, k)
+        ids[: max(1, n // 10), -1] = -1
+        w = synth.weights_softmax(g, n, k)
+        lay = oracle.layout(ids, e, r)
+        so = lay["slot_of"]
+        y = synth.bf16_normal(g, (max(lay["num_pairs"], 1), h))
+        ids_d, w_d = dev_i32(ids), dev_f32(w)
+        so_d = moe.moe_layout(d, ids_d)["slot_of"]
+    normed, rout = moe.moe_combine_norm(d, mode, dev_bf16(y), ids_d, w_d, so_d, dev_bf16(res),
+                                        dev_bf16(gamma), eps)
+    torch.cuda.synchronize()
+    gn, gr = host_bf16(normed), host_bf16(rout)
+    for t0, t1 in (ranges or [(0, n)]):
+        s = slice(t0, t1)
+        if mode == moe.MOE_COMBINE_RANKS:
+            rn, rr = oracle.combine_norm(1, y[:, s], None, None, None, res[s], gamma, eps, e, r, h)
+        else:
+            rn, rr = oracle.combine_norm(mode, y, ids[s], w[s], so[s], res[s], gamma, eps, e, r, h)
+        np.testing.assert_array_equal(gr[s], rr)
+        assert_combine_close(gn[s], rn, f"norm mode {mode}")
+        ulps = np.abs(gn[s].astype(np.int32) - rn.astype(np.int32))
+        assert ulps.max() <= 1
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_combine_norm_tiny_and_ragged(mode):
+    _check_norm(mode, 16, 2, 16, 2, 1024, seed=mode)
+    _check_norm(mode, 24, 6, 96, 12, 264, seed=10 + mode)   # ragged chunks, odd k
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+def test_combine_norm_prefill_size_sampled(mode):
+    _check_norm(mode, 4096, 8, 256, 8, 7168, seed=20 + mode, ranges=[(0, 24), (4072, 4096)])
+
+
+@pytest.mark.parametrize("h", [2048, 8192, 16384])
+def test_combine_norm_rs_shapes(h):
+    from combine_moe_layout_03_gb300 import moe
+    _check_norm(moe.MOE_COMBINE_RANKS, 64, 8, 256, 4, h, seed=h)
+    _check_norm(moe.MOE_COMBINE_TOPK_RANKS, 64, 8, 256, 4, h, seed=h + 1)
