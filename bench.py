@@ -314,14 +314,8 @@ def run_ours(args, spec, rank, world):
     per = {name: [ev[i][a].elapsed_time(ev[i][b]) for i in range(K)]
            for name, a, b in (("layout", 0, 1), ("dispatch", 1, 2), ("combine", 2, 3))}
     step_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(K)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-
     n = spec["num_tokens"]
-    value = n * K * world / (total_ms / 1e3)
+    total_ms, value = whole_job(sum(step_ms), n * K, world, dev)
     peaks = measured_peaks()
     kern = {name: statistics.mean(v) for name, v in per.items()}
     dom = max(("dispatch", "combine"), key=lambda x: kern[x])
@@ -482,9 +476,18 @@ def run_reference(args, spec) -> dict:
 
 # ---------------------------------------------------------------- main -------
 
-def reduce_replicas(values_ms: list[float]) -> float:
-    """Whole-job time of independent replicas: the slowest rank."""
-    return max(values_ms)
+def whole_job(local_ms: float, local_tokens: int, world: int, device=None):
+    """Whole-job time and throughput of independent replicas: the slowest
+    rank's time (max over ranks) and the tokens all ranks processed divided by
+    it. Collective only when world > 1 (any torch.distributed backend)."""
+    total_ms = float(local_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, local_tokens * world / (total_ms / 1e3)
 
 
 def main(argv=None):

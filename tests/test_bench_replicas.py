@@ -1,0 +1,69 @@
+"""The multi-GPU form of the benchmark runs independent replicas (no data-path
+collective): its only cross-rank step is the max over ranks of the timed
+region. Checked here with two gloo ranks on the CPU, and the JSON line's
+host-side pieces without a GPU."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local_ms = 10.0 * (rank + 1)          # rank 1 is the slow one
+    total, value = bench.whole_job(local_ms, 4096 * 5, world, device="cpu")
+    out[rank] = (total, value)
+    dist.destroy_process_group()
+
+
+def test_replicas_take_the_slowest_rank_two_gloo_ranks():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, start_method="spawn")
+        res = dict(out)
+    for rank in range(world):
+        total, value = res[rank]
+        assert total == pytest.approx(20.0)
+        # all ranks' tokens over the slowest rank's time
+        assert value == pytest.approx(2 * 4096 * 5 / 0.020)
+
+
+def test_single_rank_needs_no_collective():
+    total, value = bench.whole_job(8.0, 1000, 1)
+    assert total == 8.0 and value == pytest.approx(1000 / 0.008)
+
+
+def test_workload_bytes_and_launch_counts():
+    s = bench.workload_spec("prefill")
+    k, h = 8, 7168
+    assert s["bytes_per_token"]["dispatch"] == 2 * h + 12 * k + k * 7472
+    assert s["bytes_per_token"]["combine"] == k * 2 * h + 12 * k + 2 * h
+    assert bench.layout_launches(4096, 8, 256, 8) == 1
+    assert bench.layout_launches(50000, 8, 256, 8) == 2   # beyond the cluster's shared memory
+    sn = bench.workload_spec("prefill_norm")
+    assert sn["bytes_per_token"]["combine"] == s["bytes_per_token"]["combine"] + 4 * h
+
+
+def test_reference_arm_prints_a_line(capsys):
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3",
+                "--cpu-seconds", "0.5"])
+    import json
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["cores"] == 1
