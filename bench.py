@@ -189,13 +189,14 @@ def recorded_traffic(kernel: str, workload: str) -> int | None:
 
 def layout_launches(n: int, k: int, e: int, r: int) -> int:
     """Kernels moe_layout launches: one cluster launch while the ids of a
-    cluster block (up to 8 blocks of ~4096 pairs) and its histograms fit in
+    cluster block (up to 16 blocks of ~2048 pairs) and its histograms fit in
     200 KB of shared memory, else two (count, assign). Mirrors layout.cu."""
     pairs = n * k
-    g = min(max(-(-pairs // 4096), 1), 8)
+    per = min(max(pairs // 16, 256), 2048)
+    g = min(max(-(-pairs // per), 1), 16)
     tpb = -(-n // g)
     tpb = (tpb + 3) // 4 * 4
-    smem = (36 + 3 * e + r + 1 + 32 * e) * 4 + tpb * k * 4
+    smem = (36 + 3 * e + r + 1 + 16 * e) * 4 + tpb * k * 4
     return 1 if smem <= 200 * 1024 else 2
 
 

@@ -6,8 +6,9 @@
 // that dispatch and combine use.
 //
 // Design (all integer work, latency- not bandwidth-bound):
-//  * Up to 8 * 4096 pairs (every workload of the pages): one launch of a
-//    thread-block cluster of up to 8 blocks of 1024 threads (k_layout_cluster).
+//  * Whenever a block's ids and histograms fit in shared memory (every
+//    workload of the pages): one launch of a thread-block cluster of up to 16
+//    blocks of 512 threads, about 2048 pairs each (k_layout_cluster).
 //    Each block stages its run of ids in shared memory with 16-byte loads,
 //    builds its expert histogram, rank-mask rows and per-warp histograms
 //    there, and after a hardware cluster barrier reads the other blocks'
@@ -33,9 +34,11 @@ namespace {
 
 constexpr int kCountThreads = 128;   // one thread per token of a chunk
 constexpr int kAssignThreads = 256;  // 8 warps
-constexpr int kClusterThreads = 1024;  // 32 warps
-constexpr int kClusterMaxBlocks = 8;   // portable cluster size
-constexpr int kPairsPerClusterBlock = 4096;
+constexpr int kClusterThreads = 512;   // 16 warps
+constexpr int kClusterMaxBlocks = 16;  // non-portable cluster size where supported, else 8
+constexpr int kClusterPortableBlocks = 8;
+constexpr int kPairsPerClusterBlock = 2048;
+constexpr int kMinPairsPerClusterBlock = 256;
 constexpr size_t kClusterMaxSmem = 200 * 1024;
 
 __device__ __forceinline__ int checked_id(int e, int E, int* bad) {
@@ -327,18 +330,19 @@ __global__ void __launch_bounds__(kAssignThreads) k_layout_assign(LayoutParams p
   clear_src_tail(p, P);
 }
 
-// Everything in one launch: a cluster of G blocks (G <= 8), block c owning a
-// contiguous run of tokens. Each block stages its ids, counts them (shared
-// histogram, rank mask rows, per-warp histograms), then after a cluster
-// barrier reads the other blocks' histograms through distributed shared
-// memory to get the expert totals and its own prefix; one scan gives the
-// offsets, and the block ranks its pairs. No workspace is used except the
-// status word. A final cluster barrier keeps every block's shared memory
-// alive until the others have read it.
+// Everything in one launch: a cluster of G blocks (G <= 16), block c owning a
+// contiguous run of tokens. Each block stages its ids, counts them (rank mask
+// rows, per-warp histograms), then after a cluster barrier reads the other
+// blocks' counts through distributed shared memory to get the expert totals
+// and its own prefix; one scan gives the offsets, and the block ranks its
+// pairs. No workspace is used except the status word. A final cluster
+// barrier keeps every block's shared memory alive until the others have read
+// it.
 __global__ void __launch_bounds__(kClusterThreads) k_layout_cluster(LayoutParams p, int tokens_per_block) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ int smem[];
+  constexpr int NW = kClusterThreads / 32;
   const int E = p.num_experts, R = p.num_ranks, k = p.topk;
   const int G = (int)cluster.num_blocks();
   const int c = (int)cluster.block_rank();
@@ -348,8 +352,8 @@ __global__ void __launch_bounds__(kClusterThreads) k_layout_cluster(LayoutParams
   int* flag = rcnt + R;         // [1] invalid ids seen
   int* base = flag + 1;         // [E]
   int* rank_of = base + E;      // [E]
-  int* whist = rank_of + E;     // [32][E]
-  int* sids = whist + (kClusterThreads / 32) * E;  // [tokens_per_block * k]
+  int* whist = rank_of + E;     // [NW][E]
+  int* sids = whist + NW * E;   // [tokens_per_block * k]
   const int t0 = min(c * tokens_per_block, p.num_tokens);
   const int t1 = min(t0 + tokens_per_block, p.num_tokens);
   const int64_t p0 = (int64_t)t0 * k;
@@ -362,57 +366,64 @@ __global__ void __launch_bounds__(kClusterThreads) k_layout_cluster(LayoutParams
   __syncthreads();
   count_tokens<false>(p, t0, t1, sids, rank_of, cnt, rcnt);
   warp_histograms(E, len, sids, whist);  // starts and ends with a barrier
-  if (threadIdx.x < E) {                 // the block's expert counts
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {  // the block's expert counts
+    int v[NW];
+#pragma unroll
+    for (int w = 0; w < NW; ++w) v[w] = whist[w * E + e];
     int sum = 0;
 #pragma unroll
-    for (int g0 = 0; g0 < kClusterThreads / 32; g0 += 8) {
-      int v[8];
-#pragma unroll
-      for (int w = 0; w < 8; ++w) v[w] = whist[(g0 + w) * E + threadIdx.x];
-#pragma unroll
-      for (int w = 0; w < 8; ++w) sum += v[w];
-    }
-    cnt[threadIdx.x] = sum;
+    for (int w = 0; w < NW; ++w) sum += v[w];
+    cnt[e] = sum;
   }
   cluster.sync();  // every block's cnt/rcnt/flag is final
 
-  // Expert totals and this block's prefix from all blocks' counts: thread e
-  // owns expert e (E <= 1024 = blockDim) and issues its (at most 8) remote
+  // Expert totals and this block's prefix from all blocks' counts. Thread i
+  // owns experts [i*ept, i*ept + ept) (ept <= 2) and issues all its remote
   // loads together, so the exchange costs one distributed-shared-memory round
   // trip.
-  const int e = threadIdx.x;
-  int tot = 0, pre = 0;
-  if (e < E) {
-    int v[kClusterMaxBlocks];
+  const int ept = (E + kClusterThreads - 1) / kClusterThreads;
+  const int e0 = threadIdx.x * ept;
+  int tot[2] = {0, 0}, pre[2] = {0, 0};
 #pragma unroll
-    for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(cnt + e, b) : 0;
+  for (int i = 0; i < 2; ++i) {
+    const int e = e0 + i;
+    if (i < ept && e < E) {
+      int v[kClusterMaxBlocks];
 #pragma unroll
-    for (int b = 0; b < kClusterMaxBlocks; ++b) {
-      tot += v[b];
-      pre += (b < c) ? v[b] : 0;
+      for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(cnt + e, b) : 0;
+#pragma unroll
+      for (int b = 0; b < kClusterMaxBlocks; ++b) {
+        tot[i] += v[b];
+        pre[i] += (b < c) ? v[b] : 0;
+      }
     }
   }
   int total;
-  const int ex = block_exclusive_scan<kClusterThreads>(tot, scratch, &total);
-  if (e < E) {
-    base[e] = ex + pre;
-    if (c == 0) {
-      p.tokens_per_expert[e] = tot;
-      p.expert_offset[e] = ex;
-      if (e % p.experts_per_rank == 0) p.rank_offset[e / p.experts_per_rank] = ex;
+  int ex = block_exclusive_scan<kClusterThreads>(tot[0] + tot[1], scratch, &total);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int e = e0 + i;
+    if (i < ept && e < E) {
+      base[e] = ex + pre[i];
+      if (c == 0) {
+        p.tokens_per_expert[e] = tot[i];
+        p.expert_offset[e] = ex;
+        if (e % p.experts_per_rank == 0) p.rank_offset[e / p.experts_per_rank] = ex;
+      }
+      ex += tot[i];
     }
   }
   if (c == 0) {
-    if (e < R) {
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
       int v[kClusterMaxBlocks];
 #pragma unroll
-      for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(rcnt + e, b) : 0;
+      for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(rcnt + r, b) : 0;
       int sum = 0;
 #pragma unroll
       for (int b = 0; b < kClusterMaxBlocks; ++b) sum += v[b];
-      p.tokens_per_rank[e] = sum;
+      p.tokens_per_rank[r] = sum;
     }
-    if (e == 0) {
+    if (threadIdx.x == 0) {
       int v[kClusterMaxBlocks];
 #pragma unroll
       for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(flag, b) : 0;
@@ -425,7 +436,7 @@ __global__ void __launch_bounds__(kClusterThreads) k_layout_cluster(LayoutParams
     }
   }
   __syncthreads();
-  assign_from_histograms<kClusterThreads / 32>(p, p0, len, sids, base, whist);
+  assign_from_histograms<NW>(p, p0, len, sids, base, whist);
   clear_src_tail(p, total);
   cluster.sync();  // no block leaves while another may still read its counts
 }
@@ -446,42 +457,83 @@ static cudaError_t set_smem(const void* fn, size_t bytes) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-static bool layout_fits_cluster(int num_tokens, int topk, int num_experts, int num_ranks) {
+// Cluster plan for a shape: blocks G and tokens per block. Up to 16 blocks
+// where the device schedules a non-portable cluster of 16 (looked up once per
+// device), else 8.
+struct ClusterPlan {
+  int blocks, tokens_per_block;
+  size_t smem;
+};
+
+static int max_cluster_blocks() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kClusterPortableBlocks;
+  if (cached[dev] == 0) {
+    int best = kClusterPortableBlocks;
+    if (cudaFuncSetAttribute((const void*)k_layout_cluster,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+        cudaFuncSetAttribute((const void*)k_layout_cluster,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterMaxSmem) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(kClusterMaxBlocks);
+      cfg.blockDim = dim3(kClusterThreads);
+      cfg.dynamicSmemBytes = kClusterMaxSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kClusterMaxBlocks;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, (const void*)k_layout_cluster, &cfg) == cudaSuccess && n >= 1)
+        best = kClusterMaxBlocks;
+    }
+    cudaGetLastError();
+    cached[dev] = best;
+  }
+  return cached[dev];
+}
+
+static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int num_ranks, int gmax) {
+  // about kPairsPerClusterBlock pairs per block, but small inputs still
+  // spread over up to gmax blocks of at least kMinPairsPerClusterBlock
   const int64_t pairs = (int64_t)num_tokens * topk;
-  int g = (int)((pairs + kPairsPerClusterBlock - 1) / kPairsPerClusterBlock);
-  g = g < 1 ? 1 : (g > kClusterMaxBlocks ? kClusterMaxBlocks : g);
+  int64_t per = pairs / gmax;
+  if (per < kMinPairsPerClusterBlock) per = kMinPairsPerClusterBlock;
+  if (per > kPairsPerClusterBlock) per = kPairsPerClusterBlock;
+  int g = (int)((pairs + per - 1) / per);
+  g = g < 1 ? 1 : (g > gmax ? gmax : g);
   int tpb = (num_tokens + g - 1) / g;
-  tpb = (tpb + 3) / 4 * 4;
-  const size_t smem = (size_t)(36 + 3 * num_experts + num_ranks + 1 +
-                               (kClusterThreads / 32) * num_experts) * 4 + (size_t)tpb * topk * 4;
-  return smem <= kClusterMaxSmem;
+  tpb = (tpb + 3) / 4 * 4;  // 16-byte aligned id runs per block
+  ClusterPlan cp;
+  cp.blocks = g;
+  cp.tokens_per_block = tpb;
+  cp.smem = (size_t)(36 + 3 * num_experts + num_ranks + 1 + (kClusterThreads / 32) * num_experts) * 4 +
+            (size_t)tpb * topk * 4;
+  return cp;
 }
 
 cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s) {
   const int E = p.num_experts, R = p.num_ranks;
-  const int64_t pairs = (int64_t)p.num_tokens * p.topk;
-  if (layout_fits_cluster(p.num_tokens, p.topk, E, R)) {
-    int g = (int)((pairs + kPairsPerClusterBlock - 1) / kPairsPerClusterBlock);
-    g = g < 1 ? 1 : (g > kClusterMaxBlocks ? kClusterMaxBlocks : g);
-    int tpb = (p.num_tokens + g - 1) / g;
-    tpb = (tpb + 3) / 4 * 4;  // 16-byte aligned id runs per block
-    const size_t smem = (size_t)(36 + 3 * E + R + 1 + (kClusterThreads / 32) * E) * 4 +
-                        (size_t)tpb * p.topk * 4;
-    cudaError_t err = set_smem((const void*)k_layout_cluster, smem);
+  const ClusterPlan cp = cluster_plan(p.num_tokens, p.topk, E, R, max_cluster_blocks());
+  if (cp.smem <= kClusterMaxSmem) {
+    cudaError_t err = set_smem((const void*)k_layout_cluster, cp.smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)g);
+    cfg.gridDim = dim3((unsigned)cp.blocks);
     cfg.blockDim = dim3(kClusterThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = cp.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)g;
+    attr[0].val.clusterDim.x = (unsigned)cp.blocks;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_layout_cluster, p, tpb);
+    return cudaLaunchKernelEx(&cfg, k_layout_cluster, p, cp.tokens_per_block);
   }
   const size_t chunk_ids = (size_t)p.tokens_per_chunk * p.topk;
   const size_t smem_count = (size_t)(2 * E + R + 1) * 4 + chunk_ids * 4;

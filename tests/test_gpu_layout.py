@@ -74,9 +74,11 @@ def test_rs_sizes(t):
     (129, 2, 2, 2),
     (600, 8, 1024, 8),     # two cluster blocks
     (512, 8, 1024, 8),     # exactly one cluster block of 4096 pairs
-    (50000, 8, 256, 8),    # ids of a cluster block exceed shared memory: two-kernel path
-    (20000, 8, 1024, 16),  # large E: two-kernel path
-    (33000, 3, 64, 4),     # eight cluster blocks of 12376 pairs
+    (50000, 8, 256, 8),    # sixteen cluster blocks of 25000 pairs
+    (20000, 8, 1024, 16),  # largest E in the cluster path
+    (33000, 3, 64, 4),
+    (100000, 8, 256, 8),   # ids of a cluster block exceed shared memory: two-kernel path
+    (90000, 8, 512, 16),   # two-kernel path, larger E
 ])
 def test_ragged_and_extreme_shapes(n, k, e, r):
     g = np.random.default_rng(n * 31 + k)

@@ -56,11 +56,11 @@ def test_noalloc_matches_moe_layout_on_two_calls_in_a_row():
     # per-chunk counts in scratch (the two-kernel path): the second call runs
     # on the scratch the first one left behind, with fewer chunks and other E.
     g = np.random.default_rng(12)
-    ids1 = synth.route_uniform(g, 50000, 256, 8)
-    st, ref_st = _compare(moe, moe.MoeDesc(50000, 8, 256, 8, 8), torch.from_numpy(ids1).to(dev))
+    ids1 = synth.route_uniform(g, 100000, 256, 8)
+    st, ref_st = _compare(moe, moe.MoeDesc(100000, 8, 256, 8, 8), torch.from_numpy(ids1).to(dev))
     assert st == ref_st == moe.MOE_OK
-    ids2 = g.integers(-1, 96, size=(70000, 6)).astype(np.int32)
-    st, ref_st = _compare(moe, moe.MoeDesc(70000, 6, 96, 12, 8), torch.from_numpy(ids2).to(dev))
+    ids2 = g.integers(-1, 512, size=(90000, 8)).astype(np.int32)
+    st, ref_st = _compare(moe, moe.MoeDesc(90000, 8, 512, 16, 8), torch.from_numpy(ids2).to(dev))
     assert st == ref_st == moe.MOE_OK
 
 
