@@ -188,16 +188,52 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 3)
 }
 
 
+// The same reduction with one block per token walking its whole row: whole
+// rows per block keep each expert row's bytes streaming from DRAM together,
+// and the low register count lets four blocks share an SM. Used when there
+// are enough tokens to fill the GPU.
+constexpr int kRowThreads = 256;
+constexpr int kRowBlocksPerSm = 4;
+
+template <bool GROUP>
+__global__ void __launch_bounds__(kRowThreads) k_combine_rows(CombineParams p) {
+  const int t = blockIdx.x;
+  const int lane = (int)lane_id();
+  const int k = p.topk;
+  const int chunks = p.hidden_size / 8;
+  const size_t row_bytes = (size_t)p.hidden_size * 2;
+  int slot = -1, idx = 0;
+  float w = 0.0f;
+  if (lane < k) {
+    const int64_t qq = (int64_t)t * k + lane;
+    slot = p.slot_of[qq];
+    w = p.topk_weights[qq];
+    if (GROUP) idx = p.topk_idx[qq];
+  }
+  const PairList pl = order_pairs<GROUP>(slot, w, idx, k, p.expert_out_rows, p.experts_per_rank);
+  for (int cb = 0; cb < chunks; cb += kRowThreads) {  // uniform trip count per warp
+    const int c = cb + (int)threadIdx.x;
+    const bool on = c < chunks;
+    float res[8];
+    combine_chunk<GROUP>(pl, p.expert_out + (size_t)c * 16, row_bytes, on, res);
+    if (on) st_v4(p.out + (size_t)t * row_bytes + (size_t)c * 16, pack8(res));
+  }
+}
+
 // Combine fused with the residual add and RMSNorm that follow it (vLLM
 // compare view ds-exp-2...ds-exp-ag, moe_rs_fused.cu: reduce-scatter + residual
-// + RMSNorm in one kernel). One block per token. For every 16-byte chunk of
-// the row: x = (the combine of MODE in fp32, before rounding) + residual;
-// residual_out = bf16(x); the thread keeps x in registers. One block
-// reduction gives sum(x^2); normed = bf16((x * rsqrt(sum/H + eps)) * gamma).
+// + RMSNorm in one kernel). One block per token. For each 16-byte chunk of
+// the row a thread forms x = (the combine of MODE in fp32, before rounding) +
+// residual, writes residual_out = bf16(x) and parks x in shared memory (so
+// registers stay low and several blocks share an SM, keeping loads in
+// flight while a block waits at its reduction). One block reduction gives
+// sum(x^2); normed = bf16((x * rsqrt(sum/H + eps)) * gamma).
 constexpr int kNormThreads = 256;
 
-template <int CPT, int MODE>
+template <int MODE>
 __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams q) {
+  extern __shared__ float4 xsm4[];  // [chunks][2] float4 = the row's x in fp32
+  float* xsm = reinterpret_cast<float*>(xsm4);
   const CombineParams& p = q.c;
   __shared__ float red[kNormThreads / 32];
   const int t = blockIdx.x;
@@ -224,13 +260,11 @@ __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams
     pl = order_pairs<GROUP>(slot, w, idx, k, p.expert_out_rows, p.experts_per_rank);
   }
 
-  float xs[CPT][8];
   float ss = 0.0f;
-#pragma unroll
-  for (int i = 0; i < CPT; ++i) {
-    const int c = threadIdx.x + i * kNormThreads;
+  for (int cb = 0; cb < chunks; cb += kNormThreads) {  // uniform trip count per warp
+    const int c = cb + (int)threadIdx.x;
     const bool on = c < chunks;
-    float* x = xs[i];
+    float x[8];
     if (MODE == MOE_COMBINE_RANKS) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = 0.0f;
@@ -260,23 +294,23 @@ __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams
     } else {
       combine_chunk<GROUP>(pl, p.expert_out + (size_t)c * 16, row_bytes, on, x);
     }
-    uint4 rv = make_uint4(0, 0, 0, 0);
-    if (on) rv = ld_stream_v4(q.residual_in + (size_t)t * row_bytes + (size_t)c * 16);
-    x[0] = __fadd_rn(x[0], bf16_lo(rv.x));
-    x[1] = __fadd_rn(x[1], bf16_hi(rv.x));
-    x[2] = __fadd_rn(x[2], bf16_lo(rv.y));
-    x[3] = __fadd_rn(x[3], bf16_hi(rv.y));
-    x[4] = __fadd_rn(x[4], bf16_lo(rv.z));
-    x[5] = __fadd_rn(x[5], bf16_hi(rv.z));
-    x[6] = __fadd_rn(x[6], bf16_lo(rv.w));
-    x[7] = __fadd_rn(x[7], bf16_hi(rv.w));
     if (on) {
+      const uint4 rv = ld_stream_v4(q.residual_in + (size_t)t * row_bytes + (size_t)c * 16);
+      x[0] = __fadd_rn(x[0], bf16_lo(rv.x));
+      x[1] = __fadd_rn(x[1], bf16_hi(rv.x));
+      x[2] = __fadd_rn(x[2], bf16_lo(rv.y));
+      x[3] = __fadd_rn(x[3], bf16_hi(rv.y));
+      x[4] = __fadd_rn(x[4], bf16_lo(rv.z));
+      x[5] = __fadd_rn(x[5], bf16_hi(rv.z));
+      x[6] = __fadd_rn(x[6], bf16_lo(rv.w));
+      x[7] = __fadd_rn(x[7], bf16_hi(rv.w));
       st_v4(q.residual_out + (size_t)t * row_bytes + (size_t)c * 16, pack8(x));
 #pragma unroll
       for (int j = 0; j < 8; ++j) ss = __fmaf_rn(x[j], x[j], ss);
+      xsm4[2 * c] = make_float4(x[0], x[1], x[2], x[3]);
+      xsm4[2 * c + 1] = make_float4(x[4], x[5], x[6], x[7]);
     }
   }
-  // block sum of squares
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) red[warp] = ss;
@@ -285,18 +319,15 @@ __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams
 #pragma unroll
   for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
   const float scale = rsqrtf(__fadd_rn(__fdiv_rn(tot, (float)p.hidden_size), q.eps));
+  for (int c = threadIdx.x; c < chunks; c += kNormThreads) {
+    const uint4 g = *reinterpret_cast<const uint4*>(q.gamma + (size_t)c * 16);
+    const float gv[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
+                         bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
+    const float* x = xsm + 8 * c;
+    float y[8];
 #pragma unroll
-  for (int i = 0; i < CPT; ++i) {
-    const int c = threadIdx.x + i * kNormThreads;
-    if (c < chunks) {
-      const uint4 g = *reinterpret_cast<const uint4*>(q.gamma + (size_t)c * 16);
-      const float gv[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
-                           bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
-      float y[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(__fmul_rn(xs[i][j], scale), gv[j]);
-      st_v4(q.normed_out + (size_t)t * row_bytes + (size_t)c * 16, pack8(y));
-    }
+    for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(__fmul_rn(x[j], scale), gv[j]);
+    st_v4(q.normed_out + (size_t)t * row_bytes + (size_t)c * 16, pack8(y));
   }
 }
 
@@ -371,6 +402,13 @@ const DeviceInfo* device_info() {
 cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorInvalidDevice;
+  if (p.num_tokens >= di->sms * kRowBlocksPerSm * 2) {  // enough tokens: one block per row
+    if (p.group_by_rank)
+      k_combine_rows<true><<<(unsigned)p.num_tokens, kRowThreads, 0, s>>>(p);
+    else
+      k_combine_rows<false><<<(unsigned)p.num_tokens, kRowThreads, 0, s>>>(p);
+    return cudaGetLastError();
+  }
   const int chunks = p.hidden_size / 8;
   const int steps_per_token = (chunks + 31) / 32;  // warp steps of 32 chunks
   const int g = p.group_by_rank ? 1 : 0;
@@ -406,24 +444,17 @@ cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t 
 }
 
 cudaError_t launch_combine_norm(const CombineNormParams& p, cudaStream_t s) {
-  const int chunks = p.c.hidden_size / 8;
-  const int cpt = (chunks + kNormThreads - 1) / kNormThreads;
-  const dim3 grid((unsigned)p.c.num_tokens), block(kNormThreads);
-#define MOE_NORM_LAUNCH(C)                                                                  \
-  do {                                                                                      \
-    if (p.mode == MOE_COMBINE_TOPK)                                                         \
-      k_combine_norm<C, MOE_COMBINE_TOPK><<<grid, block, 0, s>>>(p);                        \
-    else if (p.mode == MOE_COMBINE_RANKS)                                                   \
-      k_combine_norm<C, MOE_COMBINE_RANKS><<<grid, block, 0, s>>>(p);                       \
-    else                                                                                    \
-      k_combine_norm<C, MOE_COMBINE_TOPK_RANKS><<<grid, block, 0, s>>>(p);                  \
-  } while (0)
-  if (cpt <= 1) MOE_NORM_LAUNCH(1);
-  else if (cpt <= 2) MOE_NORM_LAUNCH(2);
-  else if (cpt <= 4) MOE_NORM_LAUNCH(4);
-  else MOE_NORM_LAUNCH(8);
-#undef MOE_NORM_LAUNCH
-  return cudaGetLastError();
+  const size_t smem = (size_t)p.c.hidden_size * 4;  // the row's x in fp32
+  const void* fn = p.mode == MOE_COMBINE_TOPK    ? (const void*)k_combine_norm<MOE_COMBINE_TOPK>
+                   : p.mode == MOE_COMBINE_RANKS ? (const void*)k_combine_norm<MOE_COMBINE_RANKS>
+                                                 : (const void*)k_combine_norm<MOE_COMBINE_TOPK_RANKS>;
+  if (smem > 48 * 1024) {
+    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  CombineNormParams q = p;
+  void* args[] = {&q};
+  return cudaLaunchKernel(fn, dim3((unsigned)p.c.num_tokens), dim3(kNormThreads), args, smem, s);
 }
 
 }  // namespace moe
