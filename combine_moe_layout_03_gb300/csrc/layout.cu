@@ -295,17 +295,27 @@ __device__ int64_t scan_chunks(const LayoutParams& p, int c, int* base, int* scr
     ex += tot;
   }
   if (blockIdx.x == 0) {
-    if (threadIdx.x == 0) {
-      p.expert_offset[E] = total;
-      p.rank_offset[R] = total;
-      int f = 0;
-      for (int c2 = 0; c2 < C; ++c2) f |= __ldcg(&p.chunk_flag[c2]);
-      *p.status = f ? MOE_ERR_DEVICE_IDS : MOE_OK;
-    }
-    for (int r = threadIdx.x; r < R; r += NT) {
+    // per-rank token counts and the invalid-id flag over all chunks, 8
+    // independent loads in flight per thread
+    for (int r = threadIdx.x; r <= R; r += NT) {
       int s = 0;
-      for (int c2 = 0; c2 < C; ++c2) s += __ldcg(&p.chunk_rank[(int64_t)c2 * R + r]);
-      p.tokens_per_rank[r] = s;
+      for (int c0 = 0; c0 < C; c0 += 8) {
+        int v[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+          v[b] = (c0 + b < C) ? __ldcg(r < R ? &p.chunk_rank[(int64_t)(c0 + b) * R + r]
+                                             : &p.chunk_flag[c0 + b])
+                              : 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) s = (r < R) ? s + v[b] : (s | v[b]);
+      }
+      if (r < R) {
+        p.tokens_per_rank[r] = s;
+      } else {
+        p.expert_offset[E] = total;
+        p.rank_offset[R] = total;
+        *p.status = s ? MOE_ERR_DEVICE_IDS : MOE_OK;
+      }
     }
   }
   __syncthreads();
