@@ -275,6 +275,63 @@ class Step:
         self.combine()
 
 
+def run_ag_slots(args, rank, world):
+    """The decode all-gather's data path on one GPU: mask padded tokens, pack
+    8 ranks x 256 tokens of (ids, weights, NVFP4 payload, scales) into
+    16-byte-aligned rank slots, and unpack them into the gathered tensors."""
+    import torch
+    from combine_moe_layout_03_gb300 import moe, synth
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    r, n = 8, 256
+    c = synth.decode_case(seed=rank, n=r * n)
+    ts = [torch.from_numpy(np.ascontiguousarray(c[key])).to(dev)
+          for key in ("topk_idx", "topk_weights", "payload", "scales")]
+    n_act = torch.tensor([r * n - 3], dtype=torch.int32, device=dev)
+    slots = moe.moe_pack_slots(ts, r)
+    outs = [torch.empty_like(t) for t in ts]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        moe.moe_mask_topk_ids(ts[0], n_act)
+        moe.moe_pack_slots(ts, r, slots)
+        moe.moe_unpack_slots(slots, outs, r)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        flush_read.sum()
+        ev[i][0].record()
+        moe.moe_mask_topk_ids(ts[0], n_act)
+        ev[i][1].record()
+        moe.moe_pack_slots(ts, r, slots)
+        ev[i][2].record()
+        moe.moe_unpack_slots(slots, outs, r)
+        ev[i][3].record()
+    torch.cuda.synchronize()
+    per = {name: statistics.mean(ev[i][a].elapsed_time(ev[i][b]) for i in range(K))
+           for name, a, b in (("mask", 0, 1), ("pack", 1, 2), ("unpack", 2, 3))}
+    total_ms, value = whole_job(sum(ev[i][0].elapsed_time(ev[i][3]) for i in range(K)),
+                                r * n * K, world, dev)
+    slot_bytes = slots.numel()
+    peak = measured_peaks()
+    gbs = {name: 2 * slot_bytes / (per[name] / 1e3) / 1e9 for name in ("pack", "unpack")}
+    return {
+        "metric": "decode all-gather slot packing tokens/s and HBM GB/s", "value": round(value, 1),
+        "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(total_ms / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bytes", "data": "synthetic",
+        "config": {"workload": "decode all-gather payload: 8 ranks x 256 tokens, top-8 ids and "
+                               "weights, 3584 B NVFP4 + 448 B scales per token; mask, pack, unpack",
+                   "slot_bytes_per_rank": slot_bytes // r},
+        "kernels_us": {k: round(v * 1e3, 2) for k, v in per.items()},
+        "kernels_gbs": {k: round(v, 1) for k, v in gbs.items()},
+        "kernels_frac": {k: round(v / peak["hbm_gbs"], 4) for k, v in gbs.items()},
+        "gpu_launches": 3 * K,
+    }
+
+
 def run_ours(args, spec, rank, world):
     import torch
     import torch.distributed as dist
@@ -498,16 +555,19 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill",
-                    choices=["prefill", "decode", "rs", "skewed", "tiny", "prefill_norm"])
+                    choices=["prefill", "decode", "rs", "skewed", "tiny", "prefill_norm",
+                             "ag_slots"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
-    spec = workload_spec(args.workload)
+    spec = workload_spec(args.workload) if args.workload != "ag_slots" else None
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
+        if spec is None:
+            raise SystemExit("the reference arm covers the dispatch/combine workloads")
         if rank == 0:
             print(json.dumps(run_reference(args, spec)), flush=True)
         return 0
@@ -518,7 +578,7 @@ def main(argv=None):
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group("nccl")
-    line = run_ours(args, spec, rank, world)
+    line = run_ag_slots(args, rank, world) if spec is None else run_ours(args, spec, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

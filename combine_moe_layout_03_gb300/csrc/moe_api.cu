@@ -288,6 +288,73 @@ int moe_combine_norm(const moe_desc_t* desc, int mode, const void* expert_out,
   return cuda_status(moe::launch_combine_norm(p, (cudaStream_t)stream));
 }
 
+int moe_slot_layout(const moe_slot_desc_t* desc, int64_t* offsets, int64_t* slot_bytes) {
+  if (!desc || !offsets || !slot_bytes) return MOE_ERR_INVALID_ARG;
+  if (desc->num_tensors < 2 || desc->num_tensors > MOE_MAX_SLOT_TENSORS || desc->num_ranks < 1)
+    return MOE_ERR_INVALID_ARG;
+  int64_t cursor = 0;
+  for (int i = 0; i < desc->num_tensors; ++i) {
+    if (desc->bytes[i] < 0) return MOE_ERR_INVALID_ARG;
+    if (desc->bytes[i] % 16) return MOE_ERR_ALIGNMENT;
+    cursor = (cursor + 15) / 16 * 16;
+    offsets[i] = cursor;
+    cursor += desc->bytes[i];
+  }
+  *slot_bytes = cursor;
+  return MOE_OK;
+}
+
+static int slots_call(bool pack, const moe_slot_desc_t* desc, const void* const* tensors_in,
+                      void* const* tensors_out, const void* slots_in, void* slots_out,
+                      moe_stream_t stream) {
+  int64_t off[MOE_MAX_SLOT_TENSORS];
+  int64_t sb = 0;
+  int rc = moe_slot_layout(desc, off, &sb);
+  if (rc != MOE_OK) return rc;
+  const void* src[MOE_MAX_SLOT_TENSORS] = {};
+  void* dst[MOE_MAX_SLOT_TENSORS] = {};
+  if (pack) {
+    if (!tensors_in || !slots_out) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < desc->num_tensors; ++i) {
+      if (!tensors_in[i] && desc->bytes[i]) return MOE_ERR_INVALID_ARG;
+      if (!aligned(tensors_in[i], 16)) return MOE_ERR_ALIGNMENT;
+      src[i] = tensors_in[i];
+    }
+    if (!aligned(slots_out, 16)) return MOE_ERR_ALIGNMENT;
+    dst[0] = slots_out;
+  } else {
+    if (!tensors_out || !slots_in) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < desc->num_tensors; ++i) {
+      if (!tensors_out[i] && desc->bytes[i]) return MOE_ERR_INVALID_ARG;
+      if (!aligned(tensors_out[i], 16)) return MOE_ERR_ALIGNMENT;
+      dst[i] = tensors_out[i];
+    }
+    if (!aligned(slots_in, 16)) return MOE_ERR_ALIGNMENT;
+    src[0] = slots_in;
+  }
+  return cuda_status(moe::launch_slots(pack, src, dst, desc, off, sb, (cudaStream_t)stream));
+}
+
+int moe_pack_slots(const moe_slot_desc_t* desc, const void* const* tensors, void* slots,
+                   moe_stream_t stream) {
+  return slots_call(true, desc, tensors, nullptr, nullptr, slots, stream);
+}
+
+int moe_unpack_slots(const moe_slot_desc_t* desc, const void* slots, void* const* tensors,
+                     moe_stream_t stream) {
+  return slots_call(false, desc, nullptr, tensors, slots, nullptr, stream);
+}
+
+int moe_mask_topk_ids(int32_t* topk_idx, int32_t num_tokens, int32_t topk,
+                      const int32_t* num_actual_tokens, moe_stream_t stream) {
+  if (num_tokens < 0 || topk < 1 || topk > MOE_MAX_TOPK) return MOE_ERR_SHAPE;
+  if ((int64_t)num_tokens * topk >= ((int64_t)1 << 31)) return MOE_ERR_SHAPE;
+  if (!num_actual_tokens || (num_tokens > 0 && !topk_idx)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 4) || !aligned(num_actual_tokens, 4)) return MOE_ERR_ALIGNMENT;
+  return cuda_status(moe::launch_mask_topk_ids(topk_idx, (int64_t)num_tokens * topk, topk,
+                                               num_actual_tokens, (cudaStream_t)stream));
+}
+
 int moe_pack_record(const moe_desc_t* desc, int32_t src_token, int32_t slot_j, int32_t expert,
                     const int32_t* ids_row, const float* w_row, const void* payload_row,
                     const void* scales_row, void* record) {

@@ -77,6 +77,11 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t rows,
                                  int hidden_size, int num_ranks, cudaStream_t s);
 cudaError_t launch_combine_norm(const CombineNormParams& p, cudaStream_t s);
+cudaError_t launch_slots(bool pack, const void* const* src, void* const* dst,
+                         const moe_slot_desc_t* d, const int64_t* offsets, int64_t slot_bytes,
+                         cudaStream_t s);
+cudaError_t launch_mask_topk_ids(int32_t* ids, int64_t total, int topk, const int32_t* num_actual,
+                                 cudaStream_t s);
 constexpr int kMaxHiddenNorm = 16384;
 
 #ifdef __CUDACC__

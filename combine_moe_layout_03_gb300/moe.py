@@ -76,6 +76,21 @@ _lib.moe_combine.argtypes = [_D, ctypes.c_int, _vp, _i64, _vp, _vp, _vp, _vp, _v
 _lib.moe_combine_norm.restype = ctypes.c_int
 _lib.moe_combine_norm.argtypes = [_D, ctypes.c_int, _vp, _i64, _vp, _vp, _vp, _vp, _vp,
                                   ctypes.c_float, _vp, _vp, _vp]
+
+
+class _SlotDesc(ctypes.Structure):
+    _fields_ = [("num_tensors", _i32), ("num_ranks", _i32), ("bytes", _i64 * 4)]
+
+
+_SD = ctypes.POINTER(_SlotDesc)
+_lib.moe_slot_layout.restype = ctypes.c_int
+_lib.moe_slot_layout.argtypes = [_SD, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
+_lib.moe_pack_slots.restype = ctypes.c_int
+_lib.moe_pack_slots.argtypes = [_SD, ctypes.POINTER(_vp), _vp, _vp]
+_lib.moe_unpack_slots.restype = ctypes.c_int
+_lib.moe_unpack_slots.argtypes = [_SD, _vp, ctypes.POINTER(_vp), _vp]
+_lib.moe_mask_topk_ids.restype = ctypes.c_int
+_lib.moe_mask_topk_ids.argtypes = [_vp, _i32, _i32, _vp, _vp]
 _lib.moe_pack_record.restype = ctypes.c_int
 _lib.moe_pack_record.argtypes = [_D, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
 _lib.moe_unpack_record.restype = ctypes.c_int
@@ -253,6 +268,55 @@ def moe_combine_norm(desc: MoeDesc, mode: int, expert_out: torch.Tensor,
     return normed_out, residual_out
 
 
+def _slot_desc(num_ranks: int, sizes) -> _SlotDesc:
+    d = _SlotDesc()
+    d.num_tensors = len(sizes)
+    d.num_ranks = num_ranks
+    for i, b in enumerate(sizes):
+        d.bytes[i] = int(b)
+    return d
+
+
+def moe_slot_layout(num_ranks: int, bytes_per_rank) -> tuple[list[int], int]:
+    """Offsets of the tensors in a rank slot and the slot size (host only)."""
+    d = _slot_desc(num_ranks, bytes_per_rank)
+    off = (_i64 * 4)()
+    sb = _i64(0)
+    _check(_lib.moe_slot_layout(ctypes.byref(d), off, ctypes.byref(sb)), "moe_slot_layout")
+    return [off[i] for i in range(len(bytes_per_rank))], sb.value
+
+
+def moe_pack_slots(tensors: list, num_ranks: int, slots: torch.Tensor | None = None, stream=None):
+    """Packs tensors (each rank-major, numel divisible by num_ranks) into
+    slots uint8 [R, slot_bytes]."""
+    sizes = [t.numel() * t.element_size() // num_ranks for t in tensors]
+    _, sb = moe_slot_layout(num_ranks, sizes)
+    if slots is None:
+        slots = torch.empty((num_ranks, sb), dtype=torch.uint8, device=tensors[0].device)
+    d = _slot_desc(num_ranks, sizes)
+    arr = (_vp * 4)(*[_ptr(t) for t in tensors])
+    _check(_lib.moe_pack_slots(ctypes.byref(d), arr, _ptr(slots), _stream(stream)), "moe_pack_slots")
+    return slots
+
+
+def moe_unpack_slots(slots: torch.Tensor, outputs: list, num_ranks: int, stream=None):
+    """Fills outputs (rank-major) from slots [R, slot_bytes]."""
+    sizes = [t.numel() * t.element_size() // num_ranks for t in outputs]
+    d = _slot_desc(num_ranks, sizes)
+    arr = (_vp * 4)(*[_ptr(t) for t in outputs])
+    _check(_lib.moe_unpack_slots(ctypes.byref(d), _ptr(slots), arr, _stream(stream)),
+           "moe_unpack_slots")
+    return outputs
+
+
+def moe_mask_topk_ids(topk_idx: torch.Tensor, num_actual_tokens: torch.Tensor, stream=None):
+    """Sets ids of tokens at or past the device scalar num_actual_tokens to -1."""
+    n, k = topk_idx.shape
+    _check(_lib.moe_mask_topk_ids(_ptr(topk_idx), n, k, _ptr(num_actual_tokens), _stream(stream)),
+           "moe_mask_topk_ids")
+    return topk_idx
+
+
 def moe_pack_record(desc: MoeDesc, src_token: int, slot_j: int, expert: int, ids_row, w_row,
                     payload_row, scales_row):
     """Host-only: builds one record (numpy uint8) from host numpy rows."""
@@ -352,4 +416,5 @@ def prepare_combine_norm(desc: MoeDesc, mode: int, expert_out, topk_idx, topk_we
 def exported_symbols() -> list[str]:
     return ["moe_strerror", "moe_record_layout", "moe_workspace_size", "moe_layout",
             "moe_layout_status", "moe_dispatch", "moe_combine", "moe_pack_record",
-            "moe_unpack_record", "moe_layout_noalloc", "moe_combine_norm"]
+            "moe_unpack_record", "moe_layout_noalloc", "moe_combine_norm", "moe_slot_layout",
+            "moe_pack_slots", "moe_unpack_slots", "moe_mask_topk_ids"]

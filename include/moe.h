@@ -260,6 +260,44 @@ int moe_combine_norm(const moe_desc_t* desc, int mode, const void* expert_out,
                      const int32_t* slot_of, const void* residual_in, const void* gamma, float eps,
                      void* normed_out, void* residual_out, moe_stream_t stream);
 
+/* ---- tensor-major rank slots and padded-token mask ----------------------
+ * The decode all-gather of the vLLM compare view ds-exp-2...ds-exp-ag packs
+ * each rank's 2-4 tensors (top-k ids, weights, hidden payload, scales) into
+ * one slot, one after the other at 16-byte-aligned offsets (moe_allgather.cu
+ * "Host launcher", make_desc), and the gathered output of tensor i is every
+ * rank's tensor i in rank order. Here the R ranks are regions of one GPU: the
+ * tensors are [R][bytes[i]] (rank-major) and the slots [R][slot_bytes]. */
+#define MOE_MAX_SLOT_TENSORS 4
+typedef struct {
+  int32_t num_tensors; /* 2..4 */
+  int32_t num_ranks;   /* >= 1 */
+  int64_t bytes[MOE_MAX_SLOT_TENSORS]; /* bytes of tensor i per rank, multiples of 16 */
+} moe_slot_desc_t;
+
+/* Host only. offsets[i] of tensor i inside a slot (num_tensors entries) and
+ * the slot size. Errors: INVALID_ARG (NULL, num_tensors outside 2..4,
+ * num_ranks < 1, negative size), ALIGNMENT (a size not a multiple of 16, as
+ * make_desc rejects it). */
+int moe_slot_layout(const moe_slot_desc_t* desc, int64_t* offsets, int64_t* slot_bytes);
+
+/* Packs tensor i of rank r into slots[r] at offsets[i]. tensors is a host
+ * array of num_tensors device pointers; all device pointers 16-byte aligned.
+ * Errors: as moe_slot_layout, plus ALIGNMENT, CUDA. */
+int moe_pack_slots(const moe_slot_desc_t* desc, const void* const* tensors, void* slots,
+                   moe_stream_t stream);
+
+/* The inverse: tensor i of rank r from slots[r] at offsets[i]. */
+int moe_unpack_slots(const moe_slot_desc_t* desc, const void* slots, void* const* tensors,
+                     moe_stream_t stream);
+
+/* Padded tokens (vLLM all2all.py mask_topk_ids): topk_idx[t, :] = -1 for
+ * every t >= *num_actual_tokens, where num_actual_tokens is a device int32
+ * read by the kernel (a negative count masks every token), so a captured CUDA
+ * graph stays valid as the count changes. topk_idx: device int32 [N, k].
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, CUDA. */
+int moe_mask_topk_ids(int32_t* topk_idx, int32_t num_tokens, int32_t topk,
+                      const int32_t* num_actual_tokens, moe_stream_t stream);
+
 /* Host only: builds one record in host memory `record` (record_bytes bytes)
  * from host rows: ids_row int32 [k], w_row fp32 [k], payload_row
  * (payload_bytes, already in the out_kind format), scales_row (scale_bytes,

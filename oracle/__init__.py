@@ -58,6 +58,9 @@ def _load():
                      "oracle_identity_expert", "oracle_combine_topk", "oracle_combine_ranks",
                      "oracle_combine_topk_ranks", "oracle_combine_topk_f64"):
             getattr(_lib, name).restype = i32
+        for name in ("oracle_slot_layout", "oracle_pack_slots", "oracle_unpack_slots"):
+            getattr(_lib, name).restype = i32
+        _lib.oracle_mask_topk_ids.restype = None
         _lib.oracle_combine_norm.restype = i32
         _lib.oracle_combine_norm.argtypes = [i32] + [ctypes.c_void_p] * 4 + [i32] * 5 + \
             [ctypes.c_void_p, ctypes.c_void_p, f32, ctypes.c_void_p, ctypes.c_void_p]
@@ -263,3 +266,42 @@ def combine_norm(mode: int, y, topk_idx, topk_weights, slot_of, residual, gamma,
                                      _p(normed), _p(rout))
     _check(rc, "combine_norm")
     return normed, rout
+
+
+def slot_layout(bytes_per_rank):
+    b = np.ascontiguousarray(bytes_per_rank, dtype=np.int64)
+    off = np.zeros(len(b), np.int64)
+    sb = np.zeros(1, np.int64)
+    _check(_load().oracle_slot_layout(len(b), _p(b), _p(off), _p(sb)), "slot_layout")
+    return off.tolist(), int(sb[0])
+
+
+def _ptr_array(arrs):
+    return (ctypes.c_void_p * 4)(*[a.ctypes.data for a in arrs])
+
+
+def pack_slots(tensors, num_ranks: int) -> np.ndarray:
+    """tensors: rank-major numpy arrays; returns uint8 slots [R, slot_bytes]."""
+    ts = [np.ascontiguousarray(t).view(np.uint8).reshape(-1) for t in tensors]
+    b = np.array([t.size // num_ranks for t in ts], np.int64)
+    _, sb = slot_layout(b)
+    slots = np.zeros((num_ranks, sb), np.uint8)
+    _check(_load().oracle_pack_slots(len(ts), num_ranks, _p(b), _ptr_array(ts), _p(slots)),
+           "pack_slots")
+    return slots
+
+
+def unpack_slots(slots, bytes_per_rank, num_ranks: int):
+    s = np.ascontiguousarray(slots, dtype=np.uint8)
+    b = np.ascontiguousarray(bytes_per_rank, dtype=np.int64)
+    outs = [np.zeros(int(x) * num_ranks, np.uint8) for x in b]
+    _check(_load().oracle_unpack_slots(len(b), num_ranks, _p(b), _p(s), _ptr_array(outs)),
+           "unpack_slots")
+    return outs
+
+
+def mask_topk_ids(topk_idx, num_actual_tokens: int) -> np.ndarray:
+    ids = np.array(topk_idx, dtype=np.int32, copy=True, order="C")
+    n, k = ids.shape
+    _load().oracle_mask_topk_ids(_p(ids), n, k, int(num_actual_tokens))
+    return ids

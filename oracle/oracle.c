@@ -557,3 +557,55 @@ int oracle_combine_norm(int mode, const uint16_t* y, const int32_t* topk_idx,
   free(part);
   return 0;
 }
+
+/* ======================================================================== */
+/* Rank slots and padded tokens                                              */
+/* ======================================================================== */
+
+/* [AG] moe_allgather.cu make_desc: a cursor walks the tensors in order; each
+ * tensor starts at the cursor rounded up to 16 and must have a byte size that
+ * is a multiple of 16; the slot is the final cursor. */
+int oracle_slot_layout(int num_tensors, const int64_t* bytes, int64_t* offsets, int64_t* slot_bytes) {
+  if (num_tensors < 2 || num_tensors > 4) return -1;
+  int64_t cursor = 0;
+  for (int i = 0; i < num_tensors; ++i) {
+    if (bytes[i] < 0 || bytes[i] % 16) return -1;
+    cursor = (cursor + 15) / 16 * 16;
+    offsets[i] = cursor;
+    cursor += bytes[i];
+  }
+  *slot_bytes = cursor;
+  return 0;
+}
+
+/* Slot r holds tensor i of rank r (bytes[i] bytes at tensor + r*bytes[i]) at
+ * offsets[i]; the gathered tensor i is all ranks' pieces in rank order. */
+int oracle_pack_slots(int num_tensors, int num_ranks, const int64_t* bytes,
+                      const uint8_t* const* tensors, uint8_t* slots) {
+  int64_t off[4], sb;
+  if (oracle_slot_layout(num_tensors, bytes, off, &sb) != 0 || num_ranks < 1) return -1;
+  for (int r = 0; r < num_ranks; ++r)
+    for (int i = 0; i < num_tensors; ++i)
+      for (int64_t b = 0; b < bytes[i]; ++b)
+        slots[(size_t)r * sb + off[i] + b] = tensors[i][(size_t)r * bytes[i] + b];
+  return 0;
+}
+
+int oracle_unpack_slots(int num_tensors, int num_ranks, const int64_t* bytes,
+                        const uint8_t* slots, uint8_t* const* tensors) {
+  int64_t off[4], sb;
+  if (oracle_slot_layout(num_tensors, bytes, off, &sb) != 0 || num_ranks < 1) return -1;
+  for (int r = 0; r < num_ranks; ++r)
+    for (int i = 0; i < num_tensors; ++i)
+      for (int64_t b = 0; b < bytes[i]; ++b)
+        tensors[i][(size_t)r * bytes[i] + b] = slots[(size_t)r * sb + off[i] + b];
+  return 0;
+}
+
+/* [AG] all2all.py mask_topk_ids: every token t >= num_actual_tokens gets -1
+ * in each of its k ids. */
+void oracle_mask_topk_ids(int32_t* topk_idx, int num_tokens, int topk, int num_actual_tokens) {
+  for (int t = 0; t < num_tokens; ++t)
+    if (t >= num_actual_tokens)
+      for (int j = 0; j < topk; ++j) topk_idx[(long)t * topk + j] = -1;
+}

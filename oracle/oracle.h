@@ -75,6 +75,14 @@ int oracle_combine_norm(int mode, const uint16_t* y, const int32_t* topk_idx,
                         int topk, int num_experts, int num_ranks, int hidden_size,
                         const uint16_t* residual, const uint16_t* gamma, float eps,
                         uint16_t* normed, uint16_t* residual_out);
+/* Rank slots of the decode all-gather ([AG] make_desc) and the padded-token
+ * mask ([AG] mask_topk_ids). */
+int oracle_slot_layout(int num_tensors, const int64_t* bytes, int64_t* offsets, int64_t* slot_bytes);
+int oracle_pack_slots(int num_tensors, int num_ranks, const int64_t* bytes,
+                      const uint8_t* const* tensors, uint8_t* slots);
+int oracle_unpack_slots(int num_tensors, int num_ranks, const int64_t* bytes,
+                        const uint8_t* slots, uint8_t* const* tensors);
+void oracle_mask_topk_ids(int32_t* topk_idx, int num_tokens, int topk, int num_actual_tokens);
 /* fp64 references, used only to bound the error of the fp32 routines */
 int oracle_combine_topk_f64(const uint16_t* y, const float* topk_weights,
                             const int32_t* slot_of, int num_tokens, int topk,
