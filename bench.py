@@ -66,6 +66,11 @@ def workload_spec(name: str) -> dict:
                  out_kind="fp8", record_bytes=7472, norm=True,
                  text="prefill N=4096 H=7168 E=256 top-8 R=8; FP8 dispatch; BF16 combine "
                       "grouped by rank fused with residual add and RMSNorm")
+    elif name == "prefill_ranks":
+        s = dict(num_tokens=4096, hidden=7168, num_experts=256, topk=8, num_ranks=8,
+                 out_kind="fp8", record_bytes=7472, per_rank=True,
+                 text="prefill N=4096 H=7168 E=256 top-8 R=8; one record per (token, rank) "
+                      "(FP8 dispatch), rank rows summed back (BF16 combine)")
     elif name == "tiny":
         s = dict(num_tokens=128, hidden=1024, num_experts=16, topk=2, num_ranks=2,
                  out_kind="bf16", record_bytes=2096,
@@ -89,7 +94,7 @@ def workload_spec(name: str) -> dict:
 def make_inputs(spec: dict, seed: int = 0) -> dict:
     from combine_moe_layout_03_gb300 import synth
     n = spec["num_tokens"]
-    if spec["name"] in ("prefill", "prefill_norm"):
+    if spec["name"] in ("prefill", "prefill_norm", "prefill_ranks"):
         return synth.prefill_case(seed=seed, n=n)
     if spec["name"] == "skewed":
         return synth.skewed_case(seed=seed, n=n)
@@ -250,6 +255,9 @@ class Step:
             yy = synth.bf16_normal(synth.rng_for(seed, 11), (n * k, h))
             self.y = torch.from_numpy(yy.view(np.int16)).to(dev).view(torch.bfloat16)
         self.launches_per_step = layout_launches(n, k, e, r) + 1 + 1
+        if spec.get("per_rank"):
+            self._setup_per_rank(spec, dev, seed)
+            return
         # the three calls with their arguments marshalled once (same buffers
         # every step), so host overhead stays well below the GPU's step time
         self.layout = moe.prepare_layout(self.desc, self.ids, self.lay, self.ws)
@@ -268,6 +276,49 @@ class Step:
         else:
             self.combine = moe.prepare_combine(self.cdesc, moe.MOE_COMBINE_TOPK_RANKS, self.y,
                                                self.ids, self.w, self.lay["slot_of"], self.out)
+
+    def _setup_per_rank(self, spec, dev, seed):
+        """One record per (token, rank): the rank layout runs after the layout
+        (both timed as 'layout'); the expert of rank r returns, per received
+        token, the sum of its local pairs' weight times the dequantised row."""
+        import torch
+        moe = self.moe
+        n, h = spec["num_tokens"], spec["hidden"]
+        self.rlay = moe.moe_rank_layout(self.desc, self.lay)
+        recv = int(self.rlay["recv_offset"][-1].item())
+        self.records = torch.empty((n * spec["num_ranks"], spec["record_bytes"]), dtype=torch.uint8,
+                                   device=dev)
+        moe.moe_dispatch_ranks(self.desc, self.ids, self.w, self.x, self.sc,
+                               self.rlay["send_head"], self.records)
+        torch.cuda.synchronize()
+        rl = moe.moe_record_layout(self.desc)
+        rec = self.records[:recv]
+        q = rec[:, rl["off_payload"]:rl["off_payload"] + h].contiguous().view(torch.float8_e4m3fn)
+        sc = rec[:, rl["off_scales"]:rl["off_scales"] + 4 * (h // 128)].contiguous().view(torch.float32)
+        lw = rec[:, rl["off_weights"]:rl["off_weights"] + 4 * spec["topk"]].contiguous().view(torch.float32)
+        self.y = (q.float() * sc.repeat_interleave(128, dim=1) * lw.sum(1, keepdim=True)).to(torch.bfloat16)
+        self.recv_records = recv
+        lay_prep = moe.prepare_layout(self.desc, self.ids, self.lay, self.ws)
+        d, lay, rlay = self.desc, self.lay, self.rlay
+
+        def layout_both():
+            lay_prep()
+            moe.moe_rank_layout(d, lay, 1, rlay)
+        self.layout = layout_both
+        self.dispatch = lambda: moe.moe_dispatch_ranks(d, self.ids, self.w, self.x, self.sc,
+                                                       rlay["send_head"], self.records)
+        self.combine = lambda: moe.moe_combine_gather_ranks(self.cdesc, self.y, rlay["send_head"],
+                                                            self.out)
+        self.launches_per_step = layout_launches(n, spec["topk"], spec["num_experts"],
+                                                 spec["num_ranks"]) + 1 + 1 + 1
+        # algorithmic bytes per token from the actual (token, rank) records
+        per = recv / n
+        r = spec["num_ranks"]
+        spec["bytes_per_token"] = dict(
+            layout=12 * spec["topk"] + r + r + 4 * r + 4 * r,  # + mask in, send_head, recv_src_idx out
+            dispatch=2 * h + 12 * spec["topk"] + 4 * r + per * spec["record_bytes"],
+            combine=per * 2 * h + 4 * r + 2 * h,
+        )
 
     def run(self):
         self.layout()
@@ -393,7 +444,7 @@ def run_ours(args, spec, rank, world):
                    "num_experts": spec["num_experts"], "topk": spec["topk"],
                    "num_ranks": spec["num_ranks"], "record_bytes": spec["record_bytes"],
                    "combine_mode": "TOPK_RANKS + residual + RMSNorm" if spec.get("norm")
-                   else "TOPK_RANKS",
+                   else "rank rows gathered per token" if spec.get("per_rank") else "TOPK_RANKS",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, then "
                          f"{L2_FLUSH_BYTES >> 20} MiB read, outside the timed events); step "
                          f"working set {step_bytes / 1e6:.0f} MB",
@@ -556,7 +607,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill",
                     choices=["prefill", "decode", "rs", "skewed", "tiny", "prefill_norm",
-                             "ag_slots"])
+                             "prefill_ranks", "ag_slots"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

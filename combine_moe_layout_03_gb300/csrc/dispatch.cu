@@ -177,6 +177,90 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p)
   }
 }
 
+// One record per (token, destination rank) instead of per (token, expert)
+// (DeepEP Buffer::intranode_dispatch): the payload is built once in shared
+// memory exactly as above; thread r then writes the record for rank r at
+// send_head[t, r]. Its first segment (record bytes [0, off_payload)) is
+//   header: int32 src_token, int32 rank, int32 number of local pairs, int32 0
+//   ids:    topk_idx[t, j] - r*E/R for experts on rank r, else -1
+//   weights: topk_weights[t, j] for experts on rank r, else 0
+// (padding zero), written with 16-byte stores; payload and scales go to the
+// bulk-copy engine.
+template <int OUT_KIND>
+__global__ void __launch_bounds__(kDispatchThreads)
+    k_dispatch_ranks(DispatchParams p, const int32_t* send_head, int num_ranks, int experts_per_rank) {
+  extern __shared__ __align__(128) uint8_t img[];  // record bytes [off_payload, record_bytes)
+  __shared__ int s_ids[MOE_MAX_TOPK];
+  __shared__ uint32_t s_w[MOE_MAX_TOPK];
+  const int t = blockIdx.x;
+  const int k = p.topk;
+  const int tail = p.record_bytes - p.off_payload;
+  const int os = p.off_scales - p.off_payload;
+  constexpr bool kQuant = OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128 || OUT_KIND == MOE_PAYLOAD_NVFP4_B16;
+  uint8_t* stage = img + tail;
+  const uint8_t* row = p.hidden + (size_t)t * p.in_row_bytes;
+  if (kQuant) {
+    copy_g2s_async(stage, row, p.in_row_bytes / 16);
+  } else {
+    copy_g2s_async(img, row, p.payload_bytes / 16);
+    if (OUT_KIND == MOE_PAYLOAD_RAW && p.scale_bytes > 0)
+      copy_g2s_async(img + os, p.scales + (size_t)t * p.in_scale_bytes, p.scale_bytes / 16);
+  }
+  if (threadIdx.x < k) {
+    const int64_t q = (int64_t)t * k + threadIdx.x;
+    s_ids[threadIdx.x] = p.topk_idx[q];
+    s_w[threadIdx.x] = __float_as_uint(p.topk_weights[q]);
+  }
+  zero_bytes(img, p.payload_bytes, os);
+  zero_bytes(img, os + p.scale_bytes, tail);
+  cp_async_wait_all();
+  __syncthreads();
+  if (OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128) {
+    quant_fp8(stage, p.hidden_size, img, reinterpret_cast<float*>(img + os));
+  } else if (OUT_KIND == MOE_PAYLOAD_NVFP4_B16) {
+    quant_nvfp4(stage, p.hidden_size, img, img + os);
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  if (threadIdx.x < num_ranks) {
+    const int r = threadIdx.x;
+    const int s = send_head[(int64_t)t * num_ranks + r];
+    if (s >= 0 && (int64_t)s < p.record_capacity) {
+      const int lo = r * experts_per_rank, hi = lo + experts_per_rank;
+      int nlocal = 0;
+      for (int j = 0; j < k; ++j) nlocal += (s_ids[j] >= lo && s_ids[j] < hi) ? 1 : 0;
+      const int pad_k = (p.off_weights - p.off_ids) / 4;
+      uint8_t* rec = p.records + (size_t)s * p.record_bytes;
+      for (int v = 0; v < p.off_payload / 16; ++v) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int w = v * 4 + i;
+          uint32_t val = 0;
+          if (w < 4) {
+            val = w == 0 ? (uint32_t)t : w == 1 ? (uint32_t)r : w == 2 ? (uint32_t)nlocal : 0u;
+          } else if (w < 4 + pad_k) {
+            const int j = w - 4;
+            if (j < k) {
+              const int e = s_ids[j];
+              val = (uint32_t)((e >= lo && e < hi) ? e - lo : -1);
+            }
+          } else {
+            const int j = w - 4 - pad_k;
+            if (j < k) val = (s_ids[j] >= lo && s_ids[j] < hi) ? s_w[j] : 0u;
+          }
+          wv[i] = val;
+        }
+        st_v4(rec + 16 * v, make_uint4(wv[0], wv[1], wv[2], wv[3]));
+      }
+      bulk_store_s2g_evict_first(rec + p.off_payload, img, (uint32_t)tail, l2_evict_first_policy());
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, cudaStream_t s) {
@@ -196,6 +280,28 @@ cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, 
   }
   DispatchParams q = p;
   void* args[] = {&q};
+  return cudaLaunchKernel(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), args, smem, s);
+}
+
+cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const int32_t* send_head,
+                                  int num_ranks, int experts_per_rank, cudaStream_t s) {
+  const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16;
+  const size_t smem = (size_t)(p.record_bytes - p.off_payload) + (quant ? (size_t)p.in_row_bytes : 0);
+  const void* fn = nullptr;
+  switch (out_kind) {
+    case MOE_PAYLOAD_BF16: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_BF16>; break;
+    case MOE_PAYLOAD_FP8_E4M3_B128: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_FP8_E4M3_B128>; break;
+    case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_NVFP4_B16>; break;
+    default: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_RAW>; break;
+  }
+  if (smem > 48 * 1024) {
+    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  DispatchParams q = p;
+  const int32_t* sh = send_head;
+  int nr = num_ranks, epr = experts_per_rank;
+  void* args[] = {&q, &sh, &nr, &epr};
   return cudaLaunchKernel(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), args, smem, s);
 }
 

@@ -288,6 +288,99 @@ int moe_combine_norm(const moe_desc_t* desc, int mode, const void* expert_out,
   return cuda_status(moe::launch_combine_norm(p, (cudaStream_t)stream));
 }
 
+int moe_rank_layout(const moe_desc_t* desc, const uint8_t* is_token_in_rank,
+                    const int32_t* tokens_per_rank, const int32_t* tokens_per_expert,
+                    int32_t expert_alignment, int32_t* send_head, int32_t* recv_src_idx,
+                    int32_t* recv_offset, int32_t* recv_tokens_per_expert, moe_stream_t stream) {
+  int rc = check_desc(desc);
+  if (rc != MOE_OK) return rc;
+  if (expert_alignment < 1) return MOE_ERR_INVALID_ARG;
+  const int N = desc->num_tokens, R = desc->num_ranks, E = desc->num_experts;
+  if (!tokens_per_rank || !tokens_per_expert || !recv_offset || !recv_tokens_per_expert)
+    return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!is_token_in_rank || !send_head)) return MOE_ERR_INVALID_ARG;
+  const void* ints[] = {tokens_per_rank, tokens_per_expert, send_head, recv_src_idx, recv_offset,
+                        recv_tokens_per_expert};
+  for (const void* q : ints)
+    if (!aligned(q, 4)) return MOE_ERR_ALIGNMENT;
+  moe::RankLayoutParams p;
+  p.is_token_in_rank = is_token_in_rank;
+  p.tokens_per_rank = tokens_per_rank;
+  p.tokens_per_expert = tokens_per_expert;
+  p.send_head = send_head;
+  p.recv_src_idx = recv_src_idx;
+  p.recv_offset = recv_offset;
+  p.recv_tokens_per_expert = recv_tokens_per_expert;
+  p.num_tokens = N;
+  p.num_ranks = R;
+  p.num_experts = E;
+  p.expert_alignment = expert_alignment;
+  return cuda_status(moe::launch_rank_layout(p, (cudaStream_t)stream));
+}
+
+int moe_dispatch_ranks(const moe_desc_t* desc, const int32_t* topk_idx,
+                       const float* topk_weights, const void* hidden, const void* scales,
+                       const int32_t* send_head, void* records, size_t records_bytes,
+                       moe_stream_t stream) {
+  moe_record_layout_t lay;
+  int rc = record_layout(desc, &lay);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens;
+  if (N == 0) return MOE_OK;
+  const bool raw = desc->out_kind == MOE_PAYLOAD_RAW;
+  if (!topk_idx || !topk_weights || !hidden || !send_head || !records) return MOE_ERR_INVALID_ARG;
+  if (raw && lay.scale_bytes > 0 && !scales) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 4) || !aligned(topk_weights, 4) || !aligned(send_head, 4))
+    return MOE_ERR_ALIGNMENT;
+  if (!aligned(hidden, 16) || !aligned(records, 16) || (raw && scales && !aligned(scales, 16)))
+    return MOE_ERR_ALIGNMENT;
+  if (records_bytes < (size_t)lay.record_bytes) return MOE_ERR_CAPACITY;
+  moe::DispatchParams p;
+  p.topk_idx = topk_idx;
+  p.topk_weights = topk_weights;
+  p.hidden = (const uint8_t*)hidden;
+  p.scales = (const uint8_t*)scales;
+  p.slot_of = nullptr;
+  p.records = (uint8_t*)records;
+  p.record_capacity = (int64_t)(records_bytes / (size_t)lay.record_bytes);
+  p.num_tokens = N;
+  p.topk = desc->topk;
+  p.hidden_size = desc->hidden;
+  p.in_row_bytes = raw ? desc->raw_payload_bytes : 2 * desc->hidden;
+  p.in_scale_bytes = raw ? desc->raw_scale_bytes : 0;
+  p.record_bytes = lay.record_bytes;
+  p.off_ids = lay.off_ids;
+  p.off_weights = lay.off_weights;
+  p.off_payload = lay.off_payload;
+  p.off_scales = lay.off_scales;
+  p.payload_bytes = lay.payload_bytes;
+  p.scale_bytes = lay.scale_bytes;
+  return cuda_status(moe::launch_dispatch_ranks(p, desc->out_kind, send_head, desc->num_ranks,
+                                                desc->num_experts / desc->num_ranks,
+                                                (cudaStream_t)stream));
+}
+
+int moe_combine_gather_ranks(const moe_desc_t* desc, const void* recv_out, int64_t recv_rows,
+                             const int32_t* send_head, void* out, moe_stream_t stream) {
+  int rc = check_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens, H = desc->hidden;
+  if (H < 8 || H % 8) return MOE_ERR_SHAPE;
+  if (N == 0) return MOE_OK;
+  if (!recv_out || !send_head || !out || recv_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned(recv_out, 16) || !aligned(out, 16) || !aligned(send_head, 4))
+    return MOE_ERR_ALIGNMENT;
+  moe::RankCombineParams p;
+  p.recv_out = (const uint8_t*)recv_out;
+  p.rows = recv_rows;
+  p.send_head = send_head;
+  p.out = (uint8_t*)out;
+  p.num_tokens = N;
+  p.num_ranks = desc->num_ranks;
+  p.hidden_size = H;
+  return cuda_status(moe::launch_combine_gather_ranks(p, (cudaStream_t)stream));
+}
+
 int moe_slot_layout(const moe_slot_desc_t* desc, int64_t* offsets, int64_t* slot_bytes) {
   if (!desc || !offsets || !slot_bytes) return MOE_ERR_INVALID_ARG;
   if (desc->num_tensors < 2 || desc->num_tensors > MOE_MAX_SLOT_TENSORS || desc->num_ranks < 1)

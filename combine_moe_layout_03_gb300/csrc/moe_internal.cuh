@@ -66,6 +66,25 @@ struct CombineNormParams {
   float eps;
 };
 
+struct RankLayoutParams {
+  const uint8_t* is_token_in_rank;  // [N, R]
+  const int32_t* tokens_per_rank;   // [R]
+  const int32_t* tokens_per_expert; // [E]
+  int32_t* send_head;               // [N, R]
+  int32_t* recv_src_idx;            // [N * R], may be null
+  int32_t* recv_offset;             // [R + 1]
+  int32_t* recv_tokens_per_expert;  // [E]
+  int num_tokens, num_ranks, num_experts, expert_alignment;
+};
+
+struct RankCombineParams {
+  const uint8_t* recv_out;  // bf16 [rows, H]
+  int64_t rows;
+  const int32_t* send_head; // [N, R]
+  uint8_t* out;             // bf16 [N, H]
+  int num_tokens, num_ranks, hidden_size;
+};
+
 // Workspace carving shared by moe_workspace_size and moe_layout.
 constexpr int kLayoutTokensPerChunk = 128;
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
@@ -80,6 +99,10 @@ cudaError_t launch_combine_norm(const CombineNormParams& p, cudaStream_t s);
 cudaError_t launch_slots(bool pack, const void* const* src, void* const* dst,
                          const moe_slot_desc_t* d, const int64_t* offsets, int64_t slot_bytes,
                          cudaStream_t s);
+cudaError_t launch_rank_layout(const RankLayoutParams& p, cudaStream_t s);
+cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const int32_t* send_head,
+                                  int num_ranks, int experts_per_rank, cudaStream_t s);
+cudaError_t launch_combine_gather_ranks(const RankCombineParams& p, cudaStream_t s);
 cudaError_t launch_mask_topk_ids(int32_t* ids, int64_t total, int topk, const int32_t* num_actual,
                                  cudaStream_t s);
 constexpr int kMaxHiddenNorm = 16384;

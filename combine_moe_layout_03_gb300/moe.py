@@ -89,6 +89,12 @@ _lib.moe_pack_slots.restype = ctypes.c_int
 _lib.moe_pack_slots.argtypes = [_SD, ctypes.POINTER(_vp), _vp, _vp]
 _lib.moe_unpack_slots.restype = ctypes.c_int
 _lib.moe_unpack_slots.argtypes = [_SD, _vp, ctypes.POINTER(_vp), _vp]
+_lib.moe_rank_layout.restype = ctypes.c_int
+_lib.moe_rank_layout.argtypes = [_D, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]
+_lib.moe_dispatch_ranks.restype = ctypes.c_int
+_lib.moe_dispatch_ranks.argtypes = [_D] + [_vp] * 6 + [_sz, _vp]
+_lib.moe_combine_gather_ranks.restype = ctypes.c_int
+_lib.moe_combine_gather_ranks.argtypes = [_D, _vp, _i64, _vp, _vp, _vp]
 _lib.moe_mask_topk_ids.restype = ctypes.c_int
 _lib.moe_mask_topk_ids.argtypes = [_vp, _i32, _i32, _vp, _vp]
 _lib.moe_pack_record.restype = ctypes.c_int
@@ -268,6 +274,53 @@ def moe_combine_norm(desc: MoeDesc, mode: int, expert_out: torch.Tensor,
     return normed_out, residual_out
 
 
+def moe_rank_layout(desc: MoeDesc, lay: dict, expert_alignment: int = 1, out: dict | None = None,
+                    stream=None) -> dict:
+    """Per-rank receive layout from moe_layout's outputs (see include/moe.h)."""
+    n, r, e = desc.num_tokens, desc.num_ranks, desc.num_experts
+    dev = lay["tokens_per_rank"].device
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=dev)
+        out = dict(send_head=torch.empty((n, r), **i32), recv_src_idx=torch.empty(n * r, **i32),
+                   recv_offset=torch.empty(r + 1, **i32),
+                   recv_tokens_per_expert=torch.empty(e, **i32))
+    rc = _lib.moe_rank_layout(ctypes.byref(desc.c()), _ptr(lay["is_token_in_rank"]),
+                              _ptr(lay["tokens_per_rank"]), _ptr(lay["tokens_per_expert"]),
+                              int(expert_alignment), _ptr(out["send_head"]),
+                              _ptr(out.get("recv_src_idx")), _ptr(out["recv_offset"]),
+                              _ptr(out["recv_tokens_per_expert"]), _stream(stream))
+    _check(rc, "moe_rank_layout")
+    return out
+
+
+def moe_dispatch_ranks(desc: MoeDesc, topk_idx, topk_weights, hidden, scales, send_head,
+                       records=None, stream=None) -> torch.Tensor:
+    """One record per (token, rank) at send_head; records uint8 [N*R, record_bytes]
+    when allocated here."""
+    lay = moe_record_layout(desc)
+    if records is None:
+        records = torch.empty((desc.num_tokens * desc.num_ranks, lay["record_bytes"]),
+                              dtype=torch.uint8, device=topk_idx.device)
+    rc = _lib.moe_dispatch_ranks(ctypes.byref(desc.c()), _ptr(topk_idx), _ptr(topk_weights),
+                                 _ptr(hidden), _ptr(scales), _ptr(send_head), _ptr(records),
+                                 records.numel() * records.element_size(), _stream(stream))
+    _check(rc, "moe_dispatch_ranks")
+    return records
+
+
+def moe_combine_gather_ranks(desc: MoeDesc, recv_out: torch.Tensor, send_head: torch.Tensor,
+                             out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[t] = bf16(sum over ranks of recv_out[send_head[t, r]]), bf16 [N, H]."""
+    if out is None:
+        out = torch.empty((desc.num_tokens, desc.hidden), dtype=torch.bfloat16,
+                          device=recv_out.device)
+    rows = recv_out.numel() // max(desc.hidden, 1)
+    rc = _lib.moe_combine_gather_ranks(ctypes.byref(desc.c()), _ptr(recv_out), rows,
+                                       _ptr(send_head), _ptr(out), _stream(stream))
+    _check(rc, "moe_combine_gather_ranks")
+    return out
+
+
 def _slot_desc(num_ranks: int, sizes) -> _SlotDesc:
     d = _SlotDesc()
     d.num_tensors = len(sizes)
@@ -417,4 +470,5 @@ def exported_symbols() -> list[str]:
     return ["moe_strerror", "moe_record_layout", "moe_workspace_size", "moe_layout",
             "moe_layout_status", "moe_dispatch", "moe_combine", "moe_pack_record",
             "moe_unpack_record", "moe_layout_noalloc", "moe_combine_norm", "moe_slot_layout",
-            "moe_pack_slots", "moe_unpack_slots", "moe_mask_topk_ids"]
+            "moe_pack_slots", "moe_unpack_slots", "moe_mask_topk_ids", "moe_rank_layout",
+            "moe_dispatch_ranks", "moe_combine_gather_ranks"]

@@ -260,6 +260,57 @@ int moe_combine_norm(const moe_desc_t* desc, int mode, const void* expert_out,
                      const int32_t* slot_of, const void* residual_in, const void* gamma, float eps,
                      void* normed_out, void* residual_out, moe_stream_t stream);
 
+/* ---- one record per (token, destination rank) ----------------------------
+ * The shape of DeepEP's normal (intranode) dispatch and combine (DeepEP
+ * repository, csrc/deep_ep.cpp Buffer::intranode_dispatch /
+ * Buffer::intranode_combine): a token is sent once to every rank r with
+ * is_token_in_rank[t, r], not once per expert; each rank's experts then
+ * produce one (locally reduced) row per received token, and combine sums the
+ * ranks' rows back to token order. */
+
+/* Receive layout per rank, from moe_layout's outputs. For rank r the received
+ * tokens are the t with is_token_in_rank[t, r], in ascending t (virtual
+ * source ranks own contiguous token ranges, so this is source-rank order):
+ *   recv_offset [R+1]   exclusive prefix sum of tokens_per_rank
+ *   send_head   [N,R]   receive slot of token t on rank r, recv_offset[r] + its
+ *                       position among rank r's tokens; -1 if not sent
+ *   recv_src_idx [N*R]  source token of each receive slot, -1 past the last
+ *                       (may be NULL)
+ *   recv_tokens_per_expert [E]  tokens_per_expert[e] rounded up to a multiple
+ *                       of expert_alignment (>= 1), as DeepEP aligns its
+ *                       per-expert receive counts for grouped GEMMs
+ * Inputs: is_token_in_rank uint8 [N,R], tokens_per_rank int32 [R],
+ * tokens_per_expert int32 [E] (device). Errors: INVALID_ARG, SHAPE,
+ * ALIGNMENT, CUDA. */
+int moe_rank_layout(const moe_desc_t* desc, const uint8_t* is_token_in_rank,
+                    const int32_t* tokens_per_rank, const int32_t* tokens_per_expert,
+                    int32_t expert_alignment, int32_t* send_head, int32_t* recv_src_idx,
+                    int32_t* recv_offset, int32_t* recv_tokens_per_expert, moe_stream_t stream);
+
+/* Dispatch with one record per (token, rank) at records + send_head[t, r] *
+ * record_bytes (moe_record_layout's format and sizes). The payload and
+ * scales are those of moe_dispatch. The first segment differs (reading: the
+ * pages show DeepEP's interface, not its kernel):
+ *   header  int32 src_token, int32 rank, int32 number of the token's pairs on
+ *           the rank, int32 0
+ *   ids     topk_idx[t, j] - r*E/R (the local expert id) for experts on rank
+ *           r, else -1
+ *   weights topk_weights[t, j] for experts on rank r, else 0
+ * Errors: as moe_dispatch. */
+int moe_dispatch_ranks(const moe_desc_t* desc, const int32_t* topk_idx,
+                       const float* topk_weights, const void* hidden, const void* scales,
+                       const int32_t* send_head, void* records, size_t records_bytes,
+                       moe_stream_t stream);
+
+/* Combine of per-rank rows: recv_out bf16 [recv_rows, H] holds one row per
+ * receive slot (each rank's locally reduced expert output for the token);
+ *   out[t] = bf16( sum over r ascending with send_head[t, r] >= 0 of
+ *                  float(recv_out[send_head[t, r]]) )    (fp32, from +0)
+ * out bf16 [N, H]. H % 8 == 0; recv_out and out 16-byte aligned. Slots at or
+ * past recv_rows are skipped. Errors: INVALID_ARG, SHAPE, ALIGNMENT, CUDA. */
+int moe_combine_gather_ranks(const moe_desc_t* desc, const void* recv_out, int64_t recv_rows,
+                             const int32_t* send_head, void* out, moe_stream_t stream);
+
 /* ---- tensor-major rank slots and padded-token mask ----------------------
  * The decode all-gather of the vLLM compare view ds-exp-2...ds-exp-ag packs
  * each rank's 2-4 tensors (top-k ids, weights, hidden payload, scales) into

@@ -58,7 +58,8 @@ def _load():
                      "oracle_identity_expert", "oracle_combine_topk", "oracle_combine_ranks",
                      "oracle_combine_topk_ranks", "oracle_combine_topk_f64"):
             getattr(_lib, name).restype = i32
-        for name in ("oracle_slot_layout", "oracle_pack_slots", "oracle_unpack_slots"):
+        for name in ("oracle_slot_layout", "oracle_pack_slots", "oracle_unpack_slots",
+                     "oracle_rank_layout", "oracle_dispatch_ranks", "oracle_combine_gather_ranks"):
             getattr(_lib, name).restype = i32
         _lib.oracle_mask_topk_ids.restype = None
         _lib.oracle_combine_norm.restype = i32
@@ -305,3 +306,44 @@ def mask_topk_ids(topk_idx, num_actual_tokens: int) -> np.ndarray:
     n, k = ids.shape
     _load().oracle_mask_topk_ids(_p(ids), n, k, int(num_actual_tokens))
     return ids
+
+
+def rank_layout(is_token_in_rank, tokens_per_expert, expert_alignment: int = 1) -> dict:
+    m = np.ascontiguousarray(is_token_in_rank, dtype=np.uint8)
+    tpe = np.ascontiguousarray(tokens_per_expert, dtype=np.int32)
+    n, r = m.shape
+    out = dict(send_head=np.zeros((n, r), np.int32), recv_src_idx=np.zeros(n * r, np.int32),
+               recv_offset=np.zeros(r + 1, np.int32), recv_tokens_per_expert=np.zeros(tpe.size, np.int32))
+    _check(_load().oracle_rank_layout(_p(m), _p(tpe), n, r, tpe.size, expert_alignment,
+                                      _p(out["send_head"]), _p(out["recv_src_idx"]),
+                                      _p(out["recv_offset"]), _p(out["recv_tokens_per_expert"])),
+           "rank_layout")
+    return out
+
+
+def dispatch_ranks(topk_idx, topk_weights, hidden, scales, send_head, num_records: int,
+                   num_experts: int, in_kind: int, out_kind: int, hidden_size: int,
+                   raw_payload_bytes: int = 0, raw_scale_bytes: int = 0) -> np.ndarray:
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    sh = np.ascontiguousarray(send_head, dtype=np.int32)
+    n, k = idx.shape
+    lay = record_layout(k, hidden_size, in_kind, out_kind, raw_payload_bytes, raw_scale_bytes)
+    rec = np.zeros((num_records, lay["record_bytes"]), dtype=np.uint8)
+    h = np.ascontiguousarray(hidden)
+    sc = None if scales is None else np.ascontiguousarray(scales)
+    _check(_load().oracle_dispatch_ranks(_p(idx), _p(w), _p(h), _p(sc), n, k, num_experts,
+                                         sh.shape[1], hidden_size, in_kind, out_kind,
+                                         raw_payload_bytes, raw_scale_bytes, _p(sh), _p(rec)),
+           "dispatch_ranks")
+    return rec
+
+
+def combine_gather_ranks(recv_out, send_head, hidden_size: int) -> np.ndarray:
+    y = np.ascontiguousarray(recv_out, dtype=np.uint16)
+    sh = np.ascontiguousarray(send_head, dtype=np.int32)
+    n, r = sh.shape
+    out = np.zeros((n, hidden_size), np.uint16)
+    _check(_load().oracle_combine_gather_ranks(_p(y), _p(sh), n, r, hidden_size, _p(out)),
+           "combine_gather_ranks")
+    return out

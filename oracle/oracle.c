@@ -609,3 +609,135 @@ void oracle_mask_topk_ids(int32_t* topk_idx, int num_tokens, int topk, int num_a
     if (t >= num_actual_tokens)
       for (int j = 0; j < topk; ++j) topk_idx[(long)t * topk + j] = -1;
 }
+
+/* ======================================================================== */
+/* One record per (token, destination rank)                                  */
+/* ======================================================================== */
+
+/* [EP] Buffer::intranode_dispatch: rank r receives every token t with
+ * is_token_in_rank[t, r], here in ascending t (virtual source ranks own
+ * contiguous token ranges). recv_offset is the exclusive prefix sum of the
+ * per-rank token counts; send_head[t, r] is the token's receive slot or -1;
+ * recv_src_idx[s] the token in slot s (-1 past the last, N*R entries); the
+ * per-expert counts are rounded up to expert_alignment. */
+int oracle_rank_layout(const uint8_t* is_token_in_rank, const int32_t* tokens_per_expert,
+                       int num_tokens, int num_ranks, int num_experts, int expert_alignment,
+                       int32_t* send_head, int32_t* recv_src_idx, int32_t* recv_offset,
+                       int32_t* recv_tokens_per_expert) {
+  if (num_tokens < 0 || num_ranks < 1 || num_experts < 1 || expert_alignment < 1) return -1;
+  int run = 0;
+  for (int r = 0; r < num_ranks; ++r) {
+    recv_offset[r] = run;
+    for (int t = 0; t < num_tokens; ++t) run += is_token_in_rank[(long)t * num_ranks + r] ? 1 : 0;
+  }
+  recv_offset[num_ranks] = run;
+  if (recv_src_idx)
+    for (long s = 0; s < (long)num_tokens * num_ranks; ++s) recv_src_idx[s] = -1;
+  for (int r = 0; r < num_ranks; ++r) {
+    int cursor = recv_offset[r];
+    for (int t = 0; t < num_tokens; ++t) {
+      if (is_token_in_rank[(long)t * num_ranks + r]) {
+        send_head[(long)t * num_ranks + r] = cursor;
+        if (recv_src_idx) recv_src_idx[cursor] = t;
+        ++cursor;
+      } else {
+        send_head[(long)t * num_ranks + r] = -1;
+      }
+    }
+  }
+  for (int e = 0; e < num_experts; ++e) {
+    int c = tokens_per_expert[e];
+    recv_tokens_per_expert[e] = (c + expert_alignment - 1) / expert_alignment * expert_alignment;
+  }
+  return 0;
+}
+
+/* The record for (t, r) at send_head[t, r]: header (t, r, number of the
+ * token's pairs on rank r, 0); the id row with local ids (e - r*E/R) for
+ * experts on rank r and -1 elsewhere; the weight row with 0 elsewhere;
+ * payload and scales exactly as oracle_dispatch builds them. */
+int oracle_dispatch_ranks(const int32_t* topk_idx, const float* topk_weights, const void* hidden,
+                          const void* scales, int num_tokens, int topk, int num_experts,
+                          int num_ranks, int hidden_size, int in_kind, int out_kind,
+                          int raw_payload_bytes, int raw_scale_bytes, const int32_t* send_head,
+                          uint8_t* records) {
+  int32_t lay[7];
+  if (num_ranks < 1 || num_experts % num_ranks || topk > 32) return -1;
+  if (oracle_record_layout(topk, hidden_size, in_kind, out_kind, raw_payload_bytes,
+                           raw_scale_bytes, lay) != 0)
+    return -1;
+  const int S = lay[0], off_ids = lay[1], off_w = lay[2], off_p = lay[3];
+  const int per_rank = num_experts / num_ranks;
+  /* payload and scales of one token: the same bytes oracle_dispatch writes,
+   * taken from a one-pair dispatch of that token into a scratch record */
+  uint8_t* one = (uint8_t*)malloc((size_t)S);
+  if (!one) return -2;
+  for (int t = 0; t < num_tokens; ++t) {
+    int32_t zero_slot = 0;
+    const void* h = NULL;
+    const void* sc = NULL;
+    if (in_kind == ORACLE_RAW) {
+      h = (const uint8_t*)hidden + (size_t)t * raw_payload_bytes;
+      sc = raw_scale_bytes ? (const void*)((const uint8_t*)scales + (size_t)t * raw_scale_bytes) : NULL;
+    } else {
+      h = (const uint16_t*)hidden + (size_t)t * hidden_size;
+    }
+    int32_t row_idx[32];
+    float row_w[32];
+    for (int j = 0; j < topk; ++j) {
+      row_idx[j] = topk_idx[(long)t * topk + j];
+      row_w[j] = topk_weights[(long)t * topk + j];
+    }
+    int32_t one_idx[32];
+    float one_w[32];
+    for (int j = 0; j < topk; ++j) {
+      one_idx[j] = j == 0 ? 0 : -1;
+      one_w[j] = 0.0f;
+    }
+    int32_t one_slots[32];
+    for (int j = 0; j < topk; ++j) one_slots[j] = j == 0 ? zero_slot : -1;
+    if (oracle_dispatch(one_idx, one_w, h, sc, 1, topk, hidden_size, in_kind, out_kind,
+                        raw_payload_bytes, raw_scale_bytes, one_slots, one) != 0) {
+      free(one);
+      return -1;
+    }
+    for (int r = 0; r < num_ranks; ++r) {
+      int s = send_head[(long)t * num_ranks + r];
+      if (s < 0) continue;
+      uint8_t* rec = records + (size_t)s * S;
+      memset(rec, 0, (size_t)off_p);
+      int nlocal = 0;
+      for (int j = 0; j < topk; ++j) {
+        int e = row_idx[j];
+        int local = (e >= r * per_rank && e < (r + 1) * per_rank);
+        int32_t id = local ? e - r * per_rank : -1;
+        float w = local ? row_w[j] : 0.0f;
+        nlocal += local;
+        memcpy(rec + off_ids + 4 * j, &id, 4);
+        memcpy(rec + off_w + 4 * j, &w, 4);
+      }
+      int32_t hdr[4] = {t, r, nlocal, 0};
+      memcpy(rec, hdr, 16);
+      memcpy(rec + off_p, one + off_p, (size_t)(S - off_p));
+    }
+  }
+  free(one);
+  return 0;
+}
+
+/* [EP] Buffer::intranode_combine: out[t] = bf16(sum over ranks r ascending
+ * with send_head[t, r] >= 0 of recv_out[send_head[t, r]]), fp32 from +0. */
+int oracle_combine_gather_ranks(const uint16_t* recv_out, const int32_t* send_head,
+                                int num_tokens, int num_ranks, int hidden_size, uint16_t* out) {
+  for (int t = 0; t < num_tokens; ++t) {
+    for (int h = 0; h < hidden_size; ++h) {
+      float acc = 0.0f;
+      for (int r = 0; r < num_ranks; ++r) {
+        int s = send_head[(long)t * num_ranks + r];
+        if (s >= 0) acc = acc + oracle_bf16_to_f32(recv_out[(size_t)s * hidden_size + h]);
+      }
+      out[(size_t)t * hidden_size + h] = oracle_f32_to_bf16(acc);
+    }
+  }
+  return 0;
+}

@@ -75,6 +75,18 @@ int oracle_combine_norm(int mode, const uint16_t* y, const int32_t* topk_idx,
                         int topk, int num_experts, int num_ranks, int hidden_size,
                         const uint16_t* residual, const uint16_t* gamma, float eps,
                         uint16_t* normed, uint16_t* residual_out);
+/* One record per (token, destination rank) ([EP] intranode dispatch/combine). */
+int oracle_rank_layout(const uint8_t* is_token_in_rank, const int32_t* tokens_per_expert,
+                       int num_tokens, int num_ranks, int num_experts, int expert_alignment,
+                       int32_t* send_head, int32_t* recv_src_idx, int32_t* recv_offset,
+                       int32_t* recv_tokens_per_expert);
+int oracle_dispatch_ranks(const int32_t* topk_idx, const float* topk_weights, const void* hidden,
+                          const void* scales, int num_tokens, int topk, int num_experts,
+                          int num_ranks, int hidden_size, int in_kind, int out_kind,
+                          int raw_payload_bytes, int raw_scale_bytes, const int32_t* send_head,
+                          uint8_t* records);
+int oracle_combine_gather_ranks(const uint16_t* recv_out, const int32_t* send_head,
+                                int num_tokens, int num_ranks, int hidden_size, uint16_t* out);
 /* Rank slots of the decode all-gather ([AG] make_desc) and the padded-token
  * mask ([AG] mask_topk_ids). */
 int oracle_slot_layout(int num_tensors, const int64_t* bytes, int64_t* offsets, int64_t* slot_bytes);
