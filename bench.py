@@ -325,6 +325,69 @@ class Step:
         self.dispatch()
         self.combine()
 
+    def calls_on(self, stream):
+        """The step's three calls bound to `stream` (for graph capture)."""
+        moe = self.moe
+        h = stream.cuda_stream
+        if self.spec.get("per_rank"):
+            lp = moe.prepare_layout(self.desc, self.ids, self.lay, self.ws, h)
+            d, lay, rlay = self.desc, self.lay, self.rlay
+
+            def layout():
+                lp()
+                moe.moe_rank_layout(d, lay, 1, rlay, h)
+            return [layout,
+                    lambda: moe.moe_dispatch_ranks(d, self.ids, self.w, self.x, self.sc,
+                                                   rlay["send_head"], self.records, h),
+                    lambda: moe.moe_combine_gather_ranks(self.cdesc, self.y, rlay["send_head"],
+                                                         self.out, h)]
+        calls = [moe.prepare_layout(self.desc, self.ids, self.lay, self.ws, h),
+                 moe.prepare_dispatch(self.desc, self.ids, self.w, self.x, self.sc,
+                                      self.lay["slot_of"], self.records, h)]
+        if self.spec.get("norm"):
+            calls.append(moe.prepare_combine_norm(
+                self.cdesc, moe.MOE_COMBINE_TOPK_RANKS, self.y, self.ids, self.w,
+                self.lay["slot_of"], self.residual, self.gamma, 1e-6, self.out,
+                self.residual_out, h))
+        else:
+            calls.append(moe.prepare_combine(self.cdesc, moe.MOE_COMBINE_TOPK_RANKS, self.y,
+                                             self.ids, self.w, self.lay["slot_of"], self.out, h))
+        return calls
+
+
+def measure_graph(st: "Step", K: int, flush, flush_read) -> dict:
+    """The whole step captured once in a CUDA graph and replayed: device time
+    per replay (CUDA events around each replay, L2 flushed in between)."""
+    import torch
+    s = torch.cuda.Stream()
+    calls = st.calls_on(s)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            for c in calls:
+                c()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for c in calls:
+            c()
+    k2 = max(3, min(K, 200))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(k2)]
+    for _ in range(3):
+        g.replay()
+    for a, b in ev:
+        flush.zero_()
+        flush_read.sum()
+        a.record()
+        g.replay()
+        b.record()
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+    return {"step_us_median": round(us[len(us) // 2], 2), "step_us_min": round(us[0], 2),
+            "replays": k2}
+
 
 def run_ag_slots(args, rank, world):
     """The decode all-gather's data path on one GPU: mask padded tokens, pack
@@ -432,7 +495,8 @@ def run_ours(args, spec, rank, world):
     achieved = {name: bpt[name] * n / (kern[name] / 1e3) / 1e9 for name in kern}
     step_bytes = sum(bpt.values()) * n
 
-    e2e = measure_e2e(st, spec, dev, K, W) if rank == 0 else None
+    graph = measure_graph(st, K, flush, flush_read)
+    e2e = measure_e2e(st, spec, dev, K, W, seed=rank) if rank == 0 else None
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
@@ -459,6 +523,7 @@ def run_ours(args, spec, rank, world):
         "kernels_frac": {name: round(v / peaks["hbm_gbs"], 4) for name, v in achieved.items()},
         "step_gbs": round(step_bytes / (total_ms / K / 1e3) / 1e9, 1),
         "gpu_launches": st.launches_per_step * K,
+        "graph": graph,
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
@@ -469,43 +534,86 @@ def run_ours(args, spec, rank, world):
     return line
 
 
-def measure_e2e(st: Step, spec: dict, dev, K: int, W: int) -> dict:
-    """Same step through the public API with inputs copied from pinned host
-    memory every step and the combined output read back every step."""
+def measure_e2e(st: Step, spec: dict, dev, K: int, W: int, seed: int = 0) -> dict:
+    """The same step through the public API with the inputs copied from pinned
+    host memory every step and the combined output read back every step.
+
+    Pipelined as a serving loop would run it: two buffer sets; step i's inputs
+    are copied on one stream while step i-1 computes and step i-2's output is
+    read back on another, with events ordering each buffer's reuse. The serial
+    form (copy in, compute, copy out, one stream) is reported beside it."""
     import torch
     n = spec["num_tokens"]
+    sets = [st, Step(spec, dev, seed)]
     h_ids = st.ids.cpu().pin_memory()
     h_w = st.w.cpu().pin_memory()
     h_x = st.x.cpu().pin_memory()
     h_sc = st.sc.cpu().pin_memory() if st.sc is not None else None
-    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_w, h_x) if t is not None)
+    h_out = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_w, h_x))
     if h_sc is not None:
         h2d += h_sc.numel()
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size()
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def one():
-        st.ids.copy_(h_ids, non_blocking=True)
-        st.w.copy_(h_w, non_blocking=True)
-        st.x.copy_(h_x, non_blocking=True)
+    def copy_in(S):
+        S.ids.copy_(h_ids, non_blocking=True)
+        S.w.copy_(h_w, non_blocking=True)
+        S.x.copy_(h_x, non_blocking=True)
         if h_sc is not None:
-            st.sc.copy_(h_sc, non_blocking=True)
-        st.run()
-        h_out.copy_(st.out, non_blocking=True)
+            S.sc.copy_(h_sc, non_blocking=True)
 
-    for _ in range(max(W, 1)):
-        one()
-    torch.cuda.synchronize()
+    def serial(S):
+        copy_in(S)
+        S.run()
+        h_out[0].copy_(S.out, non_blocking=True)
+
+    def pipelined(steps):
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        for i in range(steps):
+            bset = i % 2
+            S = sets[bset]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_comp[bset])  # step i-2 is done with these inputs
+                copy_in(S)
+                ev_in[bset].record(s_in)
+            comp.wait_event(ev_in[bset])
+            if i >= 2:
+                comp.wait_event(ev_out[bset])  # step i-2's output has been read back
+            S.run()
+            ev_comp[bset].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[bset])
+                h_out[bset].copy_(S.out, non_blocking=True)
+                ev_out[bset].record(s_out)
+        comp.wait_stream(s_in)
+        comp.wait_stream(s_out)
+
     k2 = max(1, min(K, 200))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(k2):
-        one()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / k2
+    res = {}
+    for name, fn in (("serial", lambda: [serial(st) for _ in range(k2)]),
+                     ("pipelined", lambda: pipelined(k2))):
+        for _ in range(max(W, 1)):
+            serial(st)
+        pipelined(4)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(comp)
+        fn()
+        b.record(comp)
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) / k2
+    ms = res["pipelined"]
     return {"value": round(n / (ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": k2, "ms_per_step": round(ms, 4)}
+            "d2h_bytes_per_step": d2h, "steps": k2, "ms_per_step": round(ms, 4),
+            "mode": "pipelined: inputs of step i copied in while step i-1 computes and step i-2 "
+                    "is read back (two buffer sets, three streams)",
+            "serial": {"value": round(n / (res["serial"] / 1e3), 1),
+                       "ms_per_step": round(res["serial"], 4)}}
 
 
 # ---------------------------------------------------------------- oracle arm -
