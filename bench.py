@@ -12,7 +12,7 @@ Prints one JSON line. `--impl reference` times the plain CPU oracle instead
 (rank 0 only), on bounded samples of the same workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload prefill|decode|rs|skewed|tiny]
+                       [--workload prefill|decode|decode_ll|rs|skewed|tiny|...]
 Multi-GPU runs (torchrun) are independent replicas: the path has no
 cross-GPU exchange on one-GPU-per-rank hardware here.
 """
@@ -71,6 +71,12 @@ def workload_spec(name: str) -> dict:
                  out_kind="fp8", record_bytes=7472, per_rank=True,
                  text="prefill N=4096 H=7168 E=256 top-8 R=8; one record per (token, rank) "
                       "(FP8 dispatch), rank rows summed back (BF16 combine)")
+    elif name == "decode_ll":
+        s = dict(num_tokens=1024, hidden=7168, num_experts=256, topk=8, num_ranks=8,
+                 out_kind="fp8", record_bytes=7472, ll=True, max_tokens_per_rank=128,
+                 text="low-latency decode: 8 ranks x 128 tokens, H=7168, top-8 of 256 experts; "
+                      "FP8 e4m3 per-128 into fixed-capacity expert-major buffers "
+                      "[256 x 1024 positions]; BF16 top-k combine")
     elif name == "tiny":
         s = dict(num_tokens=128, hidden=1024, num_experts=16, topk=2, num_ranks=2,
                  out_kind="bf16", record_bytes=2096,
@@ -87,6 +93,18 @@ def workload_spec(name: str) -> dict:
     )
     if s.get("norm"):  # + residual in, normed and new residual out
         s["bytes_per_token"]["combine"] += 2 * 2 * h
+    if s.get("ll"):
+        e = s["num_experts"]
+        cap = r * s["max_tokens_per_rank"]
+        s["bytes_per_token"] = dict(
+            # moe_layout as above + ll_slot_of out, and the whole src_info
+            # [E, cap], layout_range [E, R] and recv_count [E] written
+            layout=4 * k + 4 * k + 4 * k + r + 4 * k + (4 * e * cap + 8 * e * r + 4 * e) / n,
+            # row, slots in; k payload rows + k scale rows out
+            dispatch=2 * h + 4 * k + k * (h + 4 * (h // 128)),
+            # k expert rows, weights, slots in; row out
+            combine=k * 2 * h + 4 * k * 2 + 2 * h,
+        )
     s["name"] = name
     return s
 
@@ -98,6 +116,9 @@ def make_inputs(spec: dict, seed: int = 0) -> dict:
         return synth.prefill_case(seed=seed, n=n)
     if spec["name"] == "skewed":
         return synth.skewed_case(seed=seed, n=n)
+    if spec["name"] == "decode_ll":
+        return synth.decode_ll_case(seed=seed, tokens_per_rank=spec["max_tokens_per_rank"],
+                                    r=spec["num_ranks"])
     if spec["name"] == "decode":
         return synth.decode_case(seed=seed, n=n)
     if spec["name"] == "rs":
@@ -255,6 +276,9 @@ class Step:
             yy = synth.bf16_normal(synth.rng_for(seed, 11), (n * k, h))
             self.y = torch.from_numpy(yy.view(np.int16)).to(dev).view(torch.bfloat16)
         self.launches_per_step = layout_launches(n, k, e, r) + 1 + 1
+        if spec.get("ll"):
+            self._setup_ll(spec, dev)
+            return
         if spec.get("per_rank"):
             self._setup_per_rank(spec, dev, seed)
             return
@@ -319,6 +343,48 @@ class Step:
             dispatch=2 * h + 12 * spec["topk"] + 4 * r + per * spec["record_bytes"],
             combine=per * 2 * h + 4 * r + 2 * h,
         )
+
+    def _setup_ll(self, spec, dev):
+        """Fixed-capacity, expert-major buffers: the LL layout runs after the
+        layout (both timed as 'layout'), the payload and scales go to
+        [E * capacity] rows, and the expert of each position returns its
+        dequantised row; the combine is the top-k reduction over those rows."""
+        import torch
+        moe = self.moe
+        h, max_t = spec["hidden"], spec["max_tokens_per_rank"]
+        self.ll = moe.moe_ll_layout(self.desc, max_t, self.ids, self.lay)
+        cap = self.ll["capacity"]
+        rows = spec["num_experts"] * cap
+        rl = moe.moe_record_layout(self.desc)
+        self.x_ll = torch.empty((rows, rl["payload_bytes"]), dtype=torch.uint8, device=dev)
+        self.s_ll = torch.empty((rows, rl["scale_bytes"]), dtype=torch.uint8, device=dev)
+        moe.moe_dispatch_ll(self.desc, self.x, self.sc, self.ll["ll_slot_of"], cap, self.x_ll,
+                            self.s_ll)
+        torch.cuda.synchronize()
+        pos = self.ll["ll_slot_of"].flatten()
+        pos = pos[pos >= 0].long()
+        q = self.x_ll.index_select(0, pos).view(torch.float8_e4m3fn)
+        sc = self.s_ll.index_select(0, pos).contiguous().view(torch.float32)
+        self.records = None
+        self.y = torch.zeros((rows, h), dtype=torch.bfloat16, device=dev)
+        self.y[pos] = (q.float() * sc.repeat_interleave(128, dim=1)).to(torch.bfloat16)
+        self.max_t = max_t
+        self.calls_on = self._ll_calls_on
+        lp, llp, dp, cp = self._ll_calls_on(torch.cuda.current_stream())
+        self.layout = lambda: (lp(), llp())
+        self.dispatch, self.combine = dp, cp
+        self.launches_per_step = layout_launches(spec["num_tokens"], spec["topk"],
+                                                 spec["num_experts"], spec["num_ranks"]) + 3
+
+    def _ll_calls_on(self, stream):
+        moe = self.moe
+        h = stream.cuda_stream
+        return [moe.prepare_layout(self.desc, self.ids, self.lay, self.ws, h),
+                moe.prepare_ll_layout(self.desc, self.max_t, self.ids, self.lay, self.ll, h),
+                moe.prepare_dispatch_ll(self.desc, self.x, self.sc, self.ll["ll_slot_of"],
+                                        self.x_ll, self.s_ll, h),
+                moe.prepare_combine(self.cdesc, moe.MOE_COMBINE_TOPK, self.y, self.ids, self.w,
+                                    self.ll["ll_slot_of"], self.out, h)]
 
     def run(self):
         self.layout()
@@ -508,7 +574,8 @@ def run_ours(args, spec, rank, world):
                    "num_experts": spec["num_experts"], "topk": spec["topk"],
                    "num_ranks": spec["num_ranks"], "record_bytes": spec["record_bytes"],
                    "combine_mode": "TOPK_RANKS + residual + RMSNorm" if spec.get("norm")
-                   else "rank rows gathered per token" if spec.get("per_rank") else "TOPK_RANKS",
+                   else "rank rows gathered per token" if spec.get("per_rank")
+                   else "TOPK over the fixed-capacity positions" if spec.get("ll") else "TOPK_RANKS",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, then "
                          f"{L2_FLUSH_BYTES >> 20} MiB read, outside the timed events); step "
                          f"working set {step_bytes / 1e6:.0f} MB",
@@ -625,6 +692,17 @@ def oracle_step(c: dict, spec: dict, t0: int, t1: int):
     e, r, h = spec["num_experts"], spec["num_ranks"], spec["hidden"]
     lay = oracle.layout(ids, e, r)
     P = lay["num_pairs"]
+    if spec.get("ll"):
+        # the fixed-capacity path: positions, packed payload, top-k combine
+        # (the expert outputs are zero rows of the full [E * capacity] buffer)
+        max_t = spec["max_tokens_per_rank"]
+        ll = oracle.ll_layout(ids, e, r, max_t)
+        rows = e * r * max_t
+        x, s = oracle.dispatch_ll(c["hidden_bf16"][t0:t1], None, ll["ll_slot_of"], rows, oracle.BF16,
+                                  oracle.FP8_E4M3_B128, h)
+        y = np.zeros((rows, h), np.uint16)
+        oracle.combine_topk(y, w, ll["ll_slot_of"], h)
+        return x
     if spec["out_kind"] == "raw":
         rec = oracle.dispatch(ids, w, c["payload"][t0:t1], c["scales"][t0:t1], lay["slot_of"], P,
                               oracle.RAW, oracle.RAW, h, 3584, 448)
@@ -715,7 +793,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill",
                     choices=["prefill", "decode", "rs", "skewed", "tiny", "prefill_norm",
-                             "prefill_ranks", "ag_slots"])
+                             "prefill_ranks", "decode_ll", "ag_slots"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

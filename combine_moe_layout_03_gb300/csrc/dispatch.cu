@@ -261,6 +261,54 @@ __global__ void __launch_bounds__(kDispatchThreads)
   }
 }
 
+// Payload and scales only, into two fixed-capacity, expert-major arrays (the
+// low-latency receive buffers of DeepEP Buffer::low_latency_dispatch):
+// pair (t, j) goes to row pos = slot_of[t, j] of x_out [rows, payload_bytes]
+// and of scales_out [rows, scale_bytes]. The payload is built once per token
+// in shared memory as above; thread j issues the two bulk stores.
+template <int OUT_KIND>
+__global__ void __launch_bounds__(kDispatchThreads)
+    k_dispatch_packed(DispatchParams p, uint8_t* x_out, uint8_t* scales_out, int64_t rows) {
+  extern __shared__ __align__(128) uint8_t img[];  // payload | scales | staged row
+  __shared__ int s_pos[MOE_MAX_TOPK];
+  const int t = blockIdx.x;
+  const int k = p.topk;
+  const int pb = p.payload_bytes, sb = p.scale_bytes;
+  constexpr bool kQuant = OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128 || OUT_KIND == MOE_PAYLOAD_NVFP4_B16;
+  uint8_t* stage = img + pb + sb;
+  const uint8_t* row = p.hidden + (size_t)t * p.in_row_bytes;
+  if (kQuant) {
+    copy_g2s_async(stage, row, p.in_row_bytes / 16);
+  } else {
+    copy_g2s_async(img, row, pb / 16);
+    if (OUT_KIND == MOE_PAYLOAD_RAW && sb > 0)
+      copy_g2s_async(img + pb, p.scales + (size_t)t * p.in_scale_bytes, sb / 16);
+  }
+  if (threadIdx.x < k) {
+    const int pos = p.slot_of[(int64_t)t * k + threadIdx.x];
+    s_pos[threadIdx.x] = (pos >= 0 && (int64_t)pos < rows) ? pos : -1;
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  if (OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128) {
+    quant_fp8(stage, p.hidden_size, img, reinterpret_cast<float*>(img + pb));
+  } else if (OUT_KIND == MOE_PAYLOAD_NVFP4_B16) {
+    quant_nvfp4(stage, p.hidden_size, img, img + pb);
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (threadIdx.x < k) {
+    const int pos = s_pos[threadIdx.x];
+    if (pos >= 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      bulk_store_s2g_evict_first(x_out + (size_t)pos * pb, img, (uint32_t)pb, pol);
+      if (sb > 0) bulk_store_s2g_evict_first(scales_out + (size_t)pos * sb, img + pb, (uint32_t)sb, pol);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, cudaStream_t s) {
@@ -302,6 +350,29 @@ cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const i
   const int32_t* sh = send_head;
   int nr = num_ranks, epr = experts_per_rank;
   void* args[] = {&q, &sh, &nr, &epr};
+  return cudaLaunchKernel(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), args, smem, s);
+}
+
+cudaError_t launch_dispatch_packed(const DispatchParams& p, int out_kind, uint8_t* x_out,
+                                   uint8_t* scales_out, int64_t rows, cudaStream_t s) {
+  const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16;
+  const size_t smem = (size_t)p.payload_bytes + (size_t)p.scale_bytes + (quant ? (size_t)p.in_row_bytes : 0);
+  const void* fn = nullptr;
+  switch (out_kind) {
+    case MOE_PAYLOAD_BF16: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_BF16>; break;
+    case MOE_PAYLOAD_FP8_E4M3_B128: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_FP8_E4M3_B128>; break;
+    case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_NVFP4_B16>; break;
+    default: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_RAW>; break;
+  }
+  if (smem > 48 * 1024) {
+    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  DispatchParams q = p;
+  uint8_t* xo = x_out;
+  uint8_t* so = scales_out;
+  int64_t r = rows;
+  void* args[] = {&q, &xo, &so, &r};
   return cudaLaunchKernel(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), args, smem, s);
 }
 

@@ -381,6 +381,77 @@ int moe_combine_gather_ranks(const moe_desc_t* desc, const void* recv_out, int64
   return cuda_status(moe::launch_combine_gather_ranks(p, (cudaStream_t)stream));
 }
 
+int moe_ll_layout(const moe_desc_t* desc, int32_t max_tokens_per_rank, const int32_t* topk_idx,
+                  const int32_t* slot_of, const int32_t* expert_offset,
+                  const int32_t* src_of_slot, int32_t* ll_slot_of, int32_t* src_info,
+                  int64_t* layout_range, int32_t* recv_count, moe_stream_t stream) {
+  int rc = check_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens, R = desc->num_ranks;
+  if (max_tokens_per_rank < 1 || N % R || N / R > max_tokens_per_rank) return MOE_ERR_SHAPE;
+  const int64_t cap = (int64_t)R * max_tokens_per_rank;
+  if ((int64_t)desc->num_experts * cap >= ((int64_t)1 << 31)) return MOE_ERR_SHAPE;
+  if (!expert_offset || !src_info || !layout_range || !recv_count) return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!topk_idx || !slot_of || !src_of_slot || !ll_slot_of)) return MOE_ERR_INVALID_ARG;
+  const void* ints[] = {topk_idx, slot_of, expert_offset, src_of_slot, ll_slot_of, src_info,
+                        recv_count};
+  for (const void* q : ints)
+    if (!aligned(q, 4)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(layout_range, 8)) return MOE_ERR_ALIGNMENT;
+  moe::LlLayoutParams p;
+  p.topk_idx = topk_idx;
+  p.slot_of = slot_of;
+  p.expert_offset = expert_offset;
+  p.src_of_slot = src_of_slot;
+  p.ll_slot_of = ll_slot_of;
+  p.src_info = src_info;
+  p.layout_range = layout_range;
+  p.recv_count = recv_count;
+  p.capacity = cap;
+  p.num_tokens = N;
+  p.topk = desc->topk;
+  p.num_experts = desc->num_experts;
+  p.num_ranks = R;
+  return cuda_status(moe::launch_ll_layout(p, (cudaStream_t)stream));
+}
+
+int moe_dispatch_ll(const moe_desc_t* desc, const void* hidden, const void* scales,
+                    const int32_t* ll_slot_of, void* x_out, size_t x_out_bytes, void* scales_out,
+                    size_t scales_out_bytes, moe_stream_t stream) {
+  moe_record_layout_t lay;
+  int rc = record_layout(desc, &lay);
+  if (rc != MOE_OK) return rc;
+  if (lay.payload_bytes % 16 || lay.scale_bytes % 16) return MOE_ERR_SHAPE;
+  const int N = desc->num_tokens;
+  if (N == 0) return MOE_OK;
+  const bool raw = desc->out_kind == MOE_PAYLOAD_RAW;
+  if (!hidden || !ll_slot_of || !x_out) return MOE_ERR_INVALID_ARG;
+  if (lay.scale_bytes > 0 && !scales_out) return MOE_ERR_INVALID_ARG;
+  if (raw && lay.scale_bytes > 0 && !scales) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ll_slot_of, 4) || !aligned(hidden, 16) || !aligned(x_out, 16) ||
+      !aligned(scales_out, 16) || (raw && scales && !aligned(scales, 16)))
+    return MOE_ERR_ALIGNMENT;
+  if (lay.payload_bytes == 0) return MOE_ERR_SHAPE;
+  int64_t rows = (int64_t)(x_out_bytes / (size_t)lay.payload_bytes);
+  if (lay.scale_bytes > 0) {
+    const int64_t srows = (int64_t)(scales_out_bytes / (size_t)lay.scale_bytes);
+    if (srows < rows) rows = srows;
+  }
+  moe::DispatchParams p = {};
+  p.hidden = (const uint8_t*)hidden;
+  p.scales = (const uint8_t*)scales;
+  p.slot_of = ll_slot_of;
+  p.num_tokens = N;
+  p.topk = desc->topk;
+  p.hidden_size = desc->hidden;
+  p.in_row_bytes = raw ? desc->raw_payload_bytes : 2 * desc->hidden;
+  p.in_scale_bytes = raw ? desc->raw_scale_bytes : 0;
+  p.payload_bytes = lay.payload_bytes;
+  p.scale_bytes = lay.scale_bytes;
+  return cuda_status(moe::launch_dispatch_packed(p, desc->out_kind, (uint8_t*)x_out,
+                                                 (uint8_t*)scales_out, rows, (cudaStream_t)stream));
+}
+
 int moe_slot_layout(const moe_slot_desc_t* desc, int64_t* offsets, int64_t* slot_bytes) {
   if (!desc || !offsets || !slot_bytes) return MOE_ERR_INVALID_ARG;
   if (desc->num_tensors < 2 || desc->num_tensors > MOE_MAX_SLOT_TENSORS || desc->num_ranks < 1)

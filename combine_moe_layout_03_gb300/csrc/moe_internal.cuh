@@ -85,6 +85,19 @@ struct RankCombineParams {
   int num_tokens, num_ranks, hidden_size;
 };
 
+struct LlLayoutParams {
+  const int32_t* topk_idx;       // [N, k]
+  const int32_t* slot_of;        // [N, k]
+  const int32_t* expert_offset;  // [E + 1]
+  const int32_t* src_of_slot;    // [N * k]
+  int32_t* ll_slot_of;           // [N, k]  e * capacity + position, or -1
+  int32_t* src_info;             // [E, capacity]
+  int64_t* layout_range;         // [E, R]  begin << 32 | count
+  int32_t* recv_count;           // [E]
+  int64_t capacity;              // R * max_tokens_per_rank
+  int num_tokens, topk, num_experts, num_ranks;
+};
+
 // Workspace carving shared by moe_workspace_size and moe_layout.
 constexpr int kLayoutTokensPerChunk = 128;
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
@@ -103,6 +116,9 @@ cudaError_t launch_rank_layout(const RankLayoutParams& p, cudaStream_t s);
 cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const int32_t* send_head,
                                   int num_ranks, int experts_per_rank, cudaStream_t s);
 cudaError_t launch_combine_gather_ranks(const RankCombineParams& p, cudaStream_t s);
+cudaError_t launch_ll_layout(const LlLayoutParams& p, cudaStream_t s);
+cudaError_t launch_dispatch_packed(const DispatchParams& p, int out_kind, uint8_t* x_out,
+                                   uint8_t* scales_out, int64_t rows, cudaStream_t s);
 cudaError_t launch_mask_topk_ids(int32_t* ids, int64_t total, int topk, const int32_t* num_actual,
                                  cudaStream_t s);
 constexpr int kMaxHiddenNorm = 16384;

@@ -137,3 +137,87 @@ cudaError_t launch_combine_gather_ranks(const RankCombineParams& p, cudaStream_t
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Fixed-capacity, expert-major receive buffers (DeepEP repository,
+// csrc/deep_ep.cpp Buffer::low_latency_dispatch: packed_recv_x
+// [E_l, R * max_tokens, H], packed_recv_src_info, packed_recv_layout_range
+// [E_l, R] int64, packed_recv_count [E_l]). Seen from one GPU the R ranks'
+// buffers are [E, R * max_tokens, ...], expert-major. Expert e's received
+// pairs are packed compactly in source-rank order, which is the stable slot
+// order within e: position = slot_of[t, j] - expert_offset[e]. Source rank s
+// owns tokens [s*T, (s+1)*T), T = N / R.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+__global__ void k_ll_layout(LlLayoutParams p) {
+  const int64_t pairs = (int64_t)p.num_tokens * p.topk;
+  const int64_t cap = p.capacity;
+  const int T = p.num_tokens / p.num_ranks;
+  const int64_t gsz = (int64_t)gridDim.x * blockDim.x;
+  const int64_t g0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // ll_slot_of and src_info of every pair
+  for (int64_t q = g0; q < pairs; q += gsz) {
+    const int s = p.slot_of[q];
+    int64_t pos = -1;
+    if (s >= 0) {
+      const int e = p.topk_idx[q];
+      const int64_t within = (int64_t)s - p.expert_offset[e];
+      if (within >= 0 && within < cap) {
+        pos = (int64_t)e * cap + within;
+        const int t = (int)(q / p.topk);
+        p.src_info[pos] = t - (t / T) * T;  // token index within its source rank
+      }
+    }
+    p.ll_slot_of[q] = pos < (int64_t)INT32_MAX ? (int32_t)pos : -1;
+  }
+  // src_info past each expert's count, counts and layout ranges
+  for (int64_t i = g0; i < (int64_t)p.num_experts * cap; i += gsz) {
+    const int e = (int)(i / cap);
+    const int64_t within = i - (int64_t)e * cap;
+    const int64_t cnt = (int64_t)p.expert_offset[e + 1] - p.expert_offset[e];
+    if (within >= cnt) p.src_info[i] = -1;
+  }
+  for (int64_t i = g0; i < (int64_t)p.num_experts * p.num_ranks; i += gsz) {
+    const int e = (int)(i / p.num_ranks), src = (int)(i % p.num_ranks);
+    // pairs of expert e whose token is below src*T / (src+1)*T: binary search
+    // of the expert's ascending src_of_slot run
+    const int lo0 = p.expert_offset[e], hi0 = p.expert_offset[e + 1];
+    int64_t bounds[2];
+    for (int b = 0; b < 2; ++b) {
+      const int64_t key = (int64_t)(src + b) * T * p.topk;
+      int lo = lo0, hi = hi0;
+      while (lo < hi) {
+        const int mid = lo + (hi - lo) / 2;
+        if ((int64_t)p.src_of_slot[mid] < key) lo = mid + 1; else hi = mid;
+      }
+      bounds[b] = lo - lo0;
+    }
+    const int64_t begin = bounds[0] < cap ? bounds[0] : cap;
+    const int64_t end = bounds[1] < cap ? bounds[1] : cap;
+    p.layout_range[i] = (begin << 32) | (end - begin);
+    if (src == 0) {
+      const int64_t c = (int64_t)hi0 - lo0;
+      p.recv_count[e] = (int32_t)(c < cap ? c : cap);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ll_layout(const LlLayoutParams& p, cudaStream_t s) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t work = (int64_t)p.num_experts * p.capacity;
+  const int64_t pairs = (int64_t)p.num_tokens * p.topk;
+  if (pairs > work) work = pairs;
+  int64_t blocks = (work + 255) / 256;
+  if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+  if (blocks < 1) blocks = 1;
+  k_ll_layout<<<(unsigned)blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

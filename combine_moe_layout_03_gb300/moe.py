@@ -95,6 +95,10 @@ _lib.moe_dispatch_ranks.restype = ctypes.c_int
 _lib.moe_dispatch_ranks.argtypes = [_D] + [_vp] * 6 + [_sz, _vp]
 _lib.moe_combine_gather_ranks.restype = ctypes.c_int
 _lib.moe_combine_gather_ranks.argtypes = [_D, _vp, _i64, _vp, _vp, _vp]
+_lib.moe_ll_layout.restype = ctypes.c_int
+_lib.moe_ll_layout.argtypes = [_D, _i32] + [_vp] * 8 + [_vp]
+_lib.moe_dispatch_ll.restype = ctypes.c_int
+_lib.moe_dispatch_ll.argtypes = [_D, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp]
 _lib.moe_mask_topk_ids.restype = ctypes.c_int
 _lib.moe_mask_topk_ids.argtypes = [_vp, _i32, _i32, _vp, _vp]
 _lib.moe_pack_record.restype = ctypes.c_int
@@ -321,6 +325,45 @@ def moe_combine_gather_ranks(desc: MoeDesc, recv_out: torch.Tensor, send_head: t
     return out
 
 
+def moe_ll_layout(desc: MoeDesc, max_tokens_per_rank: int, topk_idx, lay: dict,
+                  out: dict | None = None, stream=None) -> dict:
+    """Fixed-capacity, expert-major receive layout (see include/moe.h)."""
+    n, k, e, r = desc.num_tokens, desc.topk, desc.num_experts, desc.num_ranks
+    cap = r * max_tokens_per_rank
+    dev = topk_idx.device
+    if out is None:
+        out = dict(ll_slot_of=torch.empty((n, k), dtype=torch.int32, device=dev),
+                   src_info=torch.empty((e, cap), dtype=torch.int32, device=dev),
+                   layout_range=torch.empty((e, r), dtype=torch.int64, device=dev),
+                   recv_count=torch.empty(e, dtype=torch.int32, device=dev))
+    rc = _lib.moe_ll_layout(ctypes.byref(desc.c()), int(max_tokens_per_rank), _ptr(topk_idx),
+                            _ptr(lay["slot_of"]), _ptr(lay["expert_offset"]),
+                            _ptr(lay["src_of_slot"]), _ptr(out["ll_slot_of"]),
+                            _ptr(out["src_info"]), _ptr(out["layout_range"]),
+                            _ptr(out["recv_count"]), _stream(stream))
+    _check(rc, "moe_ll_layout")
+    out["capacity"] = cap
+    return out
+
+
+def moe_dispatch_ll(desc: MoeDesc, hidden, scales, ll_slot_of, capacity: int,
+                    x_out=None, scales_out=None, stream=None):
+    """Payload and scales into [E * capacity, ...] buffers; returns (x_out, scales_out)."""
+    lay = moe_record_layout(desc)
+    rows = desc.num_experts * capacity
+    dev = hidden.device
+    if x_out is None:
+        x_out = torch.empty((rows, lay["payload_bytes"]), dtype=torch.uint8, device=dev)
+    if scales_out is None and lay["scale_bytes"]:
+        scales_out = torch.empty((rows, lay["scale_bytes"]), dtype=torch.uint8, device=dev)
+    sb = scales_out.numel() * scales_out.element_size() if scales_out is not None else 0
+    rc = _lib.moe_dispatch_ll(ctypes.byref(desc.c()), _ptr(hidden), _ptr(scales), _ptr(ll_slot_of),
+                              _ptr(x_out), x_out.numel() * x_out.element_size(), _ptr(scales_out),
+                              sb, _stream(stream))
+    _check(rc, "moe_dispatch_ll")
+    return x_out, scales_out
+
+
 def _slot_desc(num_ranks: int, sizes) -> _SlotDesc:
     d = _SlotDesc()
     d.num_tensors = len(sizes)
@@ -444,6 +487,26 @@ def prepare_dispatch(desc: MoeDesc, topk_idx, topk_weights, hidden, scales, slot
                                            records))
 
 
+def prepare_ll_layout(desc: MoeDesc, max_tokens_per_rank: int, topk_idx, lay: dict, out: dict,
+                      stream=None) -> Prepared:
+    d = desc.c()
+    ptrs = _vps(topk_idx, lay["slot_of"], lay["expert_offset"], lay["src_of_slot"],
+                out["ll_slot_of"], out["src_info"], out["layout_range"], out["recv_count"])
+    args = (ctypes.byref(d), ctypes.c_int32(max_tokens_per_rank), *ptrs,
+            ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_ll_layout", args, (d, topk_idx, lay, out))
+
+
+def prepare_dispatch_ll(desc: MoeDesc, hidden, scales, ll_slot_of, x_out, scales_out,
+                        stream=None) -> Prepared:
+    d = desc.c()
+    sb = scales_out.numel() * scales_out.element_size() if scales_out is not None else 0
+    args = (ctypes.byref(d), *_vps(hidden, scales, ll_slot_of, x_out),
+            ctypes.c_size_t(x_out.numel() * x_out.element_size()), ctypes.c_void_p(_ptr(scales_out)),
+            ctypes.c_size_t(sb), ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_dispatch_ll", args, (d, hidden, scales, ll_slot_of, x_out, scales_out))
+
+
 def prepare_combine(desc: MoeDesc, mode: int, expert_out, topk_idx, topk_weights, slot_of, out,
                     stream=None) -> Prepared:
     d = desc.c()
@@ -471,4 +534,5 @@ def exported_symbols() -> list[str]:
             "moe_layout_status", "moe_dispatch", "moe_combine", "moe_pack_record",
             "moe_unpack_record", "moe_layout_noalloc", "moe_combine_norm", "moe_slot_layout",
             "moe_pack_slots", "moe_unpack_slots", "moe_mask_topk_ids", "moe_rank_layout",
-            "moe_dispatch_ranks", "moe_combine_gather_ranks"]
+            "moe_dispatch_ranks", "moe_combine_gather_ranks", "moe_ll_layout",
+            "moe_dispatch_ll"]

@@ -22,6 +22,10 @@ and distributions follow the workloads of the pages:
 * rs          BF16 H=8192 ~N(0,1), R=4, 32..512 tokens per rank (vLLM PR
               "Eliminate staging from NCCL symmetric reduce-scatter",
               reduce-scatter latency table), top-8 of 256.
+* decode_ll   R=8 ranks x 128 tokens, H=7168 BF16 ~N(0,1), top-8 of 256
+              distinct uniform ids, |N(0,1)| weights (DeepEP README,
+              "Low-latency kernels with pure RDMA": 128 tokens per batch,
+              7168 hidden, top-8, FP8 dispatching and BF16 combining).
 * skewed      N=16384, H=7168, 256 experts with Zipf(s=1.2) popularity, top-8
               distinct, R=16, with a few experts of zero popularity so that
               empty experts occur.
@@ -44,6 +48,7 @@ __all__ = [
     "prefill_case",
     "rs_case",
     "skewed_case",
+    "decode_ll_case",
     "PAGE_SENTINEL_WORD",
 ]
 
@@ -202,5 +207,18 @@ def skewed_case(seed: int = 0, n: int = 16384, hidden: int = 7168, e: int = 256,
         name="skewed", num_tokens=n, hidden=hidden, num_experts=e, topk=k, num_ranks=r,
         topk_idx=route_zipf(g, n, e, k, s, num_zero),
         topk_weights=weights_softmax(g, n, k),
+        hidden_bf16=bf16_normal(g, (n, hidden)),
+    )
+
+
+def decode_ll_case(seed: int = 0, tokens_per_rank: int = 128, r: int = 8, hidden: int = 7168,
+                   e: int = 256, k: int = 8) -> dict:
+    g = rng_for(seed, 6)
+    n = tokens_per_rank * r
+    return dict(
+        name="decode_ll", num_tokens=n, hidden=hidden, num_experts=e, topk=k, num_ranks=r,
+        max_tokens_per_rank=tokens_per_rank,
+        topk_idx=route_uniform(g, n, e, k),
+        topk_weights=weights_abs_normal(g, n, k),
         hidden_bf16=bf16_normal(g, (n, hidden)),
     )

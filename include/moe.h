@@ -311,6 +311,45 @@ int moe_dispatch_ranks(const moe_desc_t* desc, const int32_t* topk_idx,
 int moe_combine_gather_ranks(const moe_desc_t* desc, const void* recv_out, int64_t recv_rows,
                              const int32_t* send_head, void* out, moe_stream_t stream);
 
+/* ---- fixed-capacity, expert-major receive buffers -------------------------
+ * The low-latency layout of DeepEP (csrc/deep_ep.cpp
+ * Buffer::low_latency_dispatch / low_latency_combine): every expert has room
+ * for capacity = R * max_tokens_per_rank received tokens (packed_recv_x
+ * [E_l, R * max_tokens, H] per rank; [E, capacity, ...] for all R ranks of one
+ * GPU), so buffer sizes never depend on the routing and the calls need no
+ * host-side counts. Source rank s owns tokens [s*T, (s+1)*T), T = N / R.
+ * Reading (the pages show the interface, not the kernels): expert e's pairs
+ * are packed compactly from position 0 in source-rank, then token, order --
+ * the stable slot order of moe_layout within e. */
+
+/* From moe_layout's outputs:
+ *   ll_slot_of   int32 [N,k]       e * capacity + position of pair (t, j), or -1
+ *                                  (id -1, or beyond the expert's capacity)
+ *   src_info     int32 [E,capacity] token index within its source rank, -1 in
+ *                                  unused positions
+ *   layout_range int64 [E,R]       begin << 32 | count of expert e's pairs from
+ *                                  source rank s
+ *   recv_count   int32 [E]         pairs received by each expert (capped at
+ *                                  capacity)
+ * Needs N % R == 0 and N / R <= max_tokens_per_rank. The combine back is
+ * moe_combine (TOPK) with slot_of = ll_slot_of and expert_out the
+ * [E * capacity, H] expert outputs. Errors: INVALID_ARG, SHAPE, ALIGNMENT, CUDA. */
+int moe_ll_layout(const moe_desc_t* desc, int32_t max_tokens_per_rank, const int32_t* topk_idx,
+                  const int32_t* slot_of, const int32_t* expert_offset,
+                  const int32_t* src_of_slot, int32_t* ll_slot_of, int32_t* src_info,
+                  int64_t* layout_range, int32_t* recv_count, moe_stream_t stream);
+
+/* Dispatch into the fixed-capacity buffers: the payload of moe_dispatch
+ * (quantised once per token) goes to row ll_slot_of[t, j] of x_out
+ * [E * capacity, payload_bytes] and its scales to the same row of scales_out
+ * [E * capacity, scale_bytes] (row-major; scales_out may be NULL when there
+ * are none). payload_bytes and scale_bytes must be multiples of 16 (FP8:
+ * H % 512 == 0, as DeepEP's low-latency FP8 cast requires). x_out_bytes and
+ * scales_out_bytes give the buffers' sizes. Errors: as moe_dispatch. */
+int moe_dispatch_ll(const moe_desc_t* desc, const void* hidden, const void* scales,
+                    const int32_t* ll_slot_of, void* x_out, size_t x_out_bytes, void* scales_out,
+                    size_t scales_out_bytes, moe_stream_t stream);
+
 /* ---- tensor-major rank slots and padded-token mask ----------------------
  * The decode all-gather of the vLLM compare view ds-exp-2...ds-exp-ag packs
  * each rank's 2-4 tensors (top-k ids, weights, hidden payload, scales) into

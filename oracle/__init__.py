@@ -59,7 +59,8 @@ def _load():
                      "oracle_combine_topk_ranks", "oracle_combine_topk_f64"):
             getattr(_lib, name).restype = i32
         for name in ("oracle_slot_layout", "oracle_pack_slots", "oracle_unpack_slots",
-                     "oracle_rank_layout", "oracle_dispatch_ranks", "oracle_combine_gather_ranks"):
+                     "oracle_rank_layout", "oracle_dispatch_ranks", "oracle_combine_gather_ranks",
+                     "oracle_ll_layout", "oracle_dispatch_ll"):
             getattr(_lib, name).restype = i32
         _lib.oracle_mask_topk_ids.restype = None
         _lib.oracle_combine_norm.restype = i32
@@ -347,3 +348,31 @@ def combine_gather_ranks(recv_out, send_head, hidden_size: int) -> np.ndarray:
     _check(_load().oracle_combine_gather_ranks(_p(y), _p(sh), n, r, hidden_size, _p(out)),
            "combine_gather_ranks")
     return out
+
+
+def ll_layout(topk_idx, num_experts: int, num_ranks: int, max_tokens_per_rank: int) -> dict:
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    n, k = idx.shape
+    cap = num_ranks * max_tokens_per_rank
+    out = dict(ll_slot_of=np.zeros((n, k), np.int32), src_info=np.zeros((num_experts, cap), np.int32),
+               layout_range=np.zeros((num_experts, num_ranks), np.int64),
+               recv_count=np.zeros(num_experts, np.int32))
+    _check(_load().oracle_ll_layout(_p(idx), n, k, num_experts, num_ranks, max_tokens_per_rank,
+                                    _p(out["ll_slot_of"]), _p(out["src_info"]),
+                                    _p(out["layout_range"]), _p(out["recv_count"])), "ll_layout")
+    return out
+
+
+def dispatch_ll(hidden, scales, ll_slot_of, rows: int, in_kind: int, out_kind: int,
+                hidden_size: int, raw_payload_bytes: int = 0, raw_scale_bytes: int = 0):
+    so = np.ascontiguousarray(ll_slot_of, dtype=np.int32)
+    n, k = so.shape
+    lay = record_layout(k, hidden_size, in_kind, out_kind, raw_payload_bytes, raw_scale_bytes)
+    x = np.zeros((rows, lay["payload_bytes"]), np.uint8)
+    sc = np.zeros((rows, max(lay["scale_bytes"], 1)), np.uint8)
+    h = np.ascontiguousarray(hidden)
+    s_in = None if scales is None else np.ascontiguousarray(scales)
+    _check(_load().oracle_dispatch_ll(_p(h), _p(s_in), n, k, hidden_size, in_kind, out_kind,
+                                      raw_payload_bytes, raw_scale_bytes, _p(so), rows, _p(x), _p(sc)),
+           "dispatch_ll")
+    return x, sc[:, : lay["scale_bytes"]]

@@ -741,3 +741,90 @@ int oracle_combine_gather_ranks(const uint16_t* recv_out, const int32_t* send_he
   }
   return 0;
 }
+
+/* ======================================================================== */
+/* Fixed-capacity, expert-major receive buffers                              */
+/* ======================================================================== */
+
+/* [EP] Buffer::low_latency_dispatch: every expert has capacity = R * max
+ * positions. Reading: expert e's pairs fill positions 0, 1, ... in ascending
+ * (t, j) order (source rank s owns tokens [s*T, (s+1)*T), T = N / R, so this
+ * is source-rank order); a pair past the capacity gets no position (-1).
+ * src_info is the token's index within its source rank; layout_range[e, s] is
+ * begin << 32 | count of e's positions taken by source rank s. */
+int oracle_ll_layout(const int32_t* topk_idx, int num_tokens, int topk, int num_experts,
+                     int num_ranks, int max_tokens_per_rank, int32_t* ll_slot_of,
+                     int32_t* src_info, int64_t* layout_range, int32_t* recv_count) {
+  if (num_ranks < 1 || num_tokens % num_ranks || max_tokens_per_rank < 1) return -1;
+  const int T = num_tokens / num_ranks;
+  if (T > max_tokens_per_rank) return -1;
+  const long cap = (long)num_ranks * max_tokens_per_rank;
+  for (long i = 0; i < (long)num_experts * cap; ++i) src_info[i] = -1;
+  for (long p = 0; p < (long)num_tokens * topk; ++p) ll_slot_of[p] = -1;
+  for (int e = 0; e < num_experts; ++e) {
+    long pos = 0;
+    for (int s = 0; s < num_ranks; ++s) {
+      long begin = pos;
+      for (int t = s * T; t < (s + 1) * T; ++t) {
+        for (int j = 0; j < topk; ++j) {
+          if (topk_idx[(long)t * topk + j] != e) continue;
+          if (pos < cap) {
+            ll_slot_of[(long)t * topk + j] = (int32_t)((long)e * cap + pos);
+            src_info[(long)e * cap + pos] = t - s * T;
+          }
+          ++pos;
+        }
+      }
+      long b = begin < cap ? begin : cap;
+      long en = pos < cap ? pos : cap;
+      layout_range[(long)e * num_ranks + s] = ((int64_t)b << 32) | (int64_t)(en - b);
+    }
+    recv_count[e] = (int32_t)(pos < cap ? pos : cap);
+  }
+  return 0;
+}
+
+/* The payload and scales of each token (as oracle_dispatch builds them) to
+ * rows ll_slot_of[t, j] of x_out and scales_out. */
+int oracle_dispatch_ll(const void* hidden, const void* scales, int num_tokens, int topk,
+                       int hidden_size, int in_kind, int out_kind, int raw_payload_bytes,
+                       int raw_scale_bytes, const int32_t* ll_slot_of, int64_t rows,
+                       uint8_t* x_out, uint8_t* scales_out) {
+  int32_t lay[7];
+  if (topk > 32 || oracle_record_layout(topk, hidden_size, in_kind, out_kind, raw_payload_bytes,
+                                        raw_scale_bytes, lay) != 0)
+    return -1;
+  const int S = lay[0], off_p = lay[3], off_s = lay[4], pb = lay[5], sb = lay[6];
+  uint8_t* one = (uint8_t*)malloc((size_t)S);
+  if (!one) return -2;
+  for (int t = 0; t < num_tokens; ++t) {
+    const void* h = NULL;
+    const void* sc = NULL;
+    if (in_kind == ORACLE_RAW) {
+      h = (const uint8_t*)hidden + (size_t)t * raw_payload_bytes;
+      sc = raw_scale_bytes ? (const void*)((const uint8_t*)scales + (size_t)t * raw_scale_bytes) : NULL;
+    } else {
+      h = (const uint16_t*)hidden + (size_t)t * hidden_size;
+    }
+    int32_t one_idx[32], one_slots[32];
+    float one_w[32];
+    for (int j = 0; j < topk; ++j) {
+      one_idx[j] = j == 0 ? 0 : -1;
+      one_w[j] = 0.0f;
+      one_slots[j] = j == 0 ? 0 : -1;
+    }
+    if (oracle_dispatch(one_idx, one_w, h, sc, 1, topk, hidden_size, in_kind, out_kind,
+                        raw_payload_bytes, raw_scale_bytes, one_slots, one) != 0) {
+      free(one);
+      return -1;
+    }
+    for (int j = 0; j < topk; ++j) {
+      int pos = ll_slot_of[(long)t * topk + j];
+      if (pos < 0 || pos >= rows) continue;
+      memcpy(x_out + (size_t)pos * pb, one + off_p, (size_t)pb);
+      if (sb) memcpy(scales_out + (size_t)pos * sb, one + off_s, (size_t)sb);
+    }
+  }
+  free(one);
+  return 0;
+}

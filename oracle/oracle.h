@@ -87,6 +87,14 @@ int oracle_dispatch_ranks(const int32_t* topk_idx, const float* topk_weights, co
                           uint8_t* records);
 int oracle_combine_gather_ranks(const uint16_t* recv_out, const int32_t* send_head,
                                 int num_tokens, int num_ranks, int hidden_size, uint16_t* out);
+/* Fixed-capacity, expert-major receive buffers ([EP] low-latency dispatch). */
+int oracle_ll_layout(const int32_t* topk_idx, int num_tokens, int topk, int num_experts,
+                     int num_ranks, int max_tokens_per_rank, int32_t* ll_slot_of,
+                     int32_t* src_info, int64_t* layout_range, int32_t* recv_count);
+int oracle_dispatch_ll(const void* hidden, const void* scales, int num_tokens, int topk,
+                       int hidden_size, int in_kind, int out_kind, int raw_payload_bytes,
+                       int raw_scale_bytes, const int32_t* ll_slot_of, int64_t rows,
+                       uint8_t* x_out, uint8_t* scales_out);
 /* Rank slots of the decode all-gather ([AG] make_desc) and the padded-token
  * mask ([AG] mask_topk_ids). */
 int oracle_slot_layout(int num_tensors, const int64_t* bytes, int64_t* offsets, int64_t* slot_bytes);
