@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmoe.so")
 OBJDIR = os.path.join(PKG, "_build")
 SOURCES = ["moe_api.cu", "layout.cu", "dispatch.cu", "combine.cu", "layout_static.cu",
-           "slots.cu", "ranks.cu"]
+           "slots.cu", "ranks.cu", "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE]

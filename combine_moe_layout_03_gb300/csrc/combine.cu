@@ -3,6 +3,8 @@
 // * Top-k weighted reduction of expert outputs back to token order (DeepEP
 //   repository, csrc/deep_ep.cpp Buffer::low_latency_combine):
 //     out[t] = bf16_rn( fp32 fma chain, ascending j, of w[t,j] * y[slot_of[t,j]] )
+//   With no weights (w = 1) this is the backward of dispatch: the sum of a
+//   token's k gradient rows.
 // * The same reduction grouped by destination rank: one fp32 partial per rank,
 //   partials summed in ascending rank order, one rounding (vLLM PR
 //   "Eliminate staging from NCCL symmetric reduce-scatter", Implementation:
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 3)
     if (uu < num_units && lane < k) {
       const int64_t q = (uu / units_per_token) * k + lane;
       nslot = p.slot_of[q];
-      nw = p.topk_weights[q];
+      nw = p.topk_weights ? p.topk_weights[q] : 1.0f;
       if (GROUP) nidx = p.topk_idx[q];
     }
   };
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(kRowThreads) k_combine_rows(CombineParams p) {
   if (lane < k) {
     const int64_t qq = (int64_t)t * k + lane;
     slot = p.slot_of[qq];
-    w = p.topk_weights[qq];
+    w = p.topk_weights ? p.topk_weights[qq] : 1.0f;
     if (GROUP) idx = p.topk_idx[qq];
   }
   const PairList pl = order_pairs<GROUP>(slot, w, idx, k, p.expert_out_rows, p.experts_per_rank);
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams
     if (lane < k) {
       const int64_t qq = (int64_t)t * k + lane;
       slot = p.slot_of[qq];
-      w = p.topk_weights[qq];
+      w = p.topk_weights ? p.topk_weights[qq] : 1.0f;
       if (GROUP) idx = p.topk_idx[qq];
     }
     pl = order_pairs<GROUP>(slot, w, idx, k, p.expert_out_rows, p.experts_per_rank);

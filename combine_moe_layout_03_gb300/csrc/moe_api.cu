@@ -452,6 +452,86 @@ int moe_dispatch_ll(const moe_desc_t* desc, const void* hidden, const void* scal
                                                  (uint8_t*)scales_out, rows, (cudaStream_t)stream));
 }
 
+int moe_combine_backward(const moe_desc_t* desc, const void* grad_out, const float* topk_weights,
+                         const int32_t* slot_of, const void* expert_out, int64_t rows,
+                         void* grad_expert_out, float* grad_weights, moe_stream_t stream) {
+  int rc = check_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens, H = desc->hidden;
+  if (H < 8 || H % 8) return MOE_ERR_SHAPE;
+  if (rows < 0) return MOE_ERR_INVALID_ARG;
+  if (N == 0) return MOE_OK;
+  if (!grad_out || !topk_weights || !slot_of || !grad_expert_out) return MOE_ERR_INVALID_ARG;
+  if (expert_out && !grad_weights) return MOE_ERR_INVALID_ARG;
+  if (expert_out && expert_out == grad_expert_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(grad_out, 16) || !aligned(grad_expert_out, 16) || !aligned(expert_out, 16) ||
+      !aligned(topk_weights, 4) || !aligned(slot_of, 4) || !aligned(grad_weights, 4))
+    return MOE_ERR_ALIGNMENT;
+  moe::CombineBwdParams p;
+  p.grad_out = (const uint8_t*)grad_out;
+  p.topk_weights = topk_weights;
+  p.slot_of = slot_of;
+  p.expert_out = (const uint8_t*)expert_out;
+  p.rows = rows;
+  p.grad_expert_out = (uint8_t*)grad_expert_out;
+  p.grad_weights = expert_out ? grad_weights : nullptr;
+  p.num_tokens = N;
+  p.topk = desc->topk;
+  p.hidden_size = H;
+  return cuda_status(moe::launch_combine_backward(p, (cudaStream_t)stream));
+}
+
+int moe_dispatch_backward(const moe_desc_t* desc, const void* grad_in, int64_t rows,
+                          const int32_t* slot_of, void* grad_hidden, moe_stream_t stream) {
+  int rc = check_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens, H = desc->hidden;
+  if (H < 8 || H % 8) return MOE_ERR_SHAPE;
+  if ((int64_t)H / 8 > (int64_t)65535 * 128) return MOE_ERR_SHAPE;
+  if (rows < 0) return MOE_ERR_INVALID_ARG;
+  if (N == 0) return MOE_OK;
+  if (!grad_in || !slot_of || !grad_hidden) return MOE_ERR_INVALID_ARG;
+  if (!aligned(grad_in, 16) || !aligned(grad_hidden, 16) || !aligned(slot_of, 4))
+    return MOE_ERR_ALIGNMENT;
+  moe::CombineParams p;
+  p.expert_out = (const uint8_t*)grad_in;
+  p.expert_out_rows = rows;
+  p.topk_idx = nullptr;
+  p.topk_weights = nullptr;  // unit weights
+  p.slot_of = slot_of;
+  p.out = (uint8_t*)grad_hidden;
+  p.num_tokens = N;
+  p.topk = desc->topk;
+  p.hidden_size = H;
+  p.num_ranks = desc->num_ranks;
+  p.experts_per_rank = desc->num_experts / desc->num_ranks;
+  p.group_by_rank = 0;
+  return cuda_status(moe::launch_combine_topk(p, (cudaStream_t)stream));
+}
+
+int moe_combine_gather_ranks_backward(const moe_desc_t* desc, const void* grad_out,
+                                      const int32_t* send_head, void* grad_recv,
+                                      int64_t recv_rows, moe_stream_t stream) {
+  int rc = check_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens, H = desc->hidden;
+  if (H < 8 || H % 8) return MOE_ERR_SHAPE;
+  if (recv_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (N == 0) return MOE_OK;
+  if (!grad_out || !send_head || !grad_recv) return MOE_ERR_INVALID_ARG;
+  if (!aligned(grad_out, 16) || !aligned(grad_recv, 16) || !aligned(send_head, 4))
+    return MOE_ERR_ALIGNMENT;
+  moe::RankCombineBwdParams p;
+  p.grad_out = (const uint8_t*)grad_out;
+  p.send_head = send_head;
+  p.grad_recv = (uint8_t*)grad_recv;
+  p.rows = recv_rows;
+  p.num_tokens = N;
+  p.num_ranks = desc->num_ranks;
+  p.hidden_size = H;
+  return cuda_status(moe::launch_gather_ranks_backward(p, (cudaStream_t)stream));
+}
+
 int moe_slot_layout(const moe_slot_desc_t* desc, int64_t* offsets, int64_t* slot_bytes) {
   if (!desc || !offsets || !slot_bytes) return MOE_ERR_INVALID_ARG;
   if (desc->num_tensors < 2 || desc->num_tensors > MOE_MAX_SLOT_TENSORS || desc->num_ranks < 1)

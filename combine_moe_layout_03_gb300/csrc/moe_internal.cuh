@@ -98,6 +98,25 @@ struct LlLayoutParams {
   int num_tokens, topk, num_experts, num_ranks;
 };
 
+struct CombineBwdParams {
+  const uint8_t* grad_out;     // bf16 [N, H]
+  const float* topk_weights;   // [N, k]
+  const int32_t* slot_of;      // [N, k]
+  const uint8_t* expert_out;   // bf16 [rows, H], null: no weight gradient
+  int64_t rows;
+  uint8_t* grad_expert_out;    // bf16 [rows, H]
+  float* grad_weights;         // [N, k], used with expert_out
+  int num_tokens, topk, hidden_size;
+};
+
+struct RankCombineBwdParams {
+  const uint8_t* grad_out;  // bf16 [N, H]
+  const int32_t* send_head; // [N, R]
+  uint8_t* grad_recv;       // bf16 [rows, H]
+  int64_t rows;
+  int num_tokens, num_ranks, hidden_size;
+};
+
 // Workspace carving shared by moe_workspace_size and moe_layout.
 constexpr int kLayoutTokensPerChunk = 128;
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
@@ -117,6 +136,8 @@ cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const i
                                   int num_ranks, int experts_per_rank, cudaStream_t s);
 cudaError_t launch_combine_gather_ranks(const RankCombineParams& p, cudaStream_t s);
 cudaError_t launch_ll_layout(const LlLayoutParams& p, cudaStream_t s);
+cudaError_t launch_combine_backward(const CombineBwdParams& p, cudaStream_t s);
+cudaError_t launch_gather_ranks_backward(const RankCombineBwdParams& p, cudaStream_t s);
 cudaError_t launch_dispatch_packed(const DispatchParams& p, int out_kind, uint8_t* x_out,
                                    uint8_t* scales_out, int64_t rows, cudaStream_t s);
 cudaError_t launch_mask_topk_ids(int32_t* ids, int64_t total, int topk, const int32_t* num_actual,

@@ -99,6 +99,12 @@ _lib.moe_ll_layout.restype = ctypes.c_int
 _lib.moe_ll_layout.argtypes = [_D, _i32] + [_vp] * 8 + [_vp]
 _lib.moe_dispatch_ll.restype = ctypes.c_int
 _lib.moe_dispatch_ll.argtypes = [_D, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp]
+_lib.moe_combine_backward.restype = ctypes.c_int
+_lib.moe_combine_backward.argtypes = [_D, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp]
+_lib.moe_dispatch_backward.restype = ctypes.c_int
+_lib.moe_dispatch_backward.argtypes = [_D, _vp, _i64, _vp, _vp, _vp]
+_lib.moe_combine_gather_ranks_backward.restype = ctypes.c_int
+_lib.moe_combine_gather_ranks_backward.argtypes = [_D, _vp, _vp, _vp, _i64, _vp]
 _lib.moe_mask_topk_ids.restype = ctypes.c_int
 _lib.moe_mask_topk_ids.argtypes = [_vp, _i32, _i32, _vp, _vp]
 _lib.moe_pack_record.restype = ctypes.c_int
@@ -325,6 +331,49 @@ def moe_combine_gather_ranks(desc: MoeDesc, recv_out: torch.Tensor, send_head: t
     return out
 
 
+def moe_combine_backward(desc: MoeDesc, grad_out, topk_weights, slot_of, expert_out=None,
+                         rows: int | None = None, grad_expert_out=None, grad_weights=None,
+                         stream=None):
+    """Backward of the top-k weighted combine (see include/moe.h). Returns
+    (grad_expert_out bf16 [rows, H], grad_weights fp32 [N, k] or None)."""
+    h = desc.hidden
+    if rows is None:
+        rows = expert_out.numel() // h if expert_out is not None else grad_expert_out.numel() // h
+    dev = grad_out.device
+    if grad_expert_out is None:
+        grad_expert_out = torch.zeros((rows, h), dtype=torch.bfloat16, device=dev)
+    if expert_out is not None and grad_weights is None:
+        grad_weights = torch.empty((desc.num_tokens, desc.topk), dtype=torch.float32, device=dev)
+    rc = _lib.moe_combine_backward(ctypes.byref(desc.c()), _ptr(grad_out), _ptr(topk_weights),
+                                   _ptr(slot_of), _ptr(expert_out), int(rows), _ptr(grad_expert_out),
+                                   _ptr(grad_weights) if expert_out is not None else None,
+                                   _stream(stream))
+    _check(rc, "moe_combine_backward")
+    return grad_expert_out, grad_weights if expert_out is not None else None
+
+
+def moe_dispatch_backward(desc: MoeDesc, grad_in, slot_of, grad_hidden=None, stream=None):
+    """Backward of dispatch: grad_hidden[t] = bf16(sum_j grad_in[slot_of[t, j]])."""
+    if grad_hidden is None:
+        grad_hidden = torch.empty((desc.num_tokens, desc.hidden), dtype=torch.bfloat16,
+                                  device=grad_in.device)
+    rows = grad_in.numel() // max(desc.hidden, 1)
+    rc = _lib.moe_dispatch_backward(ctypes.byref(desc.c()), _ptr(grad_in), rows, _ptr(slot_of),
+                                    _ptr(grad_hidden), _stream(stream))
+    _check(rc, "moe_dispatch_backward")
+    return grad_hidden
+
+
+def moe_combine_gather_ranks_backward(desc: MoeDesc, grad_out, send_head, grad_recv, stream=None):
+    """grad_recv[send_head[t, r]] = grad_out[t] for every rank row the token read."""
+    rows = grad_recv.numel() // max(desc.hidden, 1)
+    rc = _lib.moe_combine_gather_ranks_backward(ctypes.byref(desc.c()), _ptr(grad_out),
+                                                _ptr(send_head), _ptr(grad_recv), rows,
+                                                _stream(stream))
+    _check(rc, "moe_combine_gather_ranks_backward")
+    return grad_recv
+
+
 def moe_ll_layout(desc: MoeDesc, max_tokens_per_rank: int, topk_idx, lay: dict,
                   out: dict | None = None, stream=None) -> dict:
     """Fixed-capacity, expert-major receive layout (see include/moe.h)."""
@@ -535,4 +584,5 @@ def exported_symbols() -> list[str]:
             "moe_unpack_record", "moe_layout_noalloc", "moe_combine_norm", "moe_slot_layout",
             "moe_pack_slots", "moe_unpack_slots", "moe_mask_topk_ids", "moe_rank_layout",
             "moe_dispatch_ranks", "moe_combine_gather_ranks", "moe_ll_layout",
-            "moe_dispatch_ll"]
+            "moe_dispatch_ll", "moe_combine_backward", "moe_dispatch_backward",
+            "moe_combine_gather_ranks_backward"]

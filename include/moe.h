@@ -350,6 +350,47 @@ int moe_dispatch_ll(const moe_desc_t* desc, const void* hidden, const void* scal
                     const int32_t* ll_slot_of, void* x_out, size_t x_out_bytes, void* scales_out,
                     size_t scales_out_bytes, moe_stream_t stream);
 
+/* ---- backward (training) ------------------------------------------------
+ * DeepEP README, "Example use in model training or inference prefilling":
+ * the backward of combine is a dispatch of the gradient through the cached
+ * handle (the layout is not recomputed), and the backward of dispatch is a
+ * combine. Here the "handle" is the slot map (slot_of, ll_slot_of or
+ * send_head) the forward calls used. */
+
+/* Backward of the top-k weighted combine out[t] = sum_j w[t,j] * y[slot_of[t,j]]
+ * (moe_combine TOPK or TOPK_RANKS, which differ only in rounding order):
+ *   grad_expert_out[slot_of[t,j]] = bf16_rn(w[t,j] * grad_out[t])  (fp32 product)
+ *   grad_weights[t,j] = sum_h grad_out[t,h] * expert_out[slot_of[t,j], h]
+ *                       (fp32 accumulation, fixed order; 0 for a pair with no slot)
+ * grad_out bf16 [N, H]; expert_out bf16 [rows, H] or NULL (then no weight
+ * gradient and grad_weights is ignored); grad_expert_out bf16 [rows, H], of
+ * which only the rows some pair names are written; grad_weights fp32 [N, k].
+ * Slots outside [0, rows) are skipped. The buffers must not overlap.
+ * H % 8 == 0, bf16 buffers 16-byte aligned. Errors: INVALID_ARG, SHAPE,
+ * ALIGNMENT, CUDA. */
+int moe_combine_backward(const moe_desc_t* desc, const void* grad_out, const float* topk_weights,
+                         const int32_t* slot_of, const void* expert_out, int64_t rows,
+                         void* grad_expert_out, float* grad_weights, moe_stream_t stream);
+
+/* Backward of dispatch with a BF16 payload (FP8 and NVFP4 taken as identity,
+ * the straight-through reading): every pair's record carried the token's row,
+ * so the gradient of that row is the sum of its pairs' gradient rows,
+ *   grad_hidden[t] = bf16_rn( fp32 sum, ascending j, of grad_in[slot_of[t,j]] )
+ * i.e. moe_combine (TOPK) with unit weights. grad_in bf16 [rows, H];
+ * grad_hidden bf16 [N, H]. Errors: as moe_combine. */
+int moe_dispatch_backward(const moe_desc_t* desc, const void* grad_in, int64_t rows,
+                          const int32_t* slot_of, void* grad_hidden, moe_stream_t stream);
+
+/* Backward of moe_combine_gather_ranks: every rank row the token's sum read
+ * gets the token's gradient, grad_recv[send_head[t, r]] = grad_out[t] for each
+ * r with send_head[t, r] in [0, recv_rows). grad_out bf16 [N, H]; grad_recv
+ * bf16 [recv_rows, H]; only named rows are written. The backward of
+ * moe_dispatch_ranks is moe_combine_gather_ranks itself. Errors: INVALID_ARG,
+ * SHAPE, ALIGNMENT, CUDA. */
+int moe_combine_gather_ranks_backward(const moe_desc_t* desc, const void* grad_out,
+                                      const int32_t* send_head, void* grad_recv,
+                                      int64_t recv_rows, moe_stream_t stream);
+
 /* ---- tensor-major rank slots and padded-token mask ----------------------
  * The decode all-gather of the vLLM compare view ds-exp-2...ds-exp-ag packs
  * each rank's 2-4 tensors (top-k ids, weights, hidden payload, scales) into

@@ -60,7 +60,8 @@ def _load():
             getattr(_lib, name).restype = i32
         for name in ("oracle_slot_layout", "oracle_pack_slots", "oracle_unpack_slots",
                      "oracle_rank_layout", "oracle_dispatch_ranks", "oracle_combine_gather_ranks",
-                     "oracle_ll_layout", "oracle_dispatch_ll"):
+                     "oracle_ll_layout", "oracle_dispatch_ll", "oracle_combine_backward",
+                     "oracle_dispatch_backward", "oracle_gather_ranks_backward"):
             getattr(_lib, name).restype = i32
         _lib.oracle_mask_topk_ids.restype = None
         _lib.oracle_combine_norm.restype = i32
@@ -376,3 +377,39 @@ def dispatch_ll(hidden, scales, ll_slot_of, rows: int, in_kind: int, out_kind: i
                                       raw_payload_bytes, raw_scale_bytes, _p(so), rows, _p(x), _p(sc)),
            "dispatch_ll")
     return x, sc[:, : lay["scale_bytes"]]
+
+
+def combine_backward(grad_out, topk_weights, slot_of, y, rows: int, hidden_size: int,
+                     grad_y=None):
+    """(grad_y bf16 [rows, H], grad_w fp32 [N, k] or None). Rows of grad_y no
+    pair names keep their given values (zeros when grad_y is None)."""
+    g = np.ascontiguousarray(grad_out, dtype=np.uint16)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    n, k = so.shape
+    gy = np.zeros((rows, hidden_size), np.uint16) if grad_y is None else np.array(grad_y, np.uint16)
+    yy = None if y is None else np.ascontiguousarray(y, dtype=np.uint16)
+    gw = np.zeros((n, k), np.float32)
+    _check(_load().oracle_combine_backward(_p(g), _p(w), _p(so), _p(yy), rows, n, k, hidden_size,
+                                           _p(gy), _p(gw)), "combine_backward")
+    return gy, (gw if y is not None else None)
+
+
+def dispatch_backward(grad_in, slot_of, hidden_size: int) -> np.ndarray:
+    gi = np.ascontiguousarray(grad_in, dtype=np.uint16)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    n, k = so.shape
+    out = np.zeros((n, hidden_size), np.uint16)
+    _check(_load().oracle_dispatch_backward(_p(gi), _p(so), n, k, hidden_size, _p(out)),
+           "dispatch_backward")
+    return out
+
+
+def gather_ranks_backward(grad_out, send_head, rows: int, hidden_size: int, grad_recv=None):
+    g = np.ascontiguousarray(grad_out, dtype=np.uint16)
+    sh = np.ascontiguousarray(send_head, dtype=np.int32)
+    n, r = sh.shape
+    gr = np.zeros((rows, hidden_size), np.uint16) if grad_recv is None else np.array(grad_recv, np.uint16)
+    _check(_load().oracle_gather_ranks_backward(_p(g), _p(sh), n, r, hidden_size, rows, _p(gr)),
+           "gather_ranks_backward")
+    return gr

@@ -828,3 +828,85 @@ int oracle_dispatch_ll(const void* hidden, const void* scales, int num_tokens, i
   free(one);
   return 0;
 }
+
+/* ======================================================================== */
+/* Backward                                                                  */
+/* ======================================================================== */
+
+/* Backward of out[t] = sum_j w[t,j] * y[slot_of[t,j]] with respect to y and w
+ * (the derivative of a weighted sum):
+ *   grad_y[slot_of[t,j], h] = bf16( fp32 product w[t,j] * g[t,h] )
+ *   grad_w[t,j] = fp32( sum over h of g[t,h] * y[slot_of[t,j], h] )
+ * The dot product is summed in fp64, where every BF16 x BF16 product is
+ * exact, and rounded to fp32 once; it bounds the fp32 sums a kernel may take
+ * in any order. A pair with no slot (or one outside [0, rows)) gets
+ * grad_w = 0 and writes no row; rows no pair names are left as they are.
+ * y may be NULL: then grad_w is not written. */
+int oracle_combine_backward(const uint16_t* grad_out, const float* topk_weights,
+                            const int32_t* slot_of, const uint16_t* y, int64_t rows,
+                            int num_tokens, int topk, int hidden_size, uint16_t* grad_y,
+                            float* grad_w) {
+  for (int t = 0; t < num_tokens; ++t) {
+    const uint16_t* g = grad_out + (size_t)t * hidden_size;
+    for (int j = 0; j < topk; ++j) {
+      long p = (long)t * topk + j;
+      int s = slot_of[p];
+      int valid = s >= 0 && s < rows;
+      if (valid) {
+        float w = topk_weights[p];
+        uint16_t* dst = grad_y + (size_t)s * hidden_size;
+        for (int h = 0; h < hidden_size; ++h) {
+          float prod = w * oracle_bf16_to_f32(g[h]);
+          dst[h] = oracle_f32_to_bf16(prod);
+        }
+      }
+      if (y) {
+        double d = 0.0;
+        if (valid) {
+          const uint16_t* row = y + (size_t)s * hidden_size;
+          for (int h = 0; h < hidden_size; ++h)
+            d += (double)oracle_bf16_to_f32(g[h]) * (double)oracle_bf16_to_f32(row[h]);
+        }
+        grad_w[p] = (float)d;
+      }
+    }
+  }
+  return 0;
+}
+
+/* Backward of dispatch with respect to the token rows: each of a token's
+ * pairs carried a copy of its row, so the row's gradient is the sum of the
+ * copies' gradients, summed in fp32 in ascending j from +0 and rounded to
+ * BF16 once (the order and precision of the combine). Payload formats are
+ * taken as identity (straight-through). */
+int oracle_dispatch_backward(const uint16_t* grad_in, const int32_t* slot_of, int num_tokens,
+                             int topk, int hidden_size, uint16_t* grad_hidden) {
+  for (int t = 0; t < num_tokens; ++t) {
+    for (int h = 0; h < hidden_size; ++h) {
+      float acc = 0.0f;
+      for (int j = 0; j < topk; ++j) {
+        int s = slot_of[(long)t * topk + j];
+        if (s < 0) continue;
+        acc = acc + oracle_bf16_to_f32(grad_in[(size_t)s * hidden_size + h]);
+      }
+      grad_hidden[(size_t)t * hidden_size + h] = oracle_f32_to_bf16(acc);
+    }
+  }
+  return 0;
+}
+
+/* Backward of the rank-row gather out[t] = sum_r recv[send_head[t, r]]: every
+ * row the sum read receives the token's gradient unchanged. */
+int oracle_gather_ranks_backward(const uint16_t* grad_out, const int32_t* send_head,
+                                 int num_tokens, int num_ranks, int hidden_size, int64_t rows,
+                                 uint16_t* grad_recv) {
+  for (int t = 0; t < num_tokens; ++t) {
+    for (int r = 0; r < num_ranks; ++r) {
+      int s = send_head[(long)t * num_ranks + r];
+      if (s < 0 || s >= rows) continue;
+      memcpy(grad_recv + (size_t)s * hidden_size, grad_out + (size_t)t * hidden_size,
+             (size_t)hidden_size * 2);
+    }
+  }
+  return 0;
+}

@@ -95,6 +95,17 @@ int oracle_dispatch_ll(const void* hidden, const void* scales, int num_tokens, i
                        int hidden_size, int in_kind, int out_kind, int raw_payload_bytes,
                        int raw_scale_bytes, const int32_t* ll_slot_of, int64_t rows,
                        uint8_t* x_out, uint8_t* scales_out);
+/* Backward ([EP] README, model training example: the backward of combine is
+ * a dispatch through the cached handle, the backward of dispatch a combine). */
+int oracle_combine_backward(const uint16_t* grad_out, const float* topk_weights,
+                            const int32_t* slot_of, const uint16_t* y, int64_t rows,
+                            int num_tokens, int topk, int hidden_size, uint16_t* grad_y,
+                            float* grad_w);
+int oracle_dispatch_backward(const uint16_t* grad_in, const int32_t* slot_of, int num_tokens,
+                             int topk, int hidden_size, uint16_t* grad_hidden);
+int oracle_gather_ranks_backward(const uint16_t* grad_out, const int32_t* send_head,
+                                 int num_tokens, int num_ranks, int hidden_size, int64_t rows,
+                                 uint16_t* grad_recv);
 /* Rank slots of the decode all-gather ([AG] make_desc) and the padded-token
  * mask ([AG] mask_topk_ids). */
 int oracle_slot_layout(int num_tensors, const int64_t* bytes, int64_t* offsets, int64_t* slot_bytes);
