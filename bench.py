@@ -71,6 +71,13 @@ def workload_spec(name: str) -> dict:
                  out_kind="fp8", record_bytes=7472, per_rank=True,
                  text="prefill N=4096 H=7168 E=256 top-8 R=8; one record per (token, rank) "
                       "(FP8 dispatch), rank rows summed back (BF16 combine)")
+    elif name == "prefill_bwd":
+        s = dict(num_tokens=4096, hidden=7168, num_experts=256, topk=8, num_ranks=8,
+                 out_kind="fp8", record_bytes=7472, bwd=True,
+                 names=("handle", "combine_backward", "dispatch_backward"),
+                 text="prefill backward N=4096 H=7168 E=256 top-8 R=8: with the forward's slot "
+                      "map cached, combine backward (bf16(w*g) to each pair's row and the fp32 "
+                      "weight gradient) then dispatch backward (sum of each token's k rows)")
     elif name == "decode_ll":
         s = dict(num_tokens=1024, hidden=7168, num_experts=256, topk=8, num_ranks=8,
                  out_kind="fp8", record_bytes=7472, ll=True, max_tokens_per_rank=128,
@@ -93,6 +100,12 @@ def workload_spec(name: str) -> dict:
     )
     if s.get("norm"):  # + residual in, normed and new residual out
         s["bytes_per_token"]["combine"] += 2 * 2 * h
+    if s.get("bwd"):
+        s["bytes_per_token"] = dict(
+            layout=0,                                          # the cached slot map: no work
+            dispatch=2 * h + 8 * k + k * 2 * h * 2 + 4 * k,    # g, w, slots, k rows of y in; k rows, grad_w out
+            combine=k * 2 * h + 4 * k + 2 * h,                 # k gradient rows, slots in; row out
+        )
     if s.get("ll"):
         e = s["num_experts"]
         cap = r * s["max_tokens_per_rank"]
@@ -112,7 +125,7 @@ def workload_spec(name: str) -> dict:
 def make_inputs(spec: dict, seed: int = 0) -> dict:
     from combine_moe_layout_03_gb300 import synth
     n = spec["num_tokens"]
-    if spec["name"] in ("prefill", "prefill_norm", "prefill_ranks"):
+    if spec["name"] in ("prefill", "prefill_norm", "prefill_ranks", "prefill_bwd"):
         return synth.prefill_case(seed=seed, n=n)
     if spec["name"] == "skewed":
         return synth.skewed_case(seed=seed, n=n)
@@ -199,7 +212,10 @@ def recorded_traffic(kernel: str, workload: str) -> int | None:
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = {"combine": "combine.cu", "dispatch": "dispatch.cu", "layout": "layout.cu"}[kernel]
+    src = {"combine": "combine.cu", "dispatch": "dispatch.cu", "layout": "layout.cu",
+           "combine_backward": "backward.cu", "dispatch_backward": "combine.cu"}.get(kernel)
+    if src is None:
+        return None
     with open(os.path.join(ROOT, "combine_moe_layout_03_gb300", "csrc", src), "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()[:16]
     for line in open(path):
@@ -278,6 +294,9 @@ class Step:
         self.launches_per_step = layout_launches(n, k, e, r) + 1 + 1
         if spec.get("ll"):
             self._setup_ll(spec, dev)
+            return
+        if spec.get("bwd"):
+            self._setup_bwd(spec, dev, seed)
             return
         if spec.get("per_rank"):
             self._setup_per_rank(spec, dev, seed)
@@ -375,6 +394,37 @@ class Step:
         self.dispatch, self.combine = dp, cp
         self.launches_per_step = layout_launches(spec["num_tokens"], spec["topk"],
                                                  spec["num_experts"], spec["num_ranks"]) + 3
+
+    def _setup_bwd(self, spec, dev, seed):
+        """The backward step with the forward's slot map cached: the upstream
+        gradient g (in the role of the step's input) goes through combine
+        backward into the pairs' gradient rows and weight gradients, and
+        dispatch backward sums each token's rows into grad_hidden (the step's
+        output)."""
+        import torch
+        from combine_moe_layout_03_gb300 import synth
+        moe = self.moe
+        n, k, h = spec["num_tokens"], spec["topk"], spec["hidden"]
+        P = self.y.shape[0]
+        self.x = torch.from_numpy(synth.bf16_normal(synth.rng_for(seed, 14), (n, h))
+                                  .view(np.int16)).to(dev).view(torch.bfloat16)
+        self.sc = None
+        self.records = None
+        self.grad_y = torch.empty((P, h), dtype=torch.bfloat16, device=dev)
+        self.grad_w = torch.empty((n, k), dtype=torch.float32, device=dev)
+        self.calls_on = self._bwd_calls_on
+        cb, db = self._bwd_calls_on(torch.cuda.current_stream())
+        self.layout = lambda: None
+        self.dispatch, self.combine = cb, db
+        self.launches_per_step = 2
+
+    def _bwd_calls_on(self, stream):
+        moe = self.moe
+        h = stream.cuda_stream
+        return [moe.prepare_combine_backward(self.cdesc, self.x, self.w, self.lay["slot_of"], self.y,
+                                             self.y.shape[0], self.grad_y, self.grad_w, h),
+                moe.prepare_dispatch_backward(self.cdesc, self.grad_y, self.lay["slot_of"],
+                                              self.out, h)]
 
     def _ll_calls_on(self, stream):
         moe = self.moe
@@ -558,8 +608,13 @@ def run_ours(args, spec, rank, world):
     kern = {name: statistics.mean(v) for name, v in per.items()}
     dom = max(("dispatch", "combine"), key=lambda x: kern[x])
     bpt = spec["bytes_per_token"]
-    achieved = {name: bpt[name] * n / (kern[name] / 1e3) / 1e9 for name in kern}
+    achieved = {name: bpt[name] * n / (kern[name] / 1e3) / 1e9 if kern[name] > 0 else 0.0
+                for name in kern}
     step_bytes = sum(bpt.values()) * n
+    # the three timed calls under their own names (the backward step's are
+    # the cached handle, combine backward and dispatch backward)
+    label = dict(zip(("layout", "dispatch", "combine"),
+                     spec.get("names", ("layout", "dispatch", "combine"))))
 
     graph = measure_graph(st, K, flush, flush_read)
     e2e = measure_e2e(st, spec, dev, K, W, seed=rank) if rank == 0 else None
@@ -575,19 +630,20 @@ def run_ours(args, spec, rank, world):
                    "num_ranks": spec["num_ranks"], "record_bytes": spec["record_bytes"],
                    "combine_mode": "TOPK_RANKS + residual + RMSNorm" if spec.get("norm")
                    else "rank rows gathered per token" if spec.get("per_rank")
-                   else "TOPK over the fixed-capacity positions" if spec.get("ll") else "TOPK_RANKS",
+                   else "TOPK over the fixed-capacity positions" if spec.get("ll")
+                   else "backward of TOPK combine and of dispatch" if spec.get("bwd") else "TOPK_RANKS",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, then "
                          f"{L2_FLUSH_BYTES >> 20} MiB read, outside the timed events); step "
                          f"working set {step_bytes / 1e6:.0f} MB",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved[dom], 1),
+        "roofline": {"bound": "hbm", "kernel": label[dom], "achieved": round(achieved[dom], 1),
                      "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(achieved[dom] / peaks["hbm_gbs"], 4),
-                     "traffic": recorded_traffic(dom, spec["name"]),
+                     "traffic": recorded_traffic(label[dom], spec["name"]),
                      "algorithmic_bytes_per_launch": bpt[dom] * n},
-        "kernels_us": {name: round(v * 1e3, 2) for name, v in kern.items()},
-        "kernels_gbs": {name: round(v, 1) for name, v in achieved.items()},
-        "kernels_frac": {name: round(v / peaks["hbm_gbs"], 4) for name, v in achieved.items()},
+        "kernels_us": {label[name]: round(v * 1e3, 2) for name, v in kern.items()},
+        "kernels_gbs": {label[name]: round(v, 1) for name, v in achieved.items()},
+        "kernels_frac": {label[name]: round(v / peaks["hbm_gbs"], 4) for name, v in achieved.items()},
         "step_gbs": round(step_bytes / (total_ms / K / 1e3) / 1e9, 1),
         "gpu_launches": st.launches_per_step * K,
         "graph": graph,
@@ -692,6 +748,13 @@ def oracle_step(c: dict, spec: dict, t0: int, t1: int):
     e, r, h = spec["num_experts"], spec["num_ranks"], spec["hidden"]
     lay = oracle.layout(ids, e, r)
     P = lay["num_pairs"]
+    if spec.get("bwd"):
+        # backward with the slot map given: combine backward (expert rows are
+        # zero rows here) then dispatch backward
+        g = c["hidden_bf16"][t0:t1]
+        y = np.zeros((max(P, 1), h), np.uint16)
+        gy, _ = oracle.combine_backward(g, w, lay["slot_of"], y, max(P, 1), h)
+        return oracle.dispatch_backward(gy, lay["slot_of"], h)
     if spec.get("ll"):
         # the fixed-capacity path: positions, packed payload, top-k combine
         # (the expert outputs are zero rows of the full [E * capacity] buffer)
@@ -720,6 +783,14 @@ def oracle_step(c: dict, spec: dict, t0: int, t1: int):
     return rec
 
 
+def oracle_pass_text(spec: dict) -> str:
+    if spec.get("bwd"):
+        return "combine backward + dispatch backward"
+    if spec.get("ll"):
+        return "layout + fixed-capacity layout + packed dispatch + top-k combine"
+    return "layout + dispatch + combine"
+
+
 def cpu_baseline(spec: dict, budget_s: float = 12.0) -> dict:
     """The oracle as it stands, single-threaded, on a bounded sample."""
     c = make_inputs(spec, 0)
@@ -735,7 +806,7 @@ def cpu_baseline(spec: dict, budget_s: float = 12.0) -> dict:
     dt = time.perf_counter() - t
     return {"value": round(sample / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"first {sample} of {n} tokens of the {spec['name']} workload, one pass of "
-                      f"layout + dispatch + rank-grouped combine ({dt:.1f} s)"}
+                      f"{oracle_pass_text(spec)} ({dt:.1f} s)"}
 
 
 def run_reference(args, spec) -> dict:
@@ -763,7 +834,8 @@ def run_reference(args, spec) -> dict:
         "config": {"workload": spec["text"], "num_tokens": n, "sample_tokens_per_step": sample},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": 1,
                          "kind": "oracle",
-                         "sample": f"first {sample} of {n} tokens per step"},
+                         "sample": f"first {sample} of {n} tokens per step, one pass of "
+                                   f"{oracle_pass_text(spec)}"},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -793,7 +865,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill",
                     choices=["prefill", "decode", "rs", "skewed", "tiny", "prefill_norm",
-                             "prefill_ranks", "decode_ll", "ag_slots"])
+                             "prefill_ranks", "prefill_bwd", "decode_ll", "ag_slots"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

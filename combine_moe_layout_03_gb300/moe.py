@@ -566,6 +566,24 @@ def prepare_combine(desc: MoeDesc, mode: int, expert_out, topk_idx, topk_weights
     return Prepared("moe_combine", args, (d, expert_out, topk_idx, topk_weights, slot_of, out))
 
 
+def prepare_combine_backward(desc: MoeDesc, grad_out, topk_weights, slot_of, expert_out, rows: int,
+                             grad_expert_out, grad_weights, stream=None) -> Prepared:
+    d = desc.c()
+    args = (ctypes.byref(d), *_vps(grad_out, topk_weights, slot_of, expert_out),
+            ctypes.c_int64(rows), *_vps(grad_expert_out, grad_weights),
+            ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_combine_backward", args, (d, grad_out, topk_weights, slot_of, expert_out,
+                                                   grad_expert_out, grad_weights))
+
+
+def prepare_dispatch_backward(desc: MoeDesc, grad_in, slot_of, grad_hidden, stream=None) -> Prepared:
+    d = desc.c()
+    rows = grad_in.numel() // max(desc.hidden, 1)
+    args = (ctypes.byref(d), ctypes.c_void_p(_ptr(grad_in)), ctypes.c_int64(rows),
+            *_vps(slot_of, grad_hidden), ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_dispatch_backward", args, (d, grad_in, slot_of, grad_hidden))
+
+
 def prepare_combine_norm(desc: MoeDesc, mode: int, expert_out, topk_idx, topk_weights, slot_of,
                          residual_in, gamma, eps: float, normed_out, residual_out,
                          stream=None) -> Prepared:
