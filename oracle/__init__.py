@@ -63,6 +63,13 @@ def _load():
                      "oracle_ll_layout", "oracle_dispatch_ll", "oracle_combine_backward",
                      "oracle_dispatch_backward", "oracle_gather_ranks_backward"):
             getattr(_lib, name).restype = i32
+        # routines with 64-bit scalar arguments need their full signatures:
+        # ctypes passes a bare Python int as a 32-bit C int
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        _lib.oracle_dispatch_ll.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, i64,
+                                            vp, vp]
+        _lib.oracle_combine_backward.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp]
+        _lib.oracle_gather_ranks_backward.argtypes = [vp, vp, i32, i32, i32, i64, vp]
         _lib.oracle_mask_topk_ids.restype = None
         _lib.oracle_combine_norm.restype = i32
         _lib.oracle_combine_norm.argtypes = [i32] + [ctypes.c_void_p] * 4 + [i32] * 5 + \
