@@ -28,6 +28,8 @@ constexpr int kBwdWarps = kBwdThreads / 32;
 
 template <int KT, bool WITH_W>
 __global__ void __launch_bounds__(kBwdThreads) k_combine_backward(CombineBwdParams p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int s_slot[KT];
   __shared__ float s_w[KT];
   __shared__ float s_red[kBwdWarps][KT];
@@ -115,6 +117,8 @@ __global__ void __launch_bounds__(kBwdThreads) k_combine_backward(CombineBwdPara
 constexpr int kGatherBwdThreads = 256;
 
 __global__ void __launch_bounds__(kGatherBwdThreads) k_gather_ranks_backward(RankCombineBwdParams p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int s_slot[MOE_MAX_RANKS];
   __shared__ int s_n;
   const int t = blockIdx.x;
@@ -150,12 +154,14 @@ cudaError_t launch_combine_backward(const CombineBwdParams& p, cudaStream_t s) {
                  : p.topk <= 16 ? bwd_kernel<16>(with_w) : bwd_kernel<32>(with_w);
   CombineBwdParams q = p;
   void* args[] = {&q};
-  return cudaLaunchKernel(fn, dim3((unsigned)p.num_tokens), dim3(kBwdThreads), args, 0, s);
+  return launch_pdl(fn, dim3((unsigned)p.num_tokens), dim3(kBwdThreads), 0, s, args);
 }
 
 cudaError_t launch_gather_ranks_backward(const RankCombineBwdParams& p, cudaStream_t s) {
-  k_gather_ranks_backward<<<(unsigned)p.num_tokens, kGatherBwdThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  RankCombineBwdParams q = p;
+  void* args[] = {&q};
+  return launch_pdl((const void*)k_gather_ranks_backward, dim3((unsigned)p.num_tokens),
+                    dim3(kGatherBwdThreads), 0, s, args);
 }
 
 }  // namespace moe

@@ -146,6 +146,8 @@ __device__ __forceinline__ void combine_chunk(const PairList& pl, const uint8_t*
 template <bool GROUP>
 __global__ void __launch_bounds__(kCombineWarps * 32, 3)
     k_combine_topk(CombineParams p, int units_per_token, int chunks_per_unit, int64_t num_units) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = (int)lane_id();
   const int k = p.topk;
   const int chunks = p.hidden_size / 8;
@@ -199,6 +201,8 @@ constexpr int kRowBlocksPerSm = 4;
 
 template <bool GROUP>
 __global__ void __launch_bounds__(kRowThreads) k_combine_rows(CombineParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const int lane = (int)lane_id();
   const int k = p.topk;
@@ -234,6 +238,8 @@ constexpr int kNormThreads = 256;
 
 template <int MODE>
 __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams q) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float4 xsm4[];  // [chunks][2] float4 = the row's x in fp32
   float* xsm = reinterpret_cast<float*>(xsm4);
   const CombineParams& p = q.c;
@@ -337,6 +343,8 @@ __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams
 template <int RB>
 __global__ void __launch_bounds__(256) k_combine_ranks(const uint8_t* partials, uint8_t* out,
                                                        int64_t chunks, int num_ranks) {
+  pdl_wait();
+  pdl_trigger();
   const size_t rank_stride = (size_t)chunks * 16;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -405,11 +413,10 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorInvalidDevice;
   if (p.num_tokens >= di->sms * kRowBlocksPerSm * 2) {  // enough tokens: one block per row
-    if (p.group_by_rank)
-      k_combine_rows<true><<<(unsigned)p.num_tokens, kRowThreads, 0, s>>>(p);
-    else
-      k_combine_rows<false><<<(unsigned)p.num_tokens, kRowThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    CombineParams q = p;
+    void* args[] = {&q};
+    const void* fn = p.group_by_rank ? (const void*)k_combine_rows<true> : (const void*)k_combine_rows<false>;
+    return launch_pdl(fn, dim3((unsigned)p.num_tokens), dim3(kRowThreads), 0, s, args);
   }
   const int chunks = p.hidden_size / 8;
   const int steps_per_token = (chunks + 31) / 32;  // warp steps of 32 chunks
@@ -426,11 +433,12 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   int64_t blocks = (num_units + kCombineWarps - 1) / kCombineWarps;
   const int64_t cap = (int64_t)di->sms * di->topk_blocks[g];
   if (blocks > cap) blocks = cap;
-  if (p.group_by_rank)
-    k_combine_topk<true><<<(unsigned)blocks, kCombineWarps * 32, 0, s>>>(p, units_per_token, chunks_per_unit, num_units);
-  else
-    k_combine_topk<false><<<(unsigned)blocks, kCombineWarps * 32, 0, s>>>(p, units_per_token, chunks_per_unit, num_units);
-  return cudaGetLastError();
+  CombineParams q = p;
+  int upt = units_per_token, cpu = chunks_per_unit;
+  int64_t nu = num_units;
+  void* args[] = {&q, &upt, &cpu, &nu};
+  const void* fn = p.group_by_rank ? (const void*)k_combine_topk<true> : (const void*)k_combine_topk<false>;
+  return launch_pdl(fn, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s, args);
 }
 
 cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t rows,
@@ -441,8 +449,12 @@ cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t 
   int64_t blocks = (chunks + 255) / 256;
   const int64_t cap = (int64_t)di->sms * 8;
   if (blocks > cap) blocks = cap;
-  k_combine_ranks<4><<<(unsigned)blocks, 256, 0, s>>>(partials, out, chunks, num_ranks);
-  return cudaGetLastError();
+  const uint8_t* a0 = partials;
+  uint8_t* a1 = out;
+  int64_t a2 = chunks;
+  int a3 = num_ranks;
+  void* args[] = {&a0, &a1, &a2, &a3};
+  return launch_pdl((const void*)k_combine_ranks<4>, dim3((unsigned)blocks), dim3(256), 0, s, args);
 }
 
 cudaError_t launch_combine_norm(const CombineNormParams& p, cudaStream_t s) {
@@ -456,7 +468,7 @@ cudaError_t launch_combine_norm(const CombineNormParams& p, cudaStream_t s) {
   }
   CombineNormParams q = p;
   void* args[] = {&q};
-  return cudaLaunchKernel(fn, dim3((unsigned)p.c.num_tokens), dim3(kNormThreads), args, smem, s);
+  return launch_pdl(fn, dim3((unsigned)p.c.num_tokens), dim3(kNormThreads), smem, s, args);
 }
 
 }  // namespace moe

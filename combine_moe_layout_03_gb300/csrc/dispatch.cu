@@ -115,6 +115,8 @@ __device__ __forceinline__ void quant_nvfp4(const uint8_t* row, int H, uint8_t* 
 
 template <int OUT_KIND>
 __global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p) {
+  pdl_wait();
+  pdl_trigger();
   // Dynamic shared memory: the record body (record bytes [16, record_bytes)),
   // then, for the quantising kinds, the staged BF16 input row.
   extern __shared__ __align__(128) uint8_t img[];
@@ -189,6 +191,8 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p)
 template <int OUT_KIND>
 __global__ void __launch_bounds__(kDispatchThreads)
     k_dispatch_ranks(DispatchParams p, const int32_t* send_head, int num_ranks, int experts_per_rank) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t img[];  // record bytes [off_payload, record_bytes)
   __shared__ int s_ids[MOE_MAX_TOPK];
   __shared__ uint32_t s_w[MOE_MAX_TOPK];
@@ -269,6 +273,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
 template <int OUT_KIND>
 __global__ void __launch_bounds__(kDispatchThreads)
     k_dispatch_packed(DispatchParams p, uint8_t* x_out, uint8_t* scales_out, int64_t rows) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t img[];  // payload | scales | staged row
   __shared__ int s_pos[MOE_MAX_TOPK];
   const int t = blockIdx.x;
@@ -328,7 +334,7 @@ cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, 
   }
   DispatchParams q = p;
   void* args[] = {&q};
-  return cudaLaunchKernel(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), args, smem, s);
+  return launch_pdl(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), smem, s, args);
 }
 
 cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const int32_t* send_head,
@@ -350,7 +356,7 @@ cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const i
   const int32_t* sh = send_head;
   int nr = num_ranks, epr = experts_per_rank;
   void* args[] = {&q, &sh, &nr, &epr};
-  return cudaLaunchKernel(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), args, smem, s);
+  return launch_pdl(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), smem, s, args);
 }
 
 cudaError_t launch_dispatch_packed(const DispatchParams& p, int out_kind, uint8_t* x_out,
@@ -373,7 +379,7 @@ cudaError_t launch_dispatch_packed(const DispatchParams& p, int out_kind, uint8_
   uint8_t* so = scales_out;
   int64_t r = rows;
   void* args[] = {&q, &xo, &so, &r};
-  return cudaLaunchKernel(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), args, smem, s);
+  return launch_pdl(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), smem, s, args);
 }
 
 }  // namespace moe

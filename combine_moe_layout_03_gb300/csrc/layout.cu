@@ -230,6 +230,8 @@ __device__ void clear_src_tail(const LayoutParams& p, int64_t P) {
 }
 
 __global__ void __launch_bounds__(kCountThreads) k_layout_count(LayoutParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int smem[];
   const int E = p.num_experts, R = p.num_ranks;
   int* cnt = smem;
@@ -323,6 +325,8 @@ __device__ int64_t scan_chunks(const LayoutParams& p, int c, int* base, int* scr
 }
 
 __global__ void __launch_bounds__(kAssignThreads) k_layout_assign(LayoutParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int smem[];
   const int E = p.num_experts;
   int* scratch = smem;            // 33 (+3 pad)
@@ -349,6 +353,8 @@ __global__ void __launch_bounds__(kAssignThreads) k_layout_assign(LayoutParams p
 // barrier keeps every block's shared memory alive until the others have read
 // it.
 __global__ void __launch_bounds__(kClusterThreads) k_layout_cluster(LayoutParams p, int tokens_per_block) {
+  pdl_wait();
+  pdl_trigger();
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ int smem[];
@@ -531,32 +537,26 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s) {
   if (cp.smem <= kClusterMaxSmem) {
     cudaError_t err = set_smem((const void*)k_layout_cluster, cp.smem);
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)cp.blocks);
-    cfg.blockDim = dim3(kClusterThreads);
-    cfg.dynamicSmemBytes = cp.smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cp.blocks;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_layout_cluster, p, cp.tokens_per_block);
+    LayoutParams q = p;
+    int tpb = cp.tokens_per_block;
+    void* args[] = {&q, &tpb};
+    return launch_pdl((const void*)k_layout_cluster, dim3((unsigned)cp.blocks), dim3(kClusterThreads),
+                      cp.smem, s, args, (unsigned)cp.blocks);
   }
   const size_t chunk_ids = (size_t)p.tokens_per_chunk * p.topk;
   const size_t smem_count = (size_t)(2 * E + R + 1) * 4 + chunk_ids * 4;
   cudaError_t err = set_smem((const void*)k_layout_count, smem_count);
   if (err != cudaSuccess) return err;
-  k_layout_count<<<p.num_chunks, kCountThreads, smem_count, s>>>(p);
-  err = cudaGetLastError();
+  LayoutParams q = p;
+  void* args[] = {&q};
+  err = launch_pdl((const void*)k_layout_count, dim3(p.num_chunks), dim3(kCountThreads), smem_count, s,
+                   args);
   if (err != cudaSuccess) return err;
   const size_t smem_assign = (size_t)(36 + 2 * E + (kAssignThreads / 32) * E) * 4 + chunk_ids * 4;
   err = set_smem((const void*)k_layout_assign, smem_assign);
   if (err != cudaSuccess) return err;
-  k_layout_assign<<<p.num_chunks, kAssignThreads, smem_assign, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl((const void*)k_layout_assign, dim3(p.num_chunks), dim3(kAssignThreads), smem_assign,
+                    s, args);
 }
 
 }  // namespace moe

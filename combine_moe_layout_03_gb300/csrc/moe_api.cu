@@ -2,9 +2,48 @@
 // documented in include/moe.h): argument validation on the host, then the
 // launches. Nothing here allocates device memory or synchronises, except
 // moe_layout_status.
+#include <stdlib.h>
 #include <string.h>
 
 #include "moe_internal.cuh"
+
+namespace moe {
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_PDL");
+    return !(v && v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
+}
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       void** args, unsigned cluster_x) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace moe
 
 namespace {
 

@@ -117,6 +117,27 @@ struct RankCombineBwdParams {
   int num_tokens, num_ranks, hidden_size;
 };
 
+// Programmatic dependent launch. Every kernel of this library begins with
+// pdl_wait() -- griddepcontrol.wait: until the previous kernel in the stream
+// has completed and its memory operations are visible -- before its first
+// access to global memory, and then calls pdl_trigger() so that the next
+// kernel's blocks may be scheduled while this one drains. Launched through
+// launch_pdl (programmatic stream serialization), a kernel can thus be
+// resident before its predecessor ends, which hides the launch gap; launched
+// without it, both instructions do nothing. Setting the environment variable
+// MOE_PDL=0 launches every kernel in plain stream order.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+bool pdl_enabled();
+
+// cudaLaunchKernelExC with the programmatic-serialization attribute (when
+// enabled) and an optional cluster size (cluster_x > 0).
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       void** args, unsigned cluster_x = 0);
+
 // Workspace carving shared by moe_workspace_size and moe_layout.
 constexpr int kLayoutTokensPerChunk = 128;
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);

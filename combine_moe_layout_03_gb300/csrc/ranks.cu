@@ -26,6 +26,8 @@ constexpr int kRankLayoutThreads = 1024;
 constexpr int kRankCombineThreads = 256;
 
 __global__ void __launch_bounds__(kRankLayoutThreads) k_rank_layout(RankLayoutParams p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int scratch[36];
   const int r = blockIdx.x;
   const int N = p.num_tokens, R = p.num_ranks;
@@ -77,6 +79,8 @@ __global__ void __launch_bounds__(kRankLayoutThreads) k_rank_layout(RankLayoutPa
 }
 
 __global__ void __launch_bounds__(kRankCombineThreads) k_combine_gather_ranks(RankCombineParams p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int s_slot[MOE_MAX_RANKS];
   __shared__ int s_n;
   const int t = blockIdx.x;
@@ -127,13 +131,16 @@ __global__ void __launch_bounds__(kRankCombineThreads) k_combine_gather_ranks(Ra
 }  // namespace
 
 cudaError_t launch_rank_layout(const RankLayoutParams& p, cudaStream_t s) {
-  k_rank_layout<<<p.num_ranks, kRankLayoutThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  RankLayoutParams q = p;
+  void* args[] = {&q};
+  return launch_pdl((const void*)k_rank_layout, dim3(p.num_ranks), dim3(kRankLayoutThreads), 0, s, args);
 }
 
 cudaError_t launch_combine_gather_ranks(const RankCombineParams& p, cudaStream_t s) {
-  k_combine_gather_ranks<<<(unsigned)p.num_tokens, kRankCombineThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  RankCombineParams q = p;
+  void* args[] = {&q};
+  return launch_pdl((const void*)k_combine_gather_ranks, dim3((unsigned)p.num_tokens),
+                    dim3(kRankCombineThreads), 0, s, args);
 }
 
 }  // namespace moe
@@ -152,6 +159,8 @@ namespace moe {
 namespace {
 
 __global__ void k_ll_layout(LlLayoutParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t pairs = (int64_t)p.num_tokens * p.topk;
   const int64_t cap = p.capacity;
   const int T = p.num_tokens / p.num_ranks;
@@ -216,8 +225,9 @@ cudaError_t launch_ll_layout(const LlLayoutParams& p, cudaStream_t s) {
   int64_t blocks = (work + 255) / 256;
   if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
   if (blocks < 1) blocks = 1;
-  k_ll_layout<<<(unsigned)blocks, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  LlLayoutParams q = p;
+  void* args[] = {&q};
+  return launch_pdl((const void*)k_ll_layout, dim3((unsigned)blocks), dim3(256), 0, s, args);
 }
 
 }  // namespace moe

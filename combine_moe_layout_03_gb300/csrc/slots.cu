@@ -33,6 +33,8 @@ struct SlotArgs {
 // are contiguous in the slot since each size is a multiple of 16).
 template <bool PACK>
 __global__ void __launch_bounds__(kSlotThreads) k_slots(SlotArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = a.vec_per_rank * a.num_ranks;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
        g += (int64_t)gridDim.x * blockDim.x) {
@@ -51,6 +53,8 @@ __global__ void __launch_bounds__(kSlotThreads) k_slots(SlotArgs a) {
 }
 
 __global__ void k_mask_topk_ids(int32_t* ids, int64_t total, int topk, const int32_t* num_actual) {
+  pdl_wait();
+  pdl_trigger();
   const int na = *num_actual;  // a negative count masks every token
   const int64_t first = (int64_t)(na > 0 ? na : 0) * topk;
   for (int64_t i = first + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -87,18 +91,20 @@ cudaError_t launch_slots(bool pack, const void* const* src, void* const* dst,
   const int64_t work = a.vec_per_rank * a.num_ranks;
   if (work == 0) return cudaSuccess;
   const int blocks = blocks_for(work, kSlotThreads);
-  if (pack)
-    k_slots<true><<<blocks, kSlotThreads, 0, s>>>(a);
-  else
-    k_slots<false><<<blocks, kSlotThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  void* args[] = {&a};
+  return launch_pdl(pack ? (const void*)k_slots<true> : (const void*)k_slots<false>, dim3(blocks),
+                    dim3(kSlotThreads), 0, s, args);
 }
 
 cudaError_t launch_mask_topk_ids(int32_t* ids, int64_t total, int topk, const int32_t* num_actual,
                                  cudaStream_t s) {
   if (total == 0) return cudaSuccess;
-  k_mask_topk_ids<<<blocks_for(total, 256), 256, 0, s>>>(ids, total, topk, num_actual);
-  return cudaGetLastError();
+  int32_t* a0 = ids;
+  int64_t a1 = total;
+  int a2 = topk;
+  const int32_t* a3 = num_actual;
+  void* args[] = {&a0, &a1, &a2, &a3};
+  return launch_pdl((const void*)k_mask_topk_ids, dim3(blocks_for(total, 256)), dim3(256), 0, s, args);
 }
 
 }  // namespace moe
