@@ -197,7 +197,6 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 3)
 // and the low register count lets four blocks share an SM. Used when there
 // are enough tokens to fill the GPU.
 constexpr int kRowThreads = 256;
-constexpr int kRowBlocksPerSm = 4;
 
 template <bool GROUP>
 __global__ void __launch_bounds__(kRowThreads) k_combine_rows(CombineParams p) {
@@ -412,7 +411,10 @@ const DeviceInfo* device_info() {
 cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorInvalidDevice;
-  if (p.num_tokens >= di->sms * kRowBlocksPerSm * 2) {  // enough tokens: one block per row
+  // One block per row from about three rows per SM up; below that the
+  // persistent warp kernel, with units of two 32-chunk steps (one pair
+  // ordering per 64 chunks), keeps every SM busy.
+  if (p.num_tokens >= di->sms * 3) {
     CombineParams q = p;
     void* args[] = {&q};
     const void* fn = p.group_by_rank ? (const void*)k_combine_rows<true> : (const void*)k_combine_rows<false>;
@@ -421,13 +423,8 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   const int chunks = p.hidden_size / 8;
   const int steps_per_token = (chunks + 31) / 32;  // warp steps of 32 chunks
   const int g = p.group_by_rank ? 1 : 0;
-  const int64_t resident_warps = (int64_t)di->sms * di->topk_blocks[g] * kCombineWarps;
-  // about 4 units per resident warp, so the grid-stride loop balances well,
-  // but as few units per token as that allows (each unit pays one prologue)
-  int64_t per_unit = (int64_t)p.num_tokens * steps_per_token / (resident_warps * 4);
-  if (per_unit < 1) per_unit = 1;
-  if (per_unit > steps_per_token) per_unit = steps_per_token;
-  const int chunks_per_unit = (int)per_unit * 32;
+  const int per_unit = steps_per_token < 2 ? steps_per_token : 2;
+  const int chunks_per_unit = per_unit * 32;
   const int units_per_token = (chunks + chunks_per_unit - 1) / chunks_per_unit;
   const int64_t num_units = (int64_t)p.num_tokens * units_per_token;
   int64_t blocks = (num_units + kCombineWarps - 1) / kCombineWarps;

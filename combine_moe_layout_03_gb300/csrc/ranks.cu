@@ -158,58 +158,137 @@ cudaError_t launch_combine_gather_ranks(const RankCombineParams& p, cudaStream_t
 namespace moe {
 namespace {
 
-__global__ void k_ll_layout(LlLayoutParams p) {
+// Three independent jobs, each given its own blocks so that they run side by
+// side (each is a short chain of dependent loads):
+//  * pair blocks: ll_slot_of and src_info of every pair, from slot_of,
+//    topk_idx and expert_offset;
+//  * fill blocks: src_info = -1 at every position past its expert's count;
+//  * range blocks: one warp per expert counts the expert's pairs per source
+//    rank from its run of src_of_slot (pair indices in ascending order, so
+//    source ranks are nondecreasing along the run). A run of up to
+//    kRangeRegs * 32 slots is held in registers and counted with shared
+//    memory atomics (one round trip of loads); a longer run is split by a
+//    binary search per source rank, one lane per rank.
+constexpr int kLlThreads = 256;
+constexpr int kRangeRegs = 8;
+
+struct LlGrid {
+  int pair_blocks, fill_blocks, range_blocks;
+};
+
+__global__ void __launch_bounds__(kLlThreads) k_ll_layout(LlLayoutParams p, LlGrid g) {
   pdl_wait();
   pdl_trigger();
-  const int64_t pairs = (int64_t)p.num_tokens * p.topk;
+  __shared__ int s_cnt[kLlThreads / 32][MOE_MAX_RANKS];
   const int64_t cap = p.capacity;
   const int T = p.num_tokens / p.num_ranks;
-  const int64_t gsz = (int64_t)gridDim.x * blockDim.x;
-  const int64_t g0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  // ll_slot_of and src_info of every pair
-  for (int64_t q = g0; q < pairs; q += gsz) {
-    const int s = p.slot_of[q];
-    int64_t pos = -1;
-    if (s >= 0) {
+  const int b = blockIdx.x;
+  if (b < g.pair_blocks) {
+    const int64_t pairs = (int64_t)p.num_tokens * p.topk;
+    for (int64_t q = (int64_t)b * kLlThreads + threadIdx.x; q < pairs;
+         q += (int64_t)g.pair_blocks * kLlThreads) {
+      const int s = p.slot_of[q];
       const int e = p.topk_idx[q];
-      const int64_t within = (int64_t)s - p.expert_offset[e];
-      if (within >= 0 && within < cap) {
-        pos = (int64_t)e * cap + within;
-        const int t = (int)(q / p.topk);
-        p.src_info[pos] = t - (t / T) * T;  // token index within its source rank
+      int64_t pos = -1;
+      if (s >= 0 && e >= 0 && e < p.num_experts) {
+        const int64_t within = (int64_t)s - p.expert_offset[e];
+        if (within >= 0 && within < cap) {
+          pos = (int64_t)e * cap + within;
+          const int t = (int)(q / p.topk);
+          p.src_info[pos] = t - (t / T) * T;  // token index within its source rank
+        }
       }
+      p.ll_slot_of[q] = pos < (int64_t)INT32_MAX ? (int32_t)pos : -1;
     }
-    p.ll_slot_of[q] = pos < (int64_t)INT32_MAX ? (int32_t)pos : -1;
+    return;
   }
-  // src_info past each expert's count, counts and layout ranges
-  for (int64_t i = g0; i < (int64_t)p.num_experts * cap; i += gsz) {
-    const int e = (int)(i / cap);
-    const int64_t within = i - (int64_t)e * cap;
-    const int64_t cnt = (int64_t)p.expert_offset[e + 1] - p.expert_offset[e];
-    if (within >= cnt) p.src_info[i] = -1;
+  if (b < g.pair_blocks + g.fill_blocks) {
+    const int64_t total = (int64_t)p.num_experts * cap;
+    for (int64_t i = (int64_t)(b - g.pair_blocks) * kLlThreads + threadIdx.x; i < total;
+         i += (int64_t)g.fill_blocks * kLlThreads) {
+      const int e = (int)(i / cap);
+      const int64_t cnt = (int64_t)p.expert_offset[e + 1] - p.expert_offset[e];
+      if (i - (int64_t)e * cap >= cnt) p.src_info[i] = -1;
+    }
+    return;
   }
-  for (int64_t i = g0; i < (int64_t)p.num_experts * p.num_ranks; i += gsz) {
-    const int e = (int)(i / p.num_ranks), src = (int)(i % p.num_ranks);
-    // pairs of expert e whose token is below src*T / (src+1)*T: binary search
-    // of the expert's ascending src_of_slot run
-    const int lo0 = p.expert_offset[e], hi0 = p.expert_offset[e + 1];
-    int64_t bounds[2];
-    for (int b = 0; b < 2; ++b) {
-      const int64_t key = (int64_t)(src + b) * T * p.topk;
-      int lo = lo0, hi = hi0;
-      while (lo < hi) {
-        const int mid = lo + (hi - lo) / 2;
-        if ((int64_t)p.src_of_slot[mid] < key) lo = mid + 1; else hi = mid;
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int R = p.num_ranks;
+  const int64_t pairs_per_rank = (int64_t)T * p.topk;
+  int* cnt = s_cnt[wib];
+  const int warps = g.range_blocks * (kLlThreads / 32);
+  for (int e = (b - g.pair_blocks - g.fill_blocks) * (kLlThreads / 32) + wib; e < p.num_experts;
+       e += warps) {
+    const int lo = p.expert_offset[e], hi = p.expert_offset[e + 1];
+    const int len = hi - lo;
+    int64_t begin_lo, begin_hi;  // begin of source ranks lane and lane + 32
+    if (len <= kRangeRegs * 32) {
+      for (int r = lane; r < R; r += 32) cnt[r] = 0;
+      __syncwarp();
+      int src[kRangeRegs];
+#pragma unroll
+      for (int c = 0; c < kRangeRegs; ++c) {
+        const int i = c * 32 + lane;
+        src[c] = i < len ? p.src_of_slot[lo + i] : -1;
       }
-      bounds[b] = lo - lo0;
+#pragma unroll
+      for (int c = 0; c < kRangeRegs; ++c)
+        if (src[c] >= 0) atomicAdd(&cnt[(int)(src[c] / pairs_per_rank)], 1);
+      __syncwarp();
+      // exclusive scan of the per-rank counts: lane r holds ranks r, r + 32
+      const int c0 = lane < R ? cnt[lane] : 0;
+      const int c1 = lane + 32 < R ? cnt[lane + 32] : 0;
+      int inc0 = c0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc0, o);
+        if (lane >= o) inc0 += v;
+      }
+      const int sum0 = __shfl_sync(0xffffffffu, inc0, 31);
+      int inc1 = c1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc1, o);
+        if (lane >= o) inc1 += v;
+      }
+      begin_lo = inc0 - c0;
+      begin_hi = sum0 + inc1 - c1;
+      __syncwarp();
+    } else {
+      // lower bound of source rank r's first pair index in the run
+      int64_t bound[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t key = (int64_t)(lane + 32 * h) * pairs_per_rank;
+        int a = lo, z = hi;
+        if (lane + 32 * h < R) {
+          while (a < z) {
+            const int mid = a + (z - a) / 2;
+            if ((int64_t)p.src_of_slot[mid] < key) a = mid + 1; else z = mid;
+          }
+        }
+        bound[h] = a - lo;
+      }
+      begin_lo = bound[0];
+      begin_hi = bound[1];
     }
-    const int64_t begin = bounds[0] < cap ? bounds[0] : cap;
-    const int64_t end = bounds[1] < cap ? bounds[1] : cap;
-    p.layout_range[i] = (begin << 32) | (end - begin);
-    if (src == 0) {
-      const int64_t c = (int64_t)hi0 - lo0;
-      p.recv_count[e] = (int32_t)(c < cap ? c : cap);
+    // begin of rank r + 1 (the run's length after the last rank)
+    const int64_t next_lo_shfl = __shfl_down_sync(0xffffffffu, begin_lo, 1);
+    const int64_t first_hi = __shfl_sync(0xffffffffu, begin_hi, 0);
+    const int64_t next_hi_shfl = __shfl_down_sync(0xffffffffu, begin_hi, 1);
+    for (int h = 0; h < 2; ++h) {
+      const int r = lane + 32 * h;
+      if (r >= R) continue;
+      const int64_t bg = h ? begin_hi : begin_lo;
+      int64_t nx;
+      if (r + 1 >= R) nx = len;
+      else if (h == 0) nx = lane == 31 ? first_hi : next_lo_shfl;
+      else nx = next_hi_shfl;
+      const int64_t b0 = bg < cap ? bg : cap;
+      const int64_t b1 = nx < cap ? nx : cap;
+      p.layout_range[(int64_t)e * R + r] = (b0 << 32) | (b1 - b0);
     }
+    if (lane == 0) p.recv_count[e] = (int32_t)(len < cap ? len : cap);
   }
 }
 
@@ -219,15 +298,19 @@ cudaError_t launch_ll_layout(const LlLayoutParams& p, cudaStream_t s) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  int64_t work = (int64_t)p.num_experts * p.capacity;
-  const int64_t pairs = (int64_t)p.num_tokens * p.topk;
-  if (pairs > work) work = pairs;
-  int64_t blocks = (work + 255) / 256;
-  if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-  if (blocks < 1) blocks = 1;
+  auto clamp = [&](int64_t blocks) {
+    const int64_t cap = (int64_t)sms * 2;
+    return (int)(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
+  };
+  LlGrid g;
+  g.pair_blocks = clamp(((int64_t)p.num_tokens * p.topk + kLlThreads - 1) / kLlThreads);
+  g.fill_blocks = clamp(((int64_t)p.num_experts * p.capacity + 4 * kLlThreads - 1) / (4 * kLlThreads));
+  g.range_blocks = clamp((p.num_experts + kLlThreads / 32 - 1) / (kLlThreads / 32));
   LlLayoutParams q = p;
-  void* args[] = {&q};
-  return launch_pdl((const void*)k_ll_layout, dim3((unsigned)blocks), dim3(256), 0, s, args);
+  void* args[] = {&q, &g};
+  return launch_pdl((const void*)k_ll_layout,
+                    dim3((unsigned)(g.pair_blocks + g.fill_blocks + g.range_blocks)), dim3(kLlThreads),
+                    0, s, args);
 }
 
 }  // namespace moe
