@@ -66,4 +66,29 @@ def test_reference_arm_prints_a_line(capsys):
     import json
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
-    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["cores"] == bench.host_cores()
+    assert line["cpu_baseline"]["value"] == line["value"]
+
+
+@pytest.mark.parametrize("name,tokens,parts", [("prefill", 4096, 32), ("decode", 1000, 7),
+                                               ("decode_ll", 5000, 16), ("prefill_bwd", 64, 4)])
+def test_oracle_chunks_are_whole_rank_multiples(name, tokens, parts):
+    spec = bench.workload_spec(name)
+    n, r = spec["num_tokens"], spec["num_ranks"]
+    chunks = bench.oracle_chunks(spec, tokens, parts)
+    sizes = {t1 - t0 for t0, t1 in chunks}
+    assert len(sizes) == 1 and all(s % r == 0 and 0 < s <= n for s in sizes)
+    assert all(0 <= t0 < t1 <= n for t0, t1 in chunks)
+    assert sum(t1 - t0 for t0, t1 in chunks) >= tokens
+
+
+def test_all_cores_baseline_runs_the_oracle_in_spawned_workers():
+    # two workers on a workload with a cheap oracle pass
+    spec = bench.workload_spec("tiny")
+    pool = bench.OraclePool(spec, 2)
+    try:
+        done = pool.run(bench.oracle_chunks(spec, 64, 4))
+    finally:
+        pool.close()
+    assert done == 64
