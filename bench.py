@@ -267,6 +267,8 @@ class Step:
             kind = moe.MOE_PAYLOAD_FP8_E4M3_B128 if spec["out_kind"] == "fp8" else moe.MOE_PAYLOAD_BF16
             self.desc = moe.MoeDesc(n, k, e, r, h, moe.MOE_PAYLOAD_BF16, kind)
         self.cdesc = moe.MoeDesc(n, k, e, r, h)
+        # the rank-grouped combine needs whole ranks of tokens
+        self.combine_mode = moe.MOE_COMBINE_TOPK_RANKS if n % r == 0 else moe.MOE_COMBINE_TOPK
         self.lay = moe.layout_outputs(self.desc, dev)
         self.ws = torch.empty(max(moe.moe_workspace_size(self.desc), 256), dtype=torch.uint8,
                               device=dev)
@@ -317,7 +319,7 @@ class Step:
                 self.cdesc, moe.MOE_COMBINE_TOPK_RANKS, self.y, self.ids, self.w,
                 self.lay["slot_of"], self.residual, self.gamma, 1e-6, self.out, self.residual_out)
         else:
-            self.combine = moe.prepare_combine(self.cdesc, moe.MOE_COMBINE_TOPK_RANKS, self.y,
+            self.combine = moe.prepare_combine(self.cdesc, self.combine_mode, self.y,
                                                self.ids, self.w, self.lay["slot_of"], self.out)
 
     def _setup_per_rank(self, spec, dev, seed):
@@ -466,7 +468,7 @@ class Step:
                 self.lay["slot_of"], self.residual, self.gamma, 1e-6, self.out,
                 self.residual_out, h))
         else:
-            calls.append(moe.prepare_combine(self.cdesc, moe.MOE_COMBINE_TOPK_RANKS, self.y,
+            calls.append(moe.prepare_combine(self.cdesc, self.combine_mode, self.y,
                                              self.ids, self.w, self.lay["slot_of"], self.out, h))
         return calls
 
@@ -562,12 +564,134 @@ def run_ag_slots(args, rank, world):
     }
 
 
+def _timed(fn, K, flush, flush_read, stream):
+    """Mean device time of fn over K calls (CUDA events at its ends, L2
+    flushed before each call), in microseconds."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev:
+        flush.zero_()
+        flush_read.sum()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+
+
+def run_decode_sweep(args, rank, world):
+    """The decode step at N = 1, 2, 4, ..., 256 tokens (raw NVFP4 payload,
+    top-8 of 256, R=8; the combine grouped by rank where N % R == 0): eager
+    step time and CUDA-graph replay time per N."""
+    import torch
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    K, W = min(args.steps, 100), args.warmup
+    clocks = ClockSampler(gpu_uuid())
+    rows, launches, total_ms, total_tokens = [], 0, 0.0, 0
+    for n in (1, 2, 4, 8, 16, 32, 64, 128, 256):
+        spec = workload_spec("decode")
+        spec["num_tokens"] = n
+        st = Step(spec, dev, seed=rank * 1000 + n)
+        for _ in range(W):
+            st.run()
+        eager = _timed(st.run, K, flush, flush_read, stream)
+        graph = measure_graph(st, K, flush, flush_read)
+        rows.append({"num_tokens": n, "eager_step_us": round(eager, 2),
+                     "graph_step_us": graph["step_us_median"],
+                     "graph_tokens_per_s": round(n / (graph["step_us_median"] / 1e6), 1)})
+        launches += st.launches_per_step * K
+        total_ms += eager * K / 1e3
+        total_tokens += n * K
+    clk = clocks.stop()
+    total_ms, value = whole_job(total_ms, total_tokens, world, dev)
+    last = rows[-1]
+    return {
+        "metric": METRIC, "value": round(last["num_tokens"] / (last["eager_step_us"] / 1e6), 1),
+        "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(last["eager_step_us"] / 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "raw bytes (NVFP4 payload), bf16 combine",
+        "data": "synthetic",
+        "config": {"workload": "decode sweep: N = 1..256 tokens, top-8 of 256 R=8, raw 3584 B + 448 B "
+                               "payload per token, BF16 combine H=7168 (value and ms_per_step at N=256)",
+                   "l2": "flushed before every timed step"},
+        "sweep": rows, "gpu_launches": launches, "clocks": clk,
+    }
+
+
+def run_rs_sweep(args, rank, world):
+    """The combine as a reduce-scatter, R=4 ranks, H=8192, 32..512 tokens per
+    rank (0.5..8 MiB of output per rank): (i) the cross-rank sum of R BF16
+    partials, (ii) the top-8 weighted reduction grouped by rank. Device time
+    per call."""
+    import torch
+    from combine_moe_layout_03_gb300 import moe, synth
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    K, W = min(args.steps, 100), args.warmup
+    peak = measured_peaks()["hbm_gbs"]
+    clocks = ClockSampler(gpu_uuid())
+    r, h, k, e = 4, 8192, 8, 256
+    rows, launches = [], 0
+    for t in (32, 64, 128, 256, 512):
+        c = synth.rs_case(seed=rank * 1000 + t, tokens_per_rank=t, hidden=h, r=r, e=e, k=k)
+        n = r * t
+        d = moe.MoeDesc(n, k, e, r, h)
+        part = torch.from_numpy(c["partials_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+        y = torch.from_numpy(c["expert_out_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+        ids = torch.from_numpy(c["topk_idx"]).to(dev)
+        w = torch.from_numpy(c["topk_weights"]).to(dev)
+        lay = moe.moe_layout(d, ids)
+        out = torch.empty((n, h), dtype=torch.bfloat16, device=dev)
+        ranks = moe.prepare_combine(d, moe.MOE_COMBINE_RANKS, part, None, None, None, out)
+        fused = moe.prepare_combine(d, moe.MOE_COMBINE_TOPK_RANKS, y, ids, w, lay["slot_of"], out)
+        for _ in range(W):
+            ranks()
+            fused()
+        us_r = _timed(ranks, K, flush, flush_read, stream)
+        us_f = _timed(fused, K, flush, flush_read, stream)
+        b_r = (r * n * h + n * h) * 2            # R partials in, the sum out
+        b_f = (k * n * h + n * h) * 2 + 12 * k * n  # k rows in, the sum out, pair info
+        rows.append({"tokens_per_rank": t, "out_mib_per_rank": t * h * 2 / 2 ** 20,
+                     "rank_sum_us": round(us_r, 2), "rank_sum_frac": round(b_r / us_r / 1e3 / peak, 3),
+                     "topk_ranks_us": round(us_f, 2), "topk_ranks_frac": round(b_f / us_f / 1e3 / peak, 3)})
+        launches += 2 * K
+    clk = clocks.stop()
+    last = rows[-1]
+    return {
+        "metric": METRIC, "value": round(r * last["tokens_per_rank"] / (last["topk_ranks_us"] / 1e6), 1),
+        "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(last["topk_ranks_us"] / 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, fp32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": "reduce-scatter sweep: R=4, H=8192, 32..512 tokens per rank; rank sum "
+                               "of BF16 partials and top-8 weighted reduction grouped by rank "
+                               "(value at 512 tokens per rank, grouped form)",
+                   "l2": "flushed before every timed call"},
+        "sweep": rows, "gpu_launches": launches, "clocks": clk,
+        "pages_context_us": {"0.5": [42.4, 35.6], "1": [43.1, 37.1], "2": [42.3, 37.4],
+                             "4": [51.6, 43.5], "8": [84.8, 76.7],
+                             "note": "NCCL symmetric reduce-scatter, staged and direct, 4 GPUs over "
+                                     "NVLink: a collective across GPUs, context only"},
+    }
+
+
 def run_ours(args, spec, rank, world):
     import torch
     import torch.distributed as dist
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    st = Step(spec, dev, seed=rank)
+    # S seeded input sets (routing, hidden rows, expert outputs); timed step i
+    # runs on set i % S
+    S = max(1, args.seeds)
+    sets = [Step(spec, dev, seed=rank * 1000 + j) for j in range(S)]
+    st = sets[0]
     stream = torch.cuda.current_stream()
     # L2 flush between steps: write a buffer larger than L2, then read another
     # one, so the written lines are evicted (and written back) before the
@@ -576,8 +700,8 @@ def run_ours(args, spec, rank, world):
     flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     K, W = args.steps, args.warmup
     clocks = ClockSampler(gpu_uuid())
-    for _ in range(W):
-        st.run()
+    for i in range(W):
+        sets[i % S].run()
     # The timed steps: events at the start and the end of each step only, so
     # that consecutive kernels may overlap their launch (programmatic
     # dependent launch) as they do in an application.
@@ -590,7 +714,7 @@ def run_ours(args, spec, rank, world):
         flush.zero_()                  # L2 flush, outside the timed events
         flush_read.sum()
         ev[i][0].record(stream)
-        st.run()
+        sets[i % S].run()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -605,12 +729,13 @@ def run_ours(args, spec, rank, world):
         flush.zero_()
         flush_read.sum()
         e = eb[i]
+        sx = sets[i % S]
         e[0].record(stream)
-        st.layout()
+        sx.layout()
         e[1].record(stream)
-        st.dispatch()
+        sx.dispatch()
         e[2].record(stream)
-        st.combine()
+        sx.combine()
         e[3].record(stream)
     torch.cuda.synchronize()
     per = {name: [eb[i][a].elapsed_time(eb[i][b]) for i in range(K)]
@@ -630,6 +755,7 @@ def run_ours(args, spec, rank, world):
     label = dict(zip(("layout", "dispatch", "combine"),
                      spec.get("names", ("layout", "dispatch", "combine"))))
 
+    per_seed = [statistics.mean(step_ms[i] for i in range(j, K, S)) * 1e3 for j in range(min(S, K))]
     graph = measure_graph(st, K, flush, flush_read)
     e2e = measure_e2e(st, spec, dev, K, W, seed=rank) if rank == 0 else None
     line = {
@@ -660,6 +786,8 @@ def run_ours(args, spec, rank, world):
         "kernels_frac": {label[name]: round(v / peaks["hbm_gbs"], 4) for name, v in achieved.items()},
         "step_gbs": round(step_bytes / (total_ms / K / 1e3) / 1e9, 1),
         "ms_per_step_serialised": round(serial_ms, 5),
+        "seeds": {"count": S, "step_us_per_seed": [round(x, 2) for x in per_seed],
+                  "step_us_median": round(statistics.median(per_seed), 2)},
         "gpu_launches": st.launches_per_step * K,
         "pdl": os.environ.get("MOE_PDL", "1") != "0",
         "graph": graph,
@@ -969,12 +1097,16 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill",
                     choices=["prefill", "decode", "rs", "skewed", "tiny", "prefill_norm",
-                             "prefill_ranks", "prefill_bwd", "decode_ll", "ag_slots"])
+                             "prefill_ranks", "prefill_bwd", "decode_ll", "ag_slots",
+                             "decode_sweep", "rs_sweep"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--seeds", type=int, default=5,
+                    help="seeded input sets the timed steps cycle through")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
-    spec = workload_spec(args.workload) if args.workload != "ag_slots" else None
+    special = {"ag_slots": run_ag_slots, "decode_sweep": run_decode_sweep, "rs_sweep": run_rs_sweep}
+    spec = workload_spec(args.workload) if args.workload not in special else None
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -991,7 +1123,7 @@ def main(argv=None):
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group("nccl")
-    line = run_ag_slots(args, rank, world) if spec is None else run_ours(args, spec, rank, world)
+    line = special[args.workload](args, rank, world) if spec is None else run_ours(args, spec, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
