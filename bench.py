@@ -19,6 +19,7 @@ cross-GPU exchange on one-GPU-per-rank hardware here.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -343,17 +344,10 @@ class Step:
         lw = rec[:, rl["off_weights"]:rl["off_weights"] + 4 * spec["topk"]].contiguous().view(torch.float32)
         self.y = (q.float() * sc.repeat_interleave(128, dim=1) * lw.sum(1, keepdim=True)).to(torch.bfloat16)
         self.recv_records = recv
-        lay_prep = moe.prepare_layout(self.desc, self.ids, self.lay, self.ws)
-        d, lay, rlay = self.desc, self.lay, self.rlay
-
-        def layout_both():
-            lay_prep()
-            moe.moe_rank_layout(d, lay, 1, rlay)
-        self.layout = layout_both
-        self.dispatch = lambda: moe.moe_dispatch_ranks(d, self.ids, self.w, self.x, self.sc,
-                                                       rlay["send_head"], self.records)
-        self.combine = lambda: moe.moe_combine_gather_ranks(self.cdesc, self.y, rlay["send_head"],
-                                                            self.out)
+        import torch
+        lp, rp, dp, cp = self._rank_calls_on(torch.cuda.current_stream())
+        self.layout = lambda: (lp(), rp())
+        self.dispatch, self.combine = dp, cp
         self.launches_per_step = layout_launches(n, spec["topk"], spec["num_experts"],
                                                  spec["num_ranks"]) + 1 + 1 + 1
         # algorithmic bytes per token from the actual (token, rank) records
@@ -438,6 +432,16 @@ class Step:
                 moe.prepare_combine(self.cdesc, moe.MOE_COMBINE_TOPK, self.y, self.ids, self.w,
                                     self.ll["ll_slot_of"], self.out, h)]
 
+    def _rank_calls_on(self, stream):
+        moe = self.moe
+        h = stream.cuda_stream
+        return [moe.prepare_layout(self.desc, self.ids, self.lay, self.ws, h),
+                moe.prepare_rank_layout(self.desc, self.lay, 1, self.rlay, h),
+                moe.prepare_dispatch_ranks(self.desc, self.ids, self.w, self.x, self.sc,
+                                           self.rlay["send_head"], self.records, h),
+                moe.prepare_combine_gather_ranks(self.cdesc, self.y, self.rlay["send_head"],
+                                                 self.out, h)]
+
     def run(self):
         self.layout()
         self.dispatch()
@@ -448,17 +452,7 @@ class Step:
         moe = self.moe
         h = stream.cuda_stream
         if self.spec.get("per_rank"):
-            lp = moe.prepare_layout(self.desc, self.ids, self.lay, self.ws, h)
-            d, lay, rlay = self.desc, self.lay, self.rlay
-
-            def layout():
-                lp()
-                moe.moe_rank_layout(d, lay, 1, rlay, h)
-            return [layout,
-                    lambda: moe.moe_dispatch_ranks(d, self.ids, self.w, self.x, self.sc,
-                                                   rlay["send_head"], self.records, h),
-                    lambda: moe.moe_combine_gather_ranks(self.cdesc, self.y, rlay["send_head"],
-                                                         self.out, h)]
+            return self._rank_calls_on(stream)
         calls = [moe.prepare_layout(self.desc, self.ids, self.lay, self.ws, h),
                  moe.prepare_dispatch(self.desc, self.ids, self.w, self.x, self.sc,
                                       self.lay["slot_of"], self.records, h)]
@@ -1123,7 +1117,15 @@ def main(argv=None):
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group("nccl")
-    line = special[args.workload](args, rank, world) if spec is None else run_ours(args, spec, rank, world)
+    # No garbage-collector pass may stall the host while it enqueues timed work
+    # (a stalled host leaves the GPU idle inside a step).
+    gc.collect()
+    gc.disable()
+    try:
+        line = special[args.workload](args, rank, world) if spec is None else \
+            run_ours(args, spec, rank, world)
+    finally:
+        gc.enable()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -556,6 +556,36 @@ def prepare_dispatch_ll(desc: MoeDesc, hidden, scales, ll_slot_of, x_out, scales
     return Prepared("moe_dispatch_ll", args, (d, hidden, scales, ll_slot_of, x_out, scales_out))
 
 
+def prepare_rank_layout(desc: MoeDesc, lay: dict, expert_alignment: int, out: dict,
+                        stream=None) -> Prepared:
+    d = desc.c()
+    args = (ctypes.byref(d), *_vps(lay["is_token_in_rank"], lay["tokens_per_rank"],
+                                   lay["tokens_per_expert"]),
+            ctypes.c_int32(expert_alignment),
+            *_vps(out["send_head"], out.get("recv_src_idx"), out["recv_offset"],
+                  out["recv_tokens_per_expert"]),
+            ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_rank_layout", args, (d, lay, out))
+
+
+def prepare_dispatch_ranks(desc: MoeDesc, topk_idx, topk_weights, hidden, scales, send_head,
+                           records, stream=None) -> Prepared:
+    d = desc.c()
+    args = (ctypes.byref(d), *_vps(topk_idx, topk_weights, hidden, scales, send_head, records),
+            ctypes.c_size_t(records.numel() * records.element_size()),
+            ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_dispatch_ranks", args, (d, topk_idx, topk_weights, hidden, scales,
+                                                 send_head, records))
+
+
+def prepare_combine_gather_ranks(desc: MoeDesc, recv_out, send_head, out, stream=None) -> Prepared:
+    d = desc.c()
+    rows = recv_out.numel() // max(desc.hidden, 1)
+    args = (ctypes.byref(d), ctypes.c_void_p(_ptr(recv_out)), ctypes.c_int64(rows),
+            *_vps(send_head, out), ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_combine_gather_ranks", args, (d, recv_out, send_head, out))
+
+
 def prepare_combine(desc: MoeDesc, mode: int, expert_out, topk_idx, topk_weights, slot_of, out,
                     stream=None) -> Prepared:
     d = desc.c()

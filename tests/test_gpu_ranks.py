@@ -108,3 +108,26 @@ def test_combine_gather_ranks(n, r, h):
     ref = oracle.combine_gather_ranks(y, orl["send_head"], h)
     assert_combine_close(got, ref, "gather ranks")
     np.testing.assert_array_equal(got, ref)
+
+
+def test_prepared_rank_calls_match_direct_calls():
+    from combine_moe_layout_03_gb300 import moe
+    c = synth.prefill_case(seed=5, n=256, hidden=1024)
+    ids, w, x = dev_i32(c["topk_idx"]), dev_f32(c["topk_weights"]), dev_bf16(c["hidden_bf16"])
+    d = moe.MoeDesc(256, 8, 256, 8, 1024, moe.MOE_PAYLOAD_BF16, moe.MOE_PAYLOAD_FP8_E4M3_B128)
+    lay = moe.moe_layout(d, ids)
+    direct = moe.moe_rank_layout(d, lay, 4)
+    rec_direct = moe.moe_dispatch_ranks(d, ids, w, x, None, direct["send_head"])
+    y = dev_bf16(synth.bf16_normal(np.random.default_rng(6), (256 * 8, 1024)))
+    out_direct = moe.moe_combine_gather_ranks(moe.MoeDesc(256, 8, 256, 8, 1024), y, direct["send_head"])
+    prep = {key: torch.full_like(v, -7) for key, v in direct.items()}
+    rec = torch.zeros_like(rec_direct)
+    out = torch.zeros_like(out_direct)
+    moe.prepare_rank_layout(d, lay, 4, prep)()
+    moe.prepare_dispatch_ranks(d, ids, w, x, None, prep["send_head"], rec)()
+    moe.prepare_combine_gather_ranks(moe.MoeDesc(256, 8, 256, 8, 1024), y, prep["send_head"], out)()
+    torch.cuda.synchronize()
+    for key in direct:
+        assert torch.equal(prep[key], direct[key]), key
+    recv = int(direct["recv_offset"][-1])  # rows past the received ones are not written
+    assert torch.equal(rec[:recv], rec_direct[:recv]) and torch.equal(out, out_direct)
