@@ -120,19 +120,28 @@ __global__ void __launch_bounds__(kGatherBwdThreads) k_gather_ranks_backward(Ran
   pdl_wait();
   pdl_trigger();
   __shared__ int s_slot[MOE_MAX_RANKS];
-  __shared__ int s_n;
+  __shared__ int s_cnt[2];
   const int t = blockIdx.x;
   const int R = p.num_ranks;
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int r = 0; r < R; ++r) {
-      const int s = p.send_head[(int64_t)t * R + r];
-      if (s >= 0 && (int64_t)s < p.rows) s_slot[n++] = s;
-    }
-    s_n = n;
+  // lanes of warps 0 and 1 load send_head[t, r] together; the valid slots are
+  // compacted by ballot
+  int s = -1;
+  bool ok = false;
+  unsigned m = 0;
+  if (threadIdx.x < 64) {
+    const int r = threadIdx.x;
+    s = r < R ? p.send_head[(int64_t)t * R + r] : -1;
+    ok = s >= 0 && (int64_t)s < p.rows;
+    m = __ballot_sync(0xffffffffu, ok);
+    if ((r & 31) == 0) s_cnt[r >> 5] = __popc(m);
   }
   __syncthreads();
-  const int n = s_n;
+  if (threadIdx.x < 64 && ok) {
+    const int r = threadIdx.x;
+    s_slot[__popc(m & ((1u << (r & 31)) - 1u)) + (r >= 32 ? s_cnt[0] : 0)] = s;
+  }
+  __syncthreads();
+  const int n = s_cnt[0] + s_cnt[1];
   const int chunks = p.hidden_size / 8;
   const size_t row_bytes = (size_t)p.hidden_size * 2;
   for (int c = threadIdx.x; c < chunks; c += kGatherBwdThreads) {

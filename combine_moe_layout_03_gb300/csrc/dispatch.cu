@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
   extern __shared__ __align__(128) uint8_t img[];  // record bytes [off_payload, record_bytes)
   __shared__ int s_ids[MOE_MAX_TOPK];
   __shared__ uint32_t s_w[MOE_MAX_TOPK];
+  __shared__ int s_head[MOE_MAX_RANKS];
   const int t = blockIdx.x;
   const int k = p.topk;
   const int tail = p.record_bytes - p.off_payload;
@@ -215,6 +216,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
     s_ids[threadIdx.x] = p.topk_idx[q];
     s_w[threadIdx.x] = __float_as_uint(p.topk_weights[q]);
   }
+  // the token's receive slots, loaded while the row is in flight
+  if (threadIdx.x < num_ranks) s_head[threadIdx.x] = send_head[(int64_t)t * num_ranks + threadIdx.x];
   zero_bytes(img, p.payload_bytes, os);
   zero_bytes(img, os + p.scale_bytes, tail);
   cp_async_wait_all();
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
 
   if (threadIdx.x < num_ranks) {
     const int r = threadIdx.x;
-    const int s = send_head[(int64_t)t * num_ranks + r];
+    const int s = s_head[r];
     if (s >= 0 && (int64_t)s < p.record_capacity) {
       const int lo = r * experts_per_rank, hi = lo + experts_per_rank;
       int nlocal = 0;

@@ -78,53 +78,84 @@ __global__ void __launch_bounds__(kRankLayoutThreads) k_rank_layout(RankLayoutPa
   }
 }
 
+// acc[i] += float(bf16 element i of v), in fp32 round-to-nearest
+__device__ __forceinline__ void add8(float* acc, uint4 v) {
+  acc[0] = __fadd_rn(acc[0], bf16_lo(v.x));
+  acc[1] = __fadd_rn(acc[1], bf16_hi(v.x));
+  acc[2] = __fadd_rn(acc[2], bf16_lo(v.y));
+  acc[3] = __fadd_rn(acc[3], bf16_hi(v.y));
+  acc[4] = __fadd_rn(acc[4], bf16_lo(v.z));
+  acc[5] = __fadd_rn(acc[5], bf16_hi(v.z));
+  acc[6] = __fadd_rn(acc[6], bf16_lo(v.w));
+  acc[7] = __fadd_rn(acc[7], bf16_hi(v.w));
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* a) {
+  uint4 o;
+  o.x = pack_bf16x2_rn(a[0], a[1]);
+  o.y = pack_bf16x2_rn(a[2], a[3]);
+  o.z = pack_bf16x2_rn(a[4], a[5]);
+  o.w = pack_bf16x2_rn(a[6], a[7]);
+  return o;
+}
+
 __global__ void __launch_bounds__(kRankCombineThreads) k_combine_gather_ranks(RankCombineParams p) {
   pdl_wait();
   pdl_trigger();
   __shared__ int s_slot[MOE_MAX_RANKS];
-  __shared__ int s_n;
+  __shared__ int s_cnt[2];
   const int t = blockIdx.x;
   const int R = p.num_ranks;
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int r = 0; r < R; ++r) {
-      const int s = p.send_head[(int64_t)t * R + r];
-      if (s >= 0 && (int64_t)s < p.rows) s_slot[n++] = s;
-    }
-    s_n = n;
+  // warps 0 and 1: lane r loads send_head[t, r] (all loads in flight at once);
+  // the valid slots are compacted in ascending r, the summation order
+  int s = -1;
+  bool ok = false;
+  unsigned m = 0;
+  if (threadIdx.x < 64) {
+    const int r = threadIdx.x;
+    s = r < R ? p.send_head[(int64_t)t * R + r] : -1;
+    ok = s >= 0 && (int64_t)s < p.rows;
+    m = __ballot_sync(0xffffffffu, ok);
+    if ((r & 31) == 0) s_cnt[r >> 5] = __popc(m);
   }
   __syncthreads();
-  const int n = s_n;
+  if (threadIdx.x < 64 && ok) {
+    const int r = threadIdx.x;
+    const int before = __popc(m & ((1u << (r & 31)) - 1u)) + (r >= 32 ? s_cnt[0] : 0);
+    s_slot[before] = s;
+  }
+  __syncthreads();
+  const int n = s_cnt[0] + s_cnt[1];
   const int chunks = p.hidden_size / 8;
   const size_t row_bytes = (size_t)p.hidden_size * 2;
-  for (int c = threadIdx.x; c < chunks; c += kRankCombineThreads) {
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    const uint8_t* col = p.recv_out + (size_t)c * 16;
-    for (int m0 = 0; m0 < n; m0 += 8) {
-      uint4 v[8];
+  // two column chunks per thread and step, four rank rows per batch: eight
+  // 16-byte loads in flight (a token reaches about half as many ranks as it
+  // has pairs, so one chunk alone would leave the loads half as deep)
+  for (int c0 = threadIdx.x; c0 < chunks; c0 += 2 * kRankCombineThreads) {
+    const int c1 = c0 + kRankCombineThreads;
+    const bool on1 = c1 < chunks;
+    float acc0[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    float acc1[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int m0 = 0; m0 < n; m0 += 4) {
+      uint4 v0[4], v1[4];
 #pragma unroll
-      for (int b = 0; b < 8; ++b)
-        if (m0 + b < n) v[b] = ld_stream_v4(col + (size_t)s_slot[m0 + b] * row_bytes);
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
+      for (int b = 0; b < 4; ++b) {
         if (m0 + b < n) {
-          acc[0] = __fadd_rn(acc[0], bf16_lo(v[b].x));
-          acc[1] = __fadd_rn(acc[1], bf16_hi(v[b].x));
-          acc[2] = __fadd_rn(acc[2], bf16_lo(v[b].y));
-          acc[3] = __fadd_rn(acc[3], bf16_hi(v[b].y));
-          acc[4] = __fadd_rn(acc[4], bf16_lo(v[b].z));
-          acc[5] = __fadd_rn(acc[5], bf16_hi(v[b].z));
-          acc[6] = __fadd_rn(acc[6], bf16_lo(v[b].w));
-          acc[7] = __fadd_rn(acc[7], bf16_hi(v[b].w));
+          const uint8_t* rowp = p.recv_out + (size_t)s_slot[m0 + b] * row_bytes;
+          v0[b] = ld_stream_v4(rowp + (size_t)c0 * 16);
+          if (on1) v1[b] = ld_stream_v4(rowp + (size_t)c1 * 16);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        if (m0 + b < n) {
+          add8(acc0, v0[b]);
+          if (on1) add8(acc1, v1[b]);
         }
       }
     }
-    uint4 o;
-    o.x = pack_bf16x2_rn(acc[0], acc[1]);
-    o.y = pack_bf16x2_rn(acc[2], acc[3]);
-    o.z = pack_bf16x2_rn(acc[4], acc[5]);
-    o.w = pack_bf16x2_rn(acc[6], acc[7]);
-    st_v4(p.out + (size_t)t * row_bytes + (size_t)c * 16, o);
+    st_v4(p.out + (size_t)t * row_bytes + (size_t)c0 * 16, pack8_bf16(acc0));
+    if (on1) st_v4(p.out + (size_t)t * row_bytes + (size_t)c1 * 16, pack8_bf16(acc1));
   }
 }
 
