@@ -209,22 +209,23 @@ def measured_peaks() -> dict:
 
 def recorded_traffic(kernel: str, workload: str) -> int | None:
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's source changed since the counters were taken."""
+    kernel's source file changed since the counters were taken (each line
+    names the .cu file and its hash at capture time)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = {"combine": "combine.cu", "dispatch": "dispatch.cu", "layout": "layout.cu",
-           "combine_backward": "backward.cu", "dispatch_backward": "combine.cu"}.get(kernel)
-    if src is None:
-        return None
-    with open(os.path.join(ROOT, "combine_moe_layout_03_gb300", "csrc", src), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
     for line in open(path):
         if line.startswith("#") or "=" not in line:
             continue
         kv = dict(x.split("=", 1) for x in line.split())
-        if kv.get("kernel") == kernel and kv.get("workload") == workload:
-            return int(kv["bytes_per_launch"]) if kv.get("source_sha256") == sha else None
+        if kv.get("kernel") != kernel or kv.get("workload") != workload:
+            continue
+        src = os.path.join(ROOT, "combine_moe_layout_03_gb300", "csrc", kv.get("source", ""))
+        if not kv.get("source") or not os.path.exists(src):
+            return None
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        return int(kv["bytes_per_launch"]) if kv.get("source_sha256") == sha else None
     return None
 
 
