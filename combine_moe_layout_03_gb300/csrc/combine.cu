@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 3)
 // are enough tokens to fill the GPU.
 constexpr int kRowThreads = 256;
 
-template <bool GROUP>
-__global__ void __launch_bounds__(kRowThreads) k_combine_rows(CombineParams p) {
+template <bool GROUP, int THREADS = kRowThreads>
+__global__ void __launch_bounds__(THREADS) k_combine_rows(CombineParams p) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kRowThreads) k_combine_rows(CombineParams p) {
     if (GROUP) idx = p.topk_idx[qq];
   }
   const PairList pl = order_pairs<GROUP>(slot, w, idx, k, p.expert_out_rows, p.experts_per_rank);
-  for (int cb = 0; cb < chunks; cb += kRowThreads) {  // uniform trip count per warp
+  for (int cb = 0; cb < chunks; cb += THREADS) {  // uniform trip count per warp
     const int c = cb + (int)threadIdx.x;
     const bool on = c < chunks;
     float res[8];
@@ -414,11 +414,17 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   // One block per row from about three rows per SM up; below that the
   // persistent warp kernel, with units of two 32-chunk steps (one pair
   // ordering per 64 chunks), keeps every SM busy.
+  // The rank-grouped form keeps two fp32 accumulators per element: its
+  // 128-thread blocks (twice as many per SM) measured 5% faster at N=4096
+  // and 11% at N=1024 than 256-thread ones; the plain form keeps 256.
   if (p.num_tokens >= di->sms * 3) {
     CombineParams q = p;
     void* args[] = {&q};
-    const void* fn = p.group_by_rank ? (const void*)k_combine_rows<true> : (const void*)k_combine_rows<false>;
-    return launch_pdl(fn, dim3((unsigned)p.num_tokens), dim3(kRowThreads), 0, s, args);
+    if (p.group_by_rank)
+      return launch_pdl((const void*)k_combine_rows<true, 128>, dim3((unsigned)p.num_tokens), dim3(128), 0,
+                        s, args);
+    return launch_pdl((const void*)k_combine_rows<false>, dim3((unsigned)p.num_tokens), dim3(kRowThreads),
+                      0, s, args);
   }
   const int chunks = p.hidden_size / 8;
   const int steps_per_token = (chunks + 31) / 32;  // warp steps of 32 chunks
