@@ -82,6 +82,13 @@ __device__ void count_tokens(const LayoutParams& p, int t0, int t1, const int* s
                              const int* rank_of, int* cnt, int* rcnt) {
   const int k = p.topk, R = p.num_ranks;
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  // a token's ids as 16-byte vectors when they are aligned (4 ids a load, a
+  // quarter of the bank conflicts of scalar reads at stride k), and its rank
+  // by a shift when experts per rank is a power of two
+  const bool vec = (k & 3) == 0 && (((uintptr_t)sids) & 15) == 0;
+  const int epr = p.experts_per_rank;
+  const bool pow2 = (epr & (epr - 1)) == 0;
+  const int sh = 31 - __clz(epr);
   for (int tb = t0 + warp * 32; tb < t1; tb += nwarps * 32) {
     const int t = tb + (int)lane_id();
     uint64_t mask = 0;
@@ -89,13 +96,20 @@ __device__ void count_tokens(const LayoutParams& p, int t0, int t1, const int* s
       const int* row_ids = sids + (t - t0) * k;
       for (int j0 = 0; j0 < k; j0 += 8) {  // 8 independent reads at a time
         int ev[8];
+        if (vec) {
+          const int4 a = reinterpret_cast<const int4*>(row_ids + j0)[0];
+          const int4 b = j0 + 4 < k ? reinterpret_cast<const int4*>(row_ids + j0)[1] : make_int4(-1, -1, -1, -1);
+          ev[0] = a.x; ev[1] = a.y; ev[2] = a.z; ev[3] = a.w;
+          ev[4] = b.x; ev[5] = b.y; ev[6] = b.z; ev[7] = b.w;
+        } else {
 #pragma unroll
-        for (int b = 0; b < 8; ++b) ev[b] = (j0 + b < k) ? row_ids[j0 + b] : -1;
+          for (int b = 0; b < 8; ++b) ev[b] = (j0 + b < k) ? row_ids[j0 + b] : -1;
+        }
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
           if (ev[b] >= 0) {
             if (COUNT_EXPERTS) atomicAdd(&cnt[ev[b]], 1);
-            mask |= 1ull << rank_of[ev[b]];
+            mask |= 1ull << (pow2 ? (ev[b] >> sh) : rank_of[ev[b]]);
           }
         }
       }
@@ -131,7 +145,7 @@ __device__ __forceinline__ int key_bits(int E) { return 32 - __clz(E); }
 // replaces each staged id by (rank of the pair among the run's pairs of the
 // same expert, in order) << 11 | (id + 1). Every thread of the block must
 // call it; ends with a barrier.
-__device__ void warp_histograms(int E, int len, int* sids, int* whist) {
+__device__ void warp_histograms(int E, int len, int* sids, int* whist, bool zero = true) {
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const unsigned lane = lane_id();
   const unsigned lt = (1u << lane) - 1u;
@@ -141,8 +155,10 @@ __device__ void warp_histograms(int E, int len, int* sids, int* whist) {
   const int nb = key_bits(E);
   const int none = (1 << nb) - 1;
   int* wh = whist + warp * E;
-  for (int e = threadIdx.x; e < nwarps * E; e += blockDim.x) whist[e] = 0;
-  __syncthreads();
+  if (zero) {
+    for (int e = threadIdx.x; e < nwarps * E; e += blockDim.x) whist[e] = 0;
+    __syncthreads();
+  }
   constexpr int S = 4;  // steps of 32 pairs whose masks are built together
   for (int qb = w0; qb < w1; qb += 32 * S) {
     int e[S], key[S];
@@ -232,14 +248,14 @@ __device__ void clear_src_tail(const LayoutParams& p, int64_t P) {
 __global__ void __launch_bounds__(kCountThreads) k_layout_count(LayoutParams p) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ int smem[];
+  extern __shared__ __align__(16) int smem[];
   const int E = p.num_experts, R = p.num_ranks;
-  int* cnt = smem;
-  int* rcnt = smem + E;
+  int* sids = smem;                              // [tokens_per_chunk * k], 16-byte aligned
+  int* cnt = sids + p.tokens_per_chunk * p.topk;  // [E]
+  int* rcnt = cnt + E;
   int* flag = rcnt + R;
   int* rank_of = flag + 1;  // [E]
-  int* sids = rank_of + E;  // [tokens_per_chunk * k]
-  for (int i = threadIdx.x; i < E + R + 1; i += blockDim.x) smem[i] = 0;
+  for (int i = threadIdx.x; i < E + R + 1; i += blockDim.x) cnt[i] = 0;
   fill_rank_of(p, rank_of);
   const int c = blockIdx.x;
   const int t0 = c * p.tokens_per_chunk;
@@ -357,31 +373,32 @@ __global__ void __launch_bounds__(kClusterThreads) k_layout_cluster(LayoutParams
   pdl_trigger();
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
-  extern __shared__ int smem[];
+  extern __shared__ __align__(16) int smem[];
   constexpr int NW = kClusterThreads / 32;
   const int E = p.num_experts, R = p.num_ranks, k = p.topk;
   const int G = (int)cluster.num_blocks();
   const int c = (int)cluster.block_rank();
-  int* scratch = smem;          // 33 (+3 pad)
-  int* cnt = smem + 36;         // [E] this block's expert counts
+  int* sids = smem;                          // [tokens_per_block * k] (a multiple of 4: aligned)
+  int* scratch = sids + tokens_per_block * k;  // 33 (+3 pad)
+  int* cnt = scratch + 36;      // [E] this block's expert counts
   int* rcnt = cnt + E;          // [R] this block's token-in-rank counts
   int* flag = rcnt + R;         // [1] invalid ids seen
   int* base = flag + 1;         // [E]
   int* rank_of = base + E;      // [E]
   int* whist = rank_of + E;     // [NW][E]
-  int* sids = whist + NW * E;   // [tokens_per_block * k]
   const int t0 = min(c * tokens_per_block, p.num_tokens);
   const int t1 = min(t0 + tokens_per_block, p.num_tokens);
   const int64_t p0 = (int64_t)t0 * k;
   const int len = (t1 - t0) * k;
 
   for (int i = threadIdx.x; i < E + R + 1; i += blockDim.x) cnt[i] = 0;
+  for (int i = threadIdx.x; i < NW * E; i += blockDim.x) whist[i] = 0;
   fill_rank_of(p, rank_of);
   __syncthreads();
   stage_ids(p, p0, p0 + len, sids, flag);
   __syncthreads();
   count_tokens<false>(p, t0, t1, sids, rank_of, cnt, rcnt);
-  warp_histograms(E, len, sids, whist);  // starts and ends with a barrier
+  warp_histograms(E, len, sids, whist, false);  // whist zeroed above; ends with a barrier
   for (int e = threadIdx.x; e < E; e += blockDim.x) {  // the block's expert counts
     int v[NW];
 #pragma unroll
