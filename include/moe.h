@@ -24,6 +24,12 @@
  *                 "Eliminate staging from NCCL symmetric reduce-scatter",
  *                 Implementation).
  *
+ * Further groups below: the fused combine + residual + RMSNorm; the
+ * per-(token, rank) layout, dispatch and gathered combine of DeepEP's normal
+ * kernels; the fixed-capacity, expert-major buffers of its low-latency
+ * kernels; the backward of combine and dispatch; the decode all-gather's
+ * rank-slot packing and padded-token mask; an allocation-free layout.
+ *
  * Conventions
  *  - Every function returns an int status: MOE_OK (0) or a negative MOE_ERR_*
  *    code; moe_strerror() names it. Nothing throws, aborts or traps. Argument
@@ -34,6 +40,12 @@
  *    says so). Work is enqueued on the caller's stream.
  *  - moe_stream_t is a cudaStream_t passed as void*; NULL is the legacy
  *    default stream.
+ *  - Kernels are launched with programmatic dependent launch: each one waits
+ *    (griddepcontrol.wait) for the previous kernel in the stream to complete
+ *    and its memory to be visible before it touches global memory, so it may
+ *    become resident early and hide the launch gap, whatever ran before it.
+ *    The environment variable MOE_PDL=0, read once per process, launches in
+ *    plain stream order instead.
  *  - Integers in records are little-endian.
  */
 #ifndef MOE_H
