@@ -26,6 +26,8 @@
 // expert row is read exactly once) and runs the fp32 fma chain in the fixed
 // order. The next unit's pair info is fetched while the current unit
 // streams, so its latency is hidden.
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -381,29 +383,31 @@ __global__ void __launch_bounds__(256) k_combine_ranks(const uint8_t* partials, 
 
 namespace {
 
-// SM count and resident blocks of each kernel, looked up once per device.
+// SM count and resident blocks of each kernel, looked up once per device
+// (std::call_once: safe when several host threads launch at once).
 struct DeviceInfo {
   int sms = 0;
   int topk_blocks[2] = {0, 0};
 };
 DeviceInfo g_info[64];
+std::once_flag g_info_once[64];
 
 const DeviceInfo* device_info() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  int dev = 0, sms = 0;
+  if (!current_device(&dev, &sms) || dev >= 64) return nullptr;
   DeviceInfo& d = g_info[dev];
-  if (d.sms == 0) {
-    int sms = 0, b0 = 0, b1 = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_combine_topk<false>, kCombineWarps * 32, 0) != cudaSuccess)
-      return nullptr;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_combine_topk<true>, kCombineWarps * 32, 0) != cudaSuccess)
-      return nullptr;
+  std::call_once(g_info_once[dev], [&d, sms] {
+    int b0 = 0, b1 = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_combine_topk<false>, kCombineWarps * 32, 0) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_combine_topk<true>, kCombineWarps * 32, 0) != cudaSuccess) {
+      cudaGetLastError();
+      b0 = b1 = 1;
+    }
     d.topk_blocks[0] = b0 > 0 ? b0 : 1;
     d.topk_blocks[1] = b1 > 0 ? b1 : 1;
     d.sms = sms;
-  }
-  return &d;
+  });
+  return d.sms > 0 ? &d : nullptr;
 }
 
 }  // namespace
@@ -465,10 +469,8 @@ cudaError_t launch_combine_norm(const CombineNormParams& p, cudaStream_t s) {
   const void* fn = p.mode == MOE_COMBINE_TOPK    ? (const void*)k_combine_norm<MOE_COMBINE_TOPK>
                    : p.mode == MOE_COMBINE_RANKS ? (const void*)k_combine_norm<MOE_COMBINE_RANKS>
                                                  : (const void*)k_combine_norm<MOE_COMBINE_TOPK_RANKS>;
-  if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
+  cudaError_t err = ensure_dynamic_smem(fn, smem);
+  if (err != cudaSuccess) return err;
   CombineNormParams q = p;
   void* args[] = {&q};
   return launch_pdl(fn, dim3((unsigned)p.c.num_tokens), dim3(kNormThreads), smem, s, args);

@@ -331,10 +331,8 @@ cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, 
     case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_dispatch<MOE_PAYLOAD_NVFP4_B16>; break;
     default: fn = (const void*)k_dispatch<MOE_PAYLOAD_RAW>; break;
   }
-  if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
+  cudaError_t err = ensure_dynamic_smem(fn, smem);
+  if (err != cudaSuccess) return err;
   DispatchParams q = p;
   void* args[] = {&q};
   return launch_pdl(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), smem, s, args);
@@ -351,10 +349,8 @@ cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const i
     case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_NVFP4_B16>; break;
     default: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_RAW>; break;
   }
-  if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
+  cudaError_t err = ensure_dynamic_smem(fn, smem);
+  if (err != cudaSuccess) return err;
   DispatchParams q = p;
   const int32_t* sh = send_head;
   int nr = num_ranks, epr = experts_per_rank;
@@ -373,10 +369,8 @@ cudaError_t launch_dispatch_packed(const DispatchParams& p, int out_kind, uint8_
     case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_NVFP4_B16>; break;
     default: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_RAW>; break;
   }
-  if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
+  cudaError_t err = ensure_dynamic_smem(fn, smem);
+  if (err != cudaSuccess) return err;
   DispatchParams q = p;
   uint8_t* xo = x_out;
   uint8_t* so = scales_out;

@@ -26,6 +26,8 @@
 // Ids outside [-1, E) count as -1 and raise the status word.
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -485,10 +487,7 @@ size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks) {
   return (b + 255) / 256 * 256;
 }
 
-static cudaError_t set_smem(const void* fn, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
+static cudaError_t set_smem(const void* fn, size_t bytes) { return ensure_dynamic_smem(fn, bytes); }
 
 // Cluster plan for a shape: blocks G and tokens per block. Up to 16 blocks
 // where the device schedules a non-portable cluster of 16 (looked up once per
@@ -498,16 +497,17 @@ struct ClusterPlan {
   size_t smem;
 };
 
+static int g_cluster_blocks[64];
+static std::once_flag g_cluster_once[64];
+
 static int max_cluster_blocks() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kClusterPortableBlocks;
-  if (cached[dev] == 0) {
+  int dev = 0, sms = 0;
+  if (!current_device(&dev, &sms) || dev >= 64) return kClusterPortableBlocks;
+  std::call_once(g_cluster_once[dev], [dev] {
     int best = kClusterPortableBlocks;
     if (cudaFuncSetAttribute((const void*)k_layout_cluster,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-        cudaFuncSetAttribute((const void*)k_layout_cluster,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterMaxSmem) == cudaSuccess) {
+        ensure_dynamic_smem((const void*)k_layout_cluster, kClusterMaxSmem) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(kClusterMaxBlocks);
       cfg.blockDim = dim3(kClusterThreads);
@@ -524,9 +524,9 @@ static int max_cluster_blocks() {
         best = kClusterMaxBlocks;
     }
     cudaGetLastError();
-    cached[dev] = best;
-  }
-  return cached[dev];
+    g_cluster_blocks[dev] = best;
+  });
+  return g_cluster_blocks[dev];
 }
 
 static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int num_ranks, int gmax) {

@@ -5,6 +5,9 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
+#include <vector>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -15,6 +18,57 @@ bool pdl_enabled() {
     return !(v && v[0] == '0' && v[1] == '\0');
   }();
   return on;
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::once_flag g_sm_once[kMaxDevices];
+int g_sm_count[kMaxDevices];
+std::mutex g_smem_mutex;
+struct SmemLimit {
+  const void* fn;
+  int dev;
+  size_t bytes;
+};
+std::vector<SmemLimit> g_smem_limits;
+}  // namespace
+
+bool current_device(int* dev, int* sms) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) {
+    cudaGetLastError();
+    return false;
+  }
+  std::call_once(g_sm_once[d], [d] {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    g_sm_count[d] = n;
+  });
+  if (g_sm_count[d] <= 0) return false;
+  *dev = d;
+  *sms = g_sm_count[d];
+  return true;
+}
+
+cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  std::lock_guard<std::mutex> lock(g_smem_mutex);
+  for (SmemLimit& l : g_smem_limits) {
+    if (l.fn == fn && l.dev == dev) {
+      if (l.bytes >= bytes) return cudaSuccess;
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+      if (e == cudaSuccess) l.bytes = bytes;
+      return e;
+    }
+  }
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) g_smem_limits.push_back({fn, dev, bytes});
+  return e;
 }
 
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,

@@ -133,6 +133,15 @@ __device__ __forceinline__ void pdl_trigger() {
 
 bool pdl_enabled();
 
+// The current device's index and SM count, looked up once per device
+// (thread-safe); false if the device cannot be queried.
+bool current_device(int* dev, int* sms);
+
+// Raises fn's dynamic shared memory limit to at least `bytes` on the current
+// device; the attribute is set only when a launch needs more than before
+// (thread-safe).
+cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
+
 // cudaLaunchKernelExC with the programmatic-serialization attribute (when
 // enabled) and an optional cluster size (cluster_x > 0).
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,

@@ -327,8 +327,7 @@ __global__ void __launch_bounds__(kLlThreads) k_ll_layout(LlLayoutParams p, LlGr
 
 cudaError_t launch_ll_layout(const LlLayoutParams& p, cudaStream_t s) {
   int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (!current_device(&dev, &sms)) sms = 148;
   auto clamp = [&](int64_t blocks) {
     const int64_t cap = (int64_t)sms * 2;
     return (int)(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));

@@ -64,8 +64,7 @@ __global__ void k_mask_topk_ids(int32_t* ids, int64_t total, int topk, const int
 
 int blocks_for(int64_t work, int threads) {
   int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (!current_device(&dev, &sms)) sms = 148;
   int64_t b = (work + threads - 1) / threads;
   const int64_t cap = (int64_t)sms * 8;
   if (b > cap) b = cap;
