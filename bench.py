@@ -310,6 +310,10 @@ class Step:
         self.layout = moe.prepare_layout(self.desc, self.ids, self.lay, self.ws)
         self.dispatch = moe.prepare_dispatch(self.desc, self.ids, self.w, self.x, self.sc,
                                              self.lay["slot_of"], self.records)
+        # the step itself runs layout and dispatch as one call, whose dispatch
+        # overlaps the layout (the breakdown loop times the two separately)
+        self.layout_dispatch = moe.prepare_layout_dispatch(self.desc, self.ids, self.w, self.x, self.sc,
+                                                           self.lay, self.ws, self.records)
         if spec.get("norm"):
             from combine_moe_layout_03_gb300 import synth
             self.residual = torch.from_numpy(synth.bf16_normal(synth.rng_for(seed, 12), (n, h))
@@ -444,8 +448,12 @@ class Step:
                                                  self.out, h)]
 
     def run(self):
-        self.layout()
-        self.dispatch()
+        fused = getattr(self, "layout_dispatch", None)
+        if fused is not None:
+            fused()
+        else:
+            self.layout()
+            self.dispatch()
         self.combine()
 
     def calls_on(self, stream):
@@ -454,9 +462,8 @@ class Step:
         h = stream.cuda_stream
         if self.spec.get("per_rank"):
             return self._rank_calls_on(stream)
-        calls = [moe.prepare_layout(self.desc, self.ids, self.lay, self.ws, h),
-                 moe.prepare_dispatch(self.desc, self.ids, self.w, self.x, self.sc,
-                                      self.lay["slot_of"], self.records, h)]
+        calls = [moe.prepare_layout_dispatch(self.desc, self.ids, self.w, self.x, self.sc, self.lay,
+                                             self.ws, self.records, h)]
         if self.spec.get("norm"):
             calls.append(moe.prepare_combine_norm(
                 self.cdesc, moe.MOE_COMBINE_TOPK_RANKS, self.y, self.ids, self.w,

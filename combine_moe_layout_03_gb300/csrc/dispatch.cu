@@ -113,10 +113,17 @@ __device__ __forceinline__ void quant_nvfp4(const uint8_t* row, int H, uint8_t* 
   }
 }
 
-template <int OUT_KIND>
+// EARLY (used only right after this library's own layout kernel, in
+// moe_layout_dispatch): the row copy, its quantisation and the id and weight
+// rows -- inputs the layout kernel does not write -- happen before
+// griddepcontrol.wait, overlapping the layout; only slot_of, the layout's
+// output, is read after it.
+template <int OUT_KIND, bool EARLY = false>
 __global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p) {
-  pdl_wait();
-  pdl_trigger();
+  if (!EARLY) {
+    pdl_wait();
+    pdl_trigger();
+  }
   // Dynamic shared memory: the record body (record bytes [16, record_bytes)),
   // then, for the quantising kinds, the staged BF16 input row.
   extern __shared__ __align__(128) uint8_t img[];
@@ -143,9 +150,11 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p)
   // slots, ids and weights of this token
   if (threadIdx.x < k) {
     const int64_t q = (int64_t)t * k + threadIdx.x;
-    const int s = p.slot_of[q];
+    if (!EARLY) {
+      const int s = p.slot_of[q];
+      s_slot[threadIdx.x] = (s >= 0 && (int64_t)s < p.record_capacity) ? s : -1;
+    }
     const int e = p.topk_idx[q];
-    s_slot[threadIdx.x] = (s >= 0 && (int64_t)s < p.record_capacity) ? s : -1;
     s_expert[threadIdx.x] = e;
     reinterpret_cast<int32_t*>(img + oi)[threadIdx.x] = e;
     reinterpret_cast<uint32_t*>(img + ow)[threadIdx.x] = __float_as_uint(p.topk_weights[q]);
@@ -164,6 +173,14 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p)
   }
 
   fence_proxy_async_smem();
+  if (EARLY) {
+    pdl_wait();  // the layout has completed: slot_of is final
+    pdl_trigger();
+    if (threadIdx.x < k) {
+      const int s = p.slot_of[(int64_t)t * k + threadIdx.x];
+      s_slot[threadIdx.x] = (s >= 0 && (int64_t)s < p.record_capacity) ? s : -1;
+    }
+  }
   __syncthreads();
 
   if (threadIdx.x < k) {
@@ -320,17 +337,25 @@ __global__ void __launch_bounds__(kDispatchThreads)
 
 }  // namespace
 
-cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, cudaStream_t s) {
+template <bool EARLY>
+const void* dispatch_kernel(int out_kind) {
+  switch (out_kind) {
+    case MOE_PAYLOAD_BF16: return (const void*)k_dispatch<MOE_PAYLOAD_BF16, EARLY>;
+    case MOE_PAYLOAD_FP8_E4M3_B128: return (const void*)k_dispatch<MOE_PAYLOAD_FP8_E4M3_B128, EARLY>;
+    case MOE_PAYLOAD_NVFP4_B16: return (const void*)k_dispatch<MOE_PAYLOAD_NVFP4_B16, EARLY>;
+    default: return (const void*)k_dispatch<MOE_PAYLOAD_RAW, EARLY>;
+  }
+}
+
+cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, cudaStream_t s,
+                            bool after_layout) {
   (void)in_kind;
   const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16;
   const size_t smem = (size_t)(p.record_bytes - 16) + (quant ? (size_t)p.in_row_bytes : 0);
-  const void* fn = nullptr;
-  switch (out_kind) {
-    case MOE_PAYLOAD_BF16: fn = (const void*)k_dispatch<MOE_PAYLOAD_BF16>; break;
-    case MOE_PAYLOAD_FP8_E4M3_B128: fn = (const void*)k_dispatch<MOE_PAYLOAD_FP8_E4M3_B128>; break;
-    case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_dispatch<MOE_PAYLOAD_NVFP4_B16>; break;
-    default: fn = (const void*)k_dispatch<MOE_PAYLOAD_RAW>; break;
-  }
+  // the early form only when the stream's previous kernel is our layout and
+  // the launch may overlap it
+  const void* fn = after_layout && pdl_enabled() ? dispatch_kernel<true>(out_kind)
+                                                 : dispatch_kernel<false>(out_kind);
   cudaError_t err = ensure_dynamic_smem(fn, smem);
   if (err != cudaSuccess) return err;
   DispatchParams q = p;

@@ -253,13 +253,20 @@ int moe_layout_status(const void* workspace, int32_t* status, moe_stream_t strea
   return MOE_OK;
 }
 
-int moe_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* topk_weights,
-                 const void* hidden, const void* scales, const int32_t* slot_of, void* records,
-                 size_t records_bytes, moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates moe_dispatch's arguments and fills its launch parameters.
+// Returns MOE_OK (p ready), or an error; *empty is set when there is no work.
+int dispatch_params(const moe_desc_t* desc, const int32_t* topk_idx, const float* topk_weights,
+                    const void* hidden, const void* scales, const int32_t* slot_of, void* records,
+                    size_t records_bytes, moe::DispatchParams* p, bool* empty) {
   moe_record_layout_t lay;
   int rc = record_layout(desc, &lay);
   if (rc != MOE_OK) return rc;
   const int N = desc->num_tokens;
+  *empty = N == 0;
   if (N == 0) return MOE_OK;
   const bool raw = desc->out_kind == MOE_PAYLOAD_RAW;
   if (!topk_idx || !topk_weights || !hidden || !slot_of || !records) return MOE_ERR_INVALID_ARG;
@@ -269,27 +276,59 @@ int moe_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* t
   if (!aligned(hidden, 16) || !aligned(records, 16) || (raw && scales && !aligned(scales, 16)))
     return MOE_ERR_ALIGNMENT;
   if (records_bytes < (size_t)lay.record_bytes) return MOE_ERR_CAPACITY;
+  p->topk_idx = topk_idx;
+  p->topk_weights = topk_weights;
+  p->hidden = (const uint8_t*)hidden;
+  p->scales = (const uint8_t*)scales;
+  p->slot_of = slot_of;
+  p->records = (uint8_t*)records;
+  p->record_capacity = (int64_t)(records_bytes / (size_t)lay.record_bytes);
+  p->num_tokens = N;
+  p->topk = desc->topk;
+  p->hidden_size = desc->hidden;
+  p->in_row_bytes = raw ? desc->raw_payload_bytes : 2 * desc->hidden;
+  p->in_scale_bytes = raw ? desc->raw_scale_bytes : 0;
+  p->record_bytes = lay.record_bytes;
+  p->off_ids = lay.off_ids;
+  p->off_weights = lay.off_weights;
+  p->off_payload = lay.off_payload;
+  p->off_scales = lay.off_scales;
+  p->payload_bytes = lay.payload_bytes;
+  p->scale_bytes = lay.scale_bytes;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* topk_weights,
+                 const void* hidden, const void* scales, const int32_t* slot_of, void* records,
+                 size_t records_bytes, moe_stream_t stream) {
   moe::DispatchParams p;
-  p.topk_idx = topk_idx;
-  p.topk_weights = topk_weights;
-  p.hidden = (const uint8_t*)hidden;
-  p.scales = (const uint8_t*)scales;
-  p.slot_of = slot_of;
-  p.records = (uint8_t*)records;
-  p.record_capacity = (int64_t)(records_bytes / (size_t)lay.record_bytes);
-  p.num_tokens = N;
-  p.topk = desc->topk;
-  p.hidden_size = desc->hidden;
-  p.in_row_bytes = raw ? desc->raw_payload_bytes : 2 * desc->hidden;
-  p.in_scale_bytes = raw ? desc->raw_scale_bytes : 0;
-  p.record_bytes = lay.record_bytes;
-  p.off_ids = lay.off_ids;
-  p.off_weights = lay.off_weights;
-  p.off_payload = lay.off_payload;
-  p.off_scales = lay.off_scales;
-  p.payload_bytes = lay.payload_bytes;
-  p.scale_bytes = lay.scale_bytes;
+  bool empty = false;
+  int rc = dispatch_params(desc, topk_idx, topk_weights, hidden, scales, slot_of, records,
+                           records_bytes, &p, &empty);
+  if (rc != MOE_OK || empty) return rc;
   return cuda_status(moe::launch_dispatch(p, desc->in_kind, desc->out_kind, (cudaStream_t)stream));
+}
+
+int moe_layout_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* topk_weights,
+                        const void* hidden, const void* scales, int32_t* tokens_per_expert,
+                        int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
+                        int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot,
+                        void* workspace, size_t ws_bytes, void* records, size_t records_bytes,
+                        moe_stream_t stream) {
+  moe::DispatchParams p;
+  bool empty = false;
+  int rc = dispatch_params(desc, topk_idx, topk_weights, hidden, scales, slot_of, records,
+                           records_bytes, &p, &empty);
+  if (rc != MOE_OK) return rc;
+  rc = moe_layout(desc, topk_idx, tokens_per_expert, tokens_per_rank, is_token_in_rank,
+                  expert_offset, rank_offset, slot_of, src_of_slot, workspace, ws_bytes, stream);
+  if (rc != MOE_OK || empty) return rc;
+  return cuda_status(
+      moe::launch_dispatch(p, desc->in_kind, desc->out_kind, (cudaStream_t)stream, true));
 }
 
 int moe_combine(const moe_desc_t* desc, int mode, const void* expert_out, int64_t expert_out_rows,

@@ -153,7 +153,11 @@ size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s);
-cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, cudaStream_t s);
+// after_layout: the previous kernel on s is this library's layout kernel,
+// launched by the same call (moe_layout_dispatch), so the row work may start
+// before it ends.
+cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, cudaStream_t s,
+                            bool after_layout = false);
 cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t rows,
                                  int hidden_size, int num_ranks, cudaStream_t s);

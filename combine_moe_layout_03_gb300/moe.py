@@ -71,6 +71,8 @@ _lib.moe_layout_status.restype = ctypes.c_int
 _lib.moe_layout_status.argtypes = [_vp, ctypes.POINTER(_i32), _vp]
 _lib.moe_dispatch.restype = ctypes.c_int
 _lib.moe_dispatch.argtypes = [_D] + [_vp] * 6 + [_sz, _vp]
+_lib.moe_layout_dispatch.restype = ctypes.c_int
+_lib.moe_layout_dispatch.argtypes = [_D] + [_vp] * 12 + [_sz, _vp, _sz, _vp]
 _lib.moe_combine.restype = ctypes.c_int
 _lib.moe_combine.argtypes = [_D, ctypes.c_int, _vp, _i64, _vp, _vp, _vp, _vp, _vp]
 _lib.moe_combine_norm.restype = ctypes.c_int
@@ -526,6 +528,36 @@ def prepare_layout(desc: MoeDesc, topk_idx, out: dict, workspace, stream=None) -
     return Prepared("moe_layout", args, (d, topk_idx, out, workspace))
 
 
+def moe_layout_dispatch(desc: MoeDesc, topk_idx, topk_weights, hidden, scales, out: dict | None = None,
+                        workspace=None, records=None, stream=None):
+    """moe_layout then moe_dispatch in one call (see include/moe.h); the
+    dispatch overlaps the layout. Returns (layout outputs dict, records)."""
+    dev = topk_idx.device
+    if out is None:
+        out = layout_outputs(desc, dev)
+    if workspace is None:
+        workspace = torch.empty(max(moe_workspace_size(desc), 256), dtype=torch.uint8, device=dev)
+    if records is None:
+        rb = moe_record_layout(desc)["record_bytes"]
+        records = torch.empty((max(desc.num_tokens * desc.topk, 1), rb), dtype=torch.uint8, device=dev)
+    prepare_layout_dispatch(desc, topk_idx, topk_weights, hidden, scales, out, workspace, records,
+                            stream)()
+    out["workspace"] = workspace
+    return out, records
+
+
+def prepare_layout_dispatch(desc: MoeDesc, topk_idx, topk_weights, hidden, scales, out: dict,
+                            workspace, records, stream=None) -> Prepared:
+    d = desc.c()
+    ptrs = _vps(topk_idx, topk_weights, hidden, scales, out["tokens_per_expert"],
+                out["tokens_per_rank"], out["is_token_in_rank"], out["expert_offset"],
+                out["rank_offset"], out["slot_of"], out.get("src_of_slot"), workspace)
+    args = (ctypes.byref(d), *ptrs, ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(_ptr(records)),
+            ctypes.c_size_t(records.numel() * records.element_size()), ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_layout_dispatch", args, (d, topk_idx, topk_weights, hidden, scales, out,
+                                                  workspace, records))
+
+
 def prepare_dispatch(desc: MoeDesc, topk_idx, topk_weights, hidden, scales, slot_of, records,
                      stream=None) -> Prepared:
     d = desc.c()
@@ -633,4 +665,4 @@ def exported_symbols() -> list[str]:
             "moe_pack_slots", "moe_unpack_slots", "moe_mask_topk_ids", "moe_rank_layout",
             "moe_dispatch_ranks", "moe_combine_gather_ranks", "moe_ll_layout",
             "moe_dispatch_ll", "moe_combine_backward", "moe_dispatch_backward",
-            "moe_combine_gather_ranks_backward"]
+            "moe_combine_gather_ranks_backward", "moe_layout_dispatch"]

@@ -199,6 +199,21 @@ int moe_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* t
                  const void* hidden, const void* scales, const int32_t* slot_of, void* records,
                  size_t records_bytes, moe_stream_t stream);
 
+/* moe_layout followed by moe_dispatch in one call: the same outputs, bit for
+ * bit, as the two calls in sequence. Because the kernel before the dispatch
+ * is then known to be this call's own layout kernel, which writes none of
+ * the dispatch's inputs, the dispatch loads and quantises its token rows
+ * while the layout still runs and reads only slot_of after it (programmatic
+ * dependent launch; with MOE_PDL=0 the two run in plain order). Arguments are
+ * those of the two calls; all of them are checked before anything is
+ * launched. Errors: as moe_layout and moe_dispatch. */
+int moe_layout_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* topk_weights,
+                        const void* hidden, const void* scales, int32_t* tokens_per_expert,
+                        int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
+                        int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot,
+                        void* workspace, size_t ws_bytes, void* records, size_t records_bytes,
+                        moe_stream_t stream);
+
 /* Combine.
  * MOE_COMBINE_TOPK: expert_out bf16 [P, H] holds the expert outputs in slot
  *   order; out bf16 [N, H] with
