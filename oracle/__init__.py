@@ -17,7 +17,7 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _HDR = os.path.join(_HERE, "oracle.h")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-BF16, FP8_E4M3_B128, NVFP4_B16, RAW = 0, 1, 2, 3
+BF16, FP8_E4M3_B128, NVFP4_B16, RAW, FP8_E4M3_UE8M0 = 0, 1, 2, 3, 4
 
 _lib = None
 
@@ -54,6 +54,7 @@ def _load():
         _lib.oracle_e2m1_encode.argtypes = [f32]
         _lib.oracle_fp8_group.restype = None
         _lib.oracle_nvfp4_group.restype = None
+        _lib.oracle_fp8_ue8m0_group.restype = None
         for name in ("oracle_record_layout", "oracle_layout", "oracle_dispatch",
                      "oracle_identity_expert", "oracle_combine_topk", "oracle_combine_ranks",
                      "oracle_combine_topk_ranks", "oracle_combine_topk_f64"):
@@ -145,6 +146,15 @@ def nvfp4_group(x_bf16: np.ndarray):
 
 
 # ---- record layout -----------------------------------------------------------
+
+def fp8_ue8m0_group(x_bf16: np.ndarray):
+    """(e4m3 codes uint8 [n], UE8M0 scale byte) of one group."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    q = np.zeros(x.size, np.uint8)
+    b = np.zeros(1, np.uint8)
+    _load().oracle_fp8_ue8m0_group(_p(x), x.size, _p(q), _p(b))
+    return q, int(b[0])
+
 
 def record_layout(topk: int, hidden: int, in_kind: int, out_kind: int,
                   raw_payload_bytes: int = 0, raw_scale_bytes: int = 0) -> dict:

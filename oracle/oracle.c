@@ -138,6 +138,31 @@ void oracle_fp8_group(const uint16_t* x, int n, uint8_t* q, float* scale) {
   *scale = s;
 }
 
+/* FP8 e4m3 per 128 channels with a power-of-two scale kept as one UE8M0
+ * byte ([EP] Buffer::low_latency_dispatch: use_ue8m0 requires round_scale,
+ * and the scales become int32 [E_l, H/512, R * maxT] -- one byte per
+ * 128-channel group, four groups to an int). The pages give no formula.
+ * Reading: the scale is rounded up to a power of two, so nothing saturates:
+ *   a = max(amax, 1e-4);  v = a / 448 (IEEE fp32);
+ *   e = the least integer with 2^e >= v;
+ *   q_i = e4m3(x_i * 2^-e)   (multiplying by a power of two is exact);
+ *   byte = e + 127           (UE8M0 stores the biased exponent: 2^(byte-127)). */
+void oracle_fp8_ue8m0_group(const uint16_t* x, int n, uint8_t* q, uint8_t* byte) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float v = fabsf(oracle_bf16_to_f32(x[i]));
+    if (v > amax) amax = v;
+  }
+  float a = (amax > 1e-4f) ? amax : 1e-4f;
+  float v = a / 448.0f;
+  int ex;
+  double m = frexp((double)v, &ex); /* v = m * 2^ex, m in [0.5, 1) */
+  int e = (m == 0.5) ? ex - 1 : ex;
+  float inv = ldexpf(1.0f, -e);
+  for (int i = 0; i < n; ++i) q[i] = oracle_e4m3_encode(oracle_bf16_to_f32(x[i]) * inv);
+  *byte = (uint8_t)(e + 127);
+}
+
 /* NVFP4: FP4 e2m1 values with one e4m3 scale byte per group of 16 ([AG]
  * decode payload: 3584 packed bytes + 448 scale bytes for hidden 7168). The
  * pages give no formula and no global scale. Reading:
@@ -193,6 +218,10 @@ int oracle_record_layout(int topk, int hidden, int in_kind, int out_kind,
     if (hidden % 16) return -1;
     pb = hidden / 2;
     sb = hidden / 16;
+  } else if (out_kind == ORACLE_FP8_E4M3_UE8M0 && in_kind == ORACLE_BF16) {
+    if (hidden % 128) return -1;
+    pb = hidden;
+    sb = hidden / 128;
   } else if (out_kind == ORACLE_RAW && in_kind == ORACLE_RAW) {
     if (raw_payload_bytes < 0 || raw_scale_bytes < 0) return -1;
     pb = raw_payload_bytes;
@@ -322,6 +351,10 @@ int oracle_dispatch(const int32_t* topk_idx, const float* topk_weights,
     } else if (out_kind == ORACLE_NVFP4_B16) {
       const uint16_t* x = (const uint16_t*)hidden + (size_t)t * hidden_size;
       for (int g = 0; g < hidden_size / 16; ++g) oracle_nvfp4_group(x + g * 16, 16, pay + g * 8, sca + g);
+    } else if (out_kind == ORACLE_FP8_E4M3_UE8M0) {
+      const uint16_t* x = (const uint16_t*)hidden + (size_t)t * hidden_size;
+      for (int g = 0; g < hidden_size / 128; ++g)
+        oracle_fp8_ue8m0_group(x + g * 128, 128, pay + g * 128, sca + g);
     } else { /* RAW: opaque bytes, copied as they are */
       memcpy(pay, (const uint8_t*)hidden + (size_t)t * pb, (size_t)pb);
       if (sb) memcpy(sca, (const uint8_t*)scales + (size_t)t * sb, (size_t)sb);
@@ -363,6 +396,9 @@ int oracle_identity_expert(const uint8_t* records, int num_records, int topk,
         float sc;
         memcpy(&sc, rec + off_s + 4 * (h / 128), 4);
         row[h] = oracle_f32_to_bf16(oracle_e4m3_value(rec[off_p + h]) * sc);
+      } else if (out_kind == ORACLE_FP8_E4M3_UE8M0) {
+        int e = (int)rec[off_s + h / 128] - 127;
+        row[h] = oracle_f32_to_bf16(ldexpf(oracle_e4m3_value(rec[off_p + h]), e));
       } else {
         uint8_t b = rec[off_p + h / 2];
         uint8_t c = (h & 1) ? (uint8_t)(b >> 4) : (uint8_t)(b & 15);

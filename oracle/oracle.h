@@ -24,7 +24,8 @@ extern "C" {
 #endif
 
 /* Payload kinds: what a record carries in its payload segment. */
-enum { ORACLE_BF16 = 0, ORACLE_FP8_E4M3_B128 = 1, ORACLE_NVFP4_B16 = 2, ORACLE_RAW = 3 };
+enum { ORACLE_BF16 = 0, ORACLE_FP8_E4M3_B128 = 1, ORACLE_NVFP4_B16 = 2, ORACLE_RAW = 3,
+       ORACLE_FP8_E4M3_UE8M0 = 4 };
 
 /* ---- number formats ---------------------------------------------------- */
 float    oracle_bf16_to_f32(uint16_t b);
@@ -37,6 +38,7 @@ uint8_t  oracle_e2m1_encode(float x);      /* nearest, ties even, saturating */
 /* ---- quantisers of one group of BF16 values ----------------------------- */
 void oracle_fp8_group(const uint16_t* x, int n, uint8_t* q, float* scale);
 void oracle_nvfp4_group(const uint16_t* x, int n, uint8_t* q_packed, uint8_t* scale);
+void oracle_fp8_ue8m0_group(const uint16_t* x, int n, uint8_t* q, uint8_t* byte);
 
 /* ---- record layout: out[7] = {record_bytes, off_ids, off_weights,
  *      off_payload, off_scales, payload_bytes, scale_bytes} ------------ */
