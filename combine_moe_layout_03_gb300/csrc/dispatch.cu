@@ -80,6 +80,42 @@ __device__ __forceinline__ void quant_fp8(const uint8_t* row, int H, uint8_t* pa
   }
 }
 
+// FP8 e4m3 with a power-of-two scale per 128 channels, kept as one UE8M0
+// byte. Same half-warp layout as quant_fp8. a = max(amax, 1e-4) -> v = a / 448
+// (IEEE) -> e = the least integer with 2^e >= v: v's exponent field, plus one
+// unless its mantissa is zero (v lies in [2^-23, 2^120], always normal) ->
+// q = e4m3(x * 2^-e), an exact scaling -> byte = e + 127.
+__device__ __forceinline__ void quant_fp8_ue8m0(const uint8_t* row, int H, uint8_t* pay, uint8_t* scl) {
+  const int groups = H / 128;
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int half = (int)(lane_id() >> 4), li = (int)(lane_id() & 15);
+  for (int gp = warp; gp * 2 < groups; gp += nwarps) {
+    const int g = gp * 2 + half;
+    const bool on = g < groups;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (on) v = *reinterpret_cast<const uint4*>(row + g * 256 + li * 16);
+    float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const uint32_t vb = __float_as_uint(__fdiv_rn(fmaxf(amax, 1e-4f), 448.0f));
+    const int e = (int)((vb >> 23) & 0xffu) - 127 + ((vb & 0x7fffffu) ? 1 : 0);
+    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+    uint2 q;
+    q.x = cvt_e4m3x2(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv)) |
+          cvt_e4m3x2(__fmul_rn(x[2], inv), __fmul_rn(x[3], inv)) << 16;
+    q.y = cvt_e4m3x2(__fmul_rn(x[4], inv), __fmul_rn(x[5], inv)) |
+          cvt_e4m3x2(__fmul_rn(x[6], inv), __fmul_rn(x[7], inv)) << 16;
+    if (on) {
+      *reinterpret_cast<uint2*>(pay + g * 128 + li * 8) = q;
+      if (li == 0) scl[g] = (uint8_t)(e + 127);
+    }
+  }
+}
+
 // NVFP4: e2m1 codes with one e4m3 scale byte per 16 channels. A lane pair
 // covers one group: 2 lanes x 8 BF16 values. amax -> sc = e4m3(amax / 6) ->
 // d = value(sc) -> q = d == 0 ? 0 : e2m1(x / d) (IEEE divisions). Byte i of
@@ -134,7 +170,8 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p)
   const int body = p.record_bytes - 16;
   const int oi = p.off_ids - 16, ow = p.off_weights - 16, op = p.off_payload - 16,
             os = p.off_scales - 16;
-  constexpr bool kQuant = OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128 || OUT_KIND == MOE_PAYLOAD_NVFP4_B16;
+  constexpr bool kQuant = OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128 || OUT_KIND == MOE_PAYLOAD_NVFP4_B16 ||
+                          OUT_KIND == MOE_PAYLOAD_FP8_E4M3_UE8M0;
   uint8_t* stage = img + body;
 
   // start the row's copies first so they overlap the small loads below
@@ -170,6 +207,8 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p)
     quant_fp8(stage, p.hidden_size, img + op, reinterpret_cast<float*>(img + os));
   } else if (OUT_KIND == MOE_PAYLOAD_NVFP4_B16) {
     quant_nvfp4(stage, p.hidden_size, img + op, img + os);
+  } else if (OUT_KIND == MOE_PAYLOAD_FP8_E4M3_UE8M0) {
+    quant_fp8_ue8m0(stage, p.hidden_size, img + op, img + os);
   }
 
   fence_proxy_async_smem();
@@ -218,7 +257,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
   const int k = p.topk;
   const int tail = p.record_bytes - p.off_payload;
   const int os = p.off_scales - p.off_payload;
-  constexpr bool kQuant = OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128 || OUT_KIND == MOE_PAYLOAD_NVFP4_B16;
+  constexpr bool kQuant = OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128 || OUT_KIND == MOE_PAYLOAD_NVFP4_B16 ||
+                          OUT_KIND == MOE_PAYLOAD_FP8_E4M3_UE8M0;
   uint8_t* stage = img + tail;
   const uint8_t* row = p.hidden + (size_t)t * p.in_row_bytes;
   if (kQuant) {
@@ -243,6 +283,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
     quant_fp8(stage, p.hidden_size, img, reinterpret_cast<float*>(img + os));
   } else if (OUT_KIND == MOE_PAYLOAD_NVFP4_B16) {
     quant_nvfp4(stage, p.hidden_size, img, img + os);
+  } else if (OUT_KIND == MOE_PAYLOAD_FP8_E4M3_UE8M0) {
+    quant_fp8_ue8m0(stage, p.hidden_size, img, img + os);
   }
   fence_proxy_async_smem();
   __syncthreads();
@@ -288,7 +330,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
 // Payload and scales only, into two fixed-capacity, expert-major arrays (the
 // low-latency receive buffers of DeepEP Buffer::low_latency_dispatch):
 // pair (t, j) goes to row pos = slot_of[t, j] of x_out [rows, payload_bytes]
-// and of scales_out [rows, scale_bytes]. The payload is built once per token
+// and of scales_out [rows, scale_bytes rounded up to 16] (pad bytes zero). The payload is built once per token
 // in shared memory as above; thread j issues the two bulk stores.
 template <int OUT_KIND>
 __global__ void __launch_bounds__(kDispatchThreads)
@@ -300,8 +342,10 @@ __global__ void __launch_bounds__(kDispatchThreads)
   const int t = blockIdx.x;
   const int k = p.topk;
   const int pb = p.payload_bytes, sb = p.scale_bytes;
-  constexpr bool kQuant = OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128 || OUT_KIND == MOE_PAYLOAD_NVFP4_B16;
-  uint8_t* stage = img + pb + sb;
+  const int sbp = (sb + 15) & ~15;  // scale rows are padded to 16 bytes (zeros)
+  constexpr bool kQuant = OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128 || OUT_KIND == MOE_PAYLOAD_NVFP4_B16 ||
+                          OUT_KIND == MOE_PAYLOAD_FP8_E4M3_UE8M0;
+  uint8_t* stage = img + pb + sbp;
   const uint8_t* row = p.hidden + (size_t)t * p.in_row_bytes;
   if (kQuant) {
     copy_g2s_async(stage, row, p.in_row_bytes / 16);
@@ -314,12 +358,15 @@ __global__ void __launch_bounds__(kDispatchThreads)
     const int pos = p.slot_of[(int64_t)t * k + threadIdx.x];
     s_pos[threadIdx.x] = (pos >= 0 && (int64_t)pos < rows) ? pos : -1;
   }
+  zero_bytes(img, pb + sb, pb + sbp);
   cp_async_wait_all();
   __syncthreads();
   if (OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128) {
     quant_fp8(stage, p.hidden_size, img, reinterpret_cast<float*>(img + pb));
   } else if (OUT_KIND == MOE_PAYLOAD_NVFP4_B16) {
     quant_nvfp4(stage, p.hidden_size, img, img + pb);
+  } else if (OUT_KIND == MOE_PAYLOAD_FP8_E4M3_UE8M0) {
+    quant_fp8_ue8m0(stage, p.hidden_size, img, img + pb);
   }
   fence_proxy_async_smem();
   __syncthreads();
@@ -328,7 +375,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
     if (pos >= 0) {
       const uint64_t pol = l2_evict_first_policy();
       bulk_store_s2g_evict_first(x_out + (size_t)pos * pb, img, (uint32_t)pb, pol);
-      if (sb > 0) bulk_store_s2g_evict_first(scales_out + (size_t)pos * sb, img + pb, (uint32_t)sb, pol);
+      if (sb > 0) bulk_store_s2g_evict_first(scales_out + (size_t)pos * sbp, img + pb, (uint32_t)sbp, pol);
       bulk_commit();
       bulk_wait_read_all();
     }
@@ -343,6 +390,7 @@ const void* dispatch_kernel(int out_kind) {
     case MOE_PAYLOAD_BF16: return (const void*)k_dispatch<MOE_PAYLOAD_BF16, EARLY>;
     case MOE_PAYLOAD_FP8_E4M3_B128: return (const void*)k_dispatch<MOE_PAYLOAD_FP8_E4M3_B128, EARLY>;
     case MOE_PAYLOAD_NVFP4_B16: return (const void*)k_dispatch<MOE_PAYLOAD_NVFP4_B16, EARLY>;
+    case MOE_PAYLOAD_FP8_E4M3_UE8M0: return (const void*)k_dispatch<MOE_PAYLOAD_FP8_E4M3_UE8M0, EARLY>;
     default: return (const void*)k_dispatch<MOE_PAYLOAD_RAW, EARLY>;
   }
 }
@@ -350,7 +398,8 @@ const void* dispatch_kernel(int out_kind) {
 cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, cudaStream_t s,
                             bool after_layout) {
   (void)in_kind;
-  const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16;
+  const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16 ||
+                     out_kind == MOE_PAYLOAD_FP8_E4M3_UE8M0;
   const size_t smem = (size_t)(p.record_bytes - 16) + (quant ? (size_t)p.in_row_bytes : 0);
   // the early form only when the stream's previous kernel is our layout and
   // the launch may overlap it
@@ -365,13 +414,15 @@ cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, 
 
 cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const int32_t* send_head,
                                   int num_ranks, int experts_per_rank, cudaStream_t s) {
-  const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16;
+  const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16 ||
+                     out_kind == MOE_PAYLOAD_FP8_E4M3_UE8M0;
   const size_t smem = (size_t)(p.record_bytes - p.off_payload) + (quant ? (size_t)p.in_row_bytes : 0);
   const void* fn = nullptr;
   switch (out_kind) {
     case MOE_PAYLOAD_BF16: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_BF16>; break;
     case MOE_PAYLOAD_FP8_E4M3_B128: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_FP8_E4M3_B128>; break;
     case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_NVFP4_B16>; break;
+    case MOE_PAYLOAD_FP8_E4M3_UE8M0: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_FP8_E4M3_UE8M0>; break;
     default: fn = (const void*)k_dispatch_ranks<MOE_PAYLOAD_RAW>; break;
   }
   cudaError_t err = ensure_dynamic_smem(fn, smem);
@@ -385,13 +436,16 @@ cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const i
 
 cudaError_t launch_dispatch_packed(const DispatchParams& p, int out_kind, uint8_t* x_out,
                                    uint8_t* scales_out, int64_t rows, cudaStream_t s) {
-  const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16;
-  const size_t smem = (size_t)p.payload_bytes + (size_t)p.scale_bytes + (quant ? (size_t)p.in_row_bytes : 0);
+  const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16 ||
+                     out_kind == MOE_PAYLOAD_FP8_E4M3_UE8M0;
+  const size_t smem = (size_t)p.payload_bytes + (size_t)((p.scale_bytes + 15) & ~15) +
+                      (quant ? (size_t)p.in_row_bytes : 0);
   const void* fn = nullptr;
   switch (out_kind) {
     case MOE_PAYLOAD_BF16: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_BF16>; break;
     case MOE_PAYLOAD_FP8_E4M3_B128: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_FP8_E4M3_B128>; break;
     case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_NVFP4_B16>; break;
+    case MOE_PAYLOAD_FP8_E4M3_UE8M0: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_FP8_E4M3_UE8M0>; break;
     default: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_RAW>; break;
   }
   cudaError_t err = ensure_dynamic_smem(fn, smem);

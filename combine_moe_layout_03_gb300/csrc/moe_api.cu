@@ -145,6 +145,11 @@ int record_layout(const moe_desc_t* d, moe_record_layout_t* o) {
         pb = H / 2;
         sb = H / 16;
         break;
+      case MOE_PAYLOAD_FP8_E4M3_UE8M0:
+        if (H % 128) return MOE_ERR_SHAPE;
+        pb = H;
+        sb = H / 128;
+        break;
       default:
         return MOE_ERR_INVALID_ARG;
     }
@@ -553,7 +558,8 @@ int moe_dispatch_ll(const moe_desc_t* desc, const void* hidden, const void* scal
   moe_record_layout_t lay;
   int rc = record_layout(desc, &lay);
   if (rc != MOE_OK) return rc;
-  if (lay.payload_bytes % 16 || lay.scale_bytes % 16) return MOE_ERR_SHAPE;
+  if (lay.payload_bytes % 16) return MOE_ERR_SHAPE;
+  const int64_t scale_row = (lay.scale_bytes + 15) / 16 * 16;  // padded scale rows
   const int N = desc->num_tokens;
   if (N == 0) return MOE_OK;
   const bool raw = desc->out_kind == MOE_PAYLOAD_RAW;
@@ -566,7 +572,7 @@ int moe_dispatch_ll(const moe_desc_t* desc, const void* hidden, const void* scal
   if (lay.payload_bytes == 0) return MOE_ERR_SHAPE;
   int64_t rows = (int64_t)(x_out_bytes / (size_t)lay.payload_bytes);
   if (lay.scale_bytes > 0) {
-    const int64_t srows = (int64_t)(scales_out_bytes / (size_t)lay.scale_bytes);
+    const int64_t srows = (int64_t)(scales_out_bytes / (size_t)scale_row);
     if (srows < rows) rows = srows;
   }
   moe::DispatchParams p = {};

@@ -30,6 +30,7 @@ MOE_PAYLOAD_BF16 = 0
 MOE_PAYLOAD_FP8_E4M3_B128 = 1
 MOE_PAYLOAD_NVFP4_B16 = 2
 MOE_PAYLOAD_RAW = 3
+MOE_PAYLOAD_FP8_E4M3_UE8M0 = 4
 
 MOE_COMBINE_TOPK = 0
 MOE_COMBINE_RANKS = 1
@@ -406,7 +407,8 @@ def moe_dispatch_ll(desc: MoeDesc, hidden, scales, ll_slot_of, capacity: int,
     if x_out is None:
         x_out = torch.empty((rows, lay["payload_bytes"]), dtype=torch.uint8, device=dev)
     if scales_out is None and lay["scale_bytes"]:
-        scales_out = torch.empty((rows, lay["scale_bytes"]), dtype=torch.uint8, device=dev)
+        scale_row = (lay["scale_bytes"] + 15) // 16 * 16
+        scales_out = torch.empty((rows, scale_row), dtype=torch.uint8, device=dev)
     sb = scales_out.numel() * scales_out.element_size() if scales_out is not None else 0
     rc = _lib.moe_dispatch_ll(ctypes.byref(desc.c()), _ptr(hidden), _ptr(scales), _ptr(ll_slot_of),
                               _ptr(x_out), x_out.numel() * x_out.element_size(), _ptr(scales_out),

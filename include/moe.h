@@ -73,11 +73,18 @@ typedef void* moe_stream_t;
 /* ---- payload kinds ------------------------------------------------------- */
 /* What the caller's hidden rows are (in_kind) and what records carry
  * (out_kind). Valid pairs: (BF16, BF16), (BF16, FP8_E4M3_B128),
- * (BF16, NVFP4_B16), (RAW, RAW). */
+ * (BF16, NVFP4_B16), (BF16, FP8_E4M3_UE8M0), (RAW, RAW). */
 #define MOE_PAYLOAD_BF16 0          /* bf16 [H] per token, H*2 bytes */
 #define MOE_PAYLOAD_FP8_E4M3_B128 1 /* e4m3 [H] + fp32 scale per 128 channels */
 #define MOE_PAYLOAD_NVFP4_B16 2     /* e2m1 [H/2 bytes] + e4m3 scale byte per 16 */
 #define MOE_PAYLOAD_RAW 3           /* opaque bytes copied as they are */
+/* e4m3 [H] + one UE8M0 byte per 128 channels (DeepEP low_latency_dispatch
+ * use_ue8m0 / round_scale: one byte per 128-channel group, four groups to an
+ * int32, H/128 bytes in group order). Reading (no formula on the pages): the
+ * scale is the least power of two 2^e >= max(amax, 1e-4)/448 (the quotient
+ * in IEEE fp32), q = e4m3_rn(x * 2^-e) (exact scaling, never saturating),
+ * byte = e + 127 (value 2^(byte-127)). */
+#define MOE_PAYLOAD_FP8_E4M3_UE8M0 4
 
 /* ---- combine modes -------------------------------------------------------- */
 #define MOE_COMBINE_TOPK 0       /* top-k weighted reduction to token order */
@@ -118,8 +125,9 @@ typedef struct {
  *   [0, 16)                 header: int32 src_token, int32 j, int32 expert, int32 0
  *   [off_ids, +4k)          the token's whole top-k id row (int32)
  *   [off_weights, +4k)      the token's fp32 weight row
- *   [off_payload, +payload_bytes)  BF16 row | e4m3 bytes | packed e2m1 | raw
- *   [off_scales, +scale_bytes)     none | fp32 per 128 | e4m3 byte per 16 | raw
+ *   [off_payload, +payload_bytes)  BF16 row | e4m3 bytes | packed e2m1 | raw | e4m3 bytes
+ *   [off_scales, +scale_bytes)     none | fp32 per 128 | e4m3 byte per 16 | raw |
+ *                                  UE8M0 byte per 128
  * NVFP4 packing: byte i holds element 2i in bits 0-3 and element 2i+1 in bits
  * 4-7; e2m1 code = sign << 3 | magnitude index into {0,.5,1,1.5,2,3,4,6}. */
 typedef struct {
@@ -369,10 +377,13 @@ int moe_ll_layout(const moe_desc_t* desc, int32_t max_tokens_per_rank, const int
 /* Dispatch into the fixed-capacity buffers: the payload of moe_dispatch
  * (quantised once per token) goes to row ll_slot_of[t, j] of x_out
  * [E * capacity, payload_bytes] and its scales to the same row of scales_out
- * [E * capacity, scale_bytes] (row-major; scales_out may be NULL when there
- * are none). payload_bytes and scale_bytes must be multiples of 16 (FP8:
- * H % 512 == 0, as DeepEP's low-latency FP8 cast requires). x_out_bytes and
- * scales_out_bytes give the buffers' sizes. Errors: as moe_dispatch. */
+ * [E * capacity, scale_row] with scale_row = scale_bytes rounded up to a
+ * multiple of 16, the pad bytes zero (row-major; scales_out may be NULL when
+ * there are none). payload_bytes must be a multiple of 16. FP8 with fp32
+ * scales has no pad when H % 512 == 0, as DeepEP's low-latency FP8 cast
+ * requires; UE8M0 scales (H/128 bytes, 56 at H = 7168) are padded to 64.
+ * x_out_bytes and scales_out_bytes give the buffers' sizes. Errors: as
+ * moe_dispatch. */
 int moe_dispatch_ll(const moe_desc_t* desc, const void* hidden, const void* scales,
                     const int32_t* ll_slot_of, void* x_out, size_t x_out_bytes, void* scales_out,
                     size_t scales_out_bytes, moe_stream_t stream);

@@ -387,13 +387,14 @@ def dispatch_ll(hidden, scales, ll_slot_of, rows: int, in_kind: int, out_kind: i
     n, k = so.shape
     lay = record_layout(k, hidden_size, in_kind, out_kind, raw_payload_bytes, raw_scale_bytes)
     x = np.zeros((rows, lay["payload_bytes"]), np.uint8)
-    sc = np.zeros((rows, max(lay["scale_bytes"], 1)), np.uint8)
+    scale_row = (lay["scale_bytes"] + 15) // 16 * 16
+    sc = np.zeros((rows, max(scale_row, 1)), np.uint8)
     h = np.ascontiguousarray(hidden)
     s_in = None if scales is None else np.ascontiguousarray(scales)
     _check(_load().oracle_dispatch_ll(_p(h), _p(s_in), n, k, hidden_size, in_kind, out_kind,
                                       raw_payload_bytes, raw_scale_bytes, _p(so), rows, _p(x), _p(sc)),
            "dispatch_ll")
-    return x, sc[:, : lay["scale_bytes"]]
+    return x, sc[:, :scale_row]
 
 
 def combine_backward(grad_out, topk_weights, slot_of, y, rows: int, hidden_size: int,

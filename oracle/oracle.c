@@ -821,7 +821,9 @@ int oracle_ll_layout(const int32_t* topk_idx, int num_tokens, int topk, int num_
 }
 
 /* The payload and scales of each token (as oracle_dispatch builds them) to
- * rows ll_slot_of[t, j] of x_out and scales_out. */
+ * rows ll_slot_of[t, j] of x_out and scales_out; scale rows are scale_bytes
+ * rounded up to 16 bytes apart, the pad left zero (the caller zeroes
+ * scales_out). */
 int oracle_dispatch_ll(const void* hidden, const void* scales, int num_tokens, int topk,
                        int hidden_size, int in_kind, int out_kind, int raw_payload_bytes,
                        int raw_scale_bytes, const int32_t* ll_slot_of, int64_t rows,
@@ -858,7 +860,7 @@ int oracle_dispatch_ll(const void* hidden, const void* scales, int num_tokens, i
       int pos = ll_slot_of[(long)t * topk + j];
       if (pos < 0 || pos >= rows) continue;
       memcpy(x_out + (size_t)pos * pb, one + off_p, (size_t)pb);
-      if (sb) memcpy(scales_out + (size_t)pos * sb, one + off_s, (size_t)sb);
+      if (sb) memcpy(scales_out + (size_t)pos * pad16(sb), one + off_s, (size_t)sb);
     }
   }
   free(one);

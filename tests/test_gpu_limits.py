@@ -39,7 +39,8 @@ def _dispatch(ids, w, e, r, h, in_kind, out_kind, x_dev, sc_dev=None, rp=0, rs=0
     return host(rec)
 
 
-@pytest.mark.parametrize("out_kind", [oracle.BF16, oracle.FP8_E4M3_B128, oracle.NVFP4_B16])
+@pytest.mark.parametrize("out_kind", [oracle.BF16, oracle.FP8_E4M3_B128, oracle.NVFP4_B16,
+                                      oracle.FP8_E4M3_UE8M0])
 def test_dispatch_largest_row_top32_1024_experts_64_ranks(out_kind):
     n = 24
     ids, w = _route(1 + out_kind, n, MAX_K, MAX_E)

@@ -85,7 +85,8 @@ def test_ll_layout_rejects_uneven_or_oversize_ranks():
         oracle.ll_layout(ids, 8, 3, 8)   # 10 tokens per rank > 8
 
 
-@pytest.mark.parametrize("out_kind", [oracle.BF16, oracle.FP8_E4M3_B128, oracle.NVFP4_B16, oracle.RAW])
+@pytest.mark.parametrize("out_kind", [oracle.BF16, oracle.FP8_E4M3_B128, oracle.NVFP4_B16, oracle.RAW,
+                                      oracle.FP8_E4M3_UE8M0])
 def test_dispatch_ll_rows_are_the_records_payload(out_kind):
     E, R, maxT = 256, 8, 4
     if out_kind == oracle.RAW:
@@ -103,12 +104,14 @@ def test_dispatch_ll_rows_are_the_records_payload(out_kind):
     rows = E * R * maxT
     xo, so = oracle.dispatch_ll(x, sc, ll["ll_slot_of"], rows, in_kind, out_kind, H, pbr, sbr)
     pb, sb = rl["payload_bytes"], rl["scale_bytes"]
-    assert xo.shape == (rows, pb) and so.shape == (rows, sb)
+    sr = (sb + 15) // 16 * 16  # scale rows padded to 16 bytes
+    assert xo.shape == (rows, pb) and so.shape == (rows, sr)
     filled = np.zeros(rows, bool)
     for t in range(32):
         for j in range(8):
             p, s = ll["ll_slot_of"][t, j], lay["slot_of"][t, j]
             np.testing.assert_array_equal(xo[p], rec[s, rl["off_payload"]:rl["off_payload"] + pb])
-            np.testing.assert_array_equal(so[p], rec[s, rl["off_scales"]:rl["off_scales"] + sb])
+            np.testing.assert_array_equal(so[p, :sb], rec[s, rl["off_scales"]:rl["off_scales"] + sb])
+            assert not so[p, sb:].any()
             filled[p] = True
     assert not xo[~filled].any() and not so[~filled].any()
