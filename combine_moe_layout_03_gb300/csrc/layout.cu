@@ -9,15 +9,18 @@
 //  * Whenever a block's ids and histograms fit in shared memory (every
 //    workload of the pages): one launch of a thread-block cluster of up to 16
 //    blocks of 512 threads, about 2048 pairs each (k_layout_cluster).
-//    Each block stages its run of ids in shared memory with 16-byte loads,
-//    builds its expert histogram, rank-mask rows and per-warp histograms
-//    there, and after a hardware cluster barrier reads the other blocks'
-//    histograms through distributed shared memory to get the expert totals
-//    and its own prefix. Each block then ranks its pairs: per-warp starting
-//    slots from a scan over warps, and within a warp the rank of a pair among
-//    equal experts is popc(match_any mask & lanes below). Slots follow
+//    Each block stages its run of ids in shared memory with 16-byte
+//    asynchronous copies, builds its rank-mask rows and per-warp expert
+//    histograms there, and pushes its expert counts into every block's
+//    shared memory (distributed shared memory stores) before one hardware
+//    cluster barrier; after it each block has all counts locally, so one
+//    block scan gives the expert totals, offsets and its own prefix. Each
+//    block then ranks its pairs: per-warp starting slots from a scan over
+//    warps, and within a warp the rank of a pair among equal experts is the
+//    number of lanes below it whose ids match on every bit. Slots follow
 //    ascending (t, j) inside every expert: deterministic, no global atomics,
-//    no workspace except the status word.
+//    no workspace except the status word. slot_of and src_of_slot are both
+//    written as coalesced runs.
 //  * Larger inputs: k_layout_count (one block per 128-token chunk, chunk
 //    histograms to the workspace), then k_layout_assign, where every block
 //    scans the chunk histograms itself (redundantly, from L2), so no
@@ -37,6 +40,7 @@ namespace {
 constexpr int kCountThreads = 128;   // one thread per token of a chunk
 constexpr int kAssignThreads = 256;  // 8 warps
 constexpr int kClusterThreads = 512;   // 16 warps
+constexpr int kClusterWarps = kClusterThreads / 32;
 constexpr int kClusterMaxBlocks = 16;  // non-portable cluster size where supported, else 8
 constexpr int kClusterPortableBlocks = 8;
 constexpr int kPairsPerClusterBlock = 2048;
@@ -362,118 +366,376 @@ __global__ void __launch_bounds__(kAssignThreads) k_layout_assign(LayoutParams p
   clear_src_tail(p, P);
 }
 
+// Exclusive prefix sums of two per-thread values over the block at once (all
+// threads must call); scratch holds >= 80 ints. *ta, *tb get the block sums.
+template <int NT>
+__device__ __forceinline__ int2 block_exclusive_scan2(int a, int b, int* scratch, int* ta, int* tb) {
+  constexpr int NW = NT / 32;
+  const int warp = threadIdx.x >> 5;
+  const int ia = warp_inclusive_scan(a), ib = warp_inclusive_scan(b);
+  if (lane_id() == 31) {
+    scratch[warp] = ia;
+    scratch[40 + warp] = ib;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int wa = (lane_id() < NW) ? scratch[lane_id()] : 0;
+    const int wb = (lane_id() < NW) ? scratch[40 + lane_id()] : 0;
+    const int sa = warp_inclusive_scan(wa), sb = warp_inclusive_scan(wb);
+    if (lane_id() < NW) {
+      scratch[lane_id()] = sa - wa;
+      scratch[40 + lane_id()] = sb - wb;
+    }
+    if (lane_id() == NW - 1) {
+      scratch[32] = sa;
+      scratch[72] = sb;
+    }
+  }
+  __syncthreads();
+  *ta = scratch[32];
+  *tb = scratch[72];
+  return make_int2(scratch[warp] + ia - a, scratch[40 + warp] + ib - b);
+}
+
+// Rank masks of tokens [t0, t1) whose ids are staged in sids, L lanes per
+// token (k % L == 0) so that few tokens still keep every warp busy; MASK is
+// uint32_t when R <= 32. masks[t - t0] gets the token's mask. Each warp counts
+// tokens per rank in registers (lane r % 32 holds rank r) and writes them to
+// wrc[warp][R]; no shared atomics. Returns whether an id outside [-1, E) was
+// seen. Every thread of the block must call it.
+template <typename MASK, int L>
+__device__ bool token_masks(const LayoutParams& p, int t0, int t1, const int* sids, const int* rank_of,
+                            MASK* masks, int* wrc) {
+  const int k = p.topk, R = p.num_ranks, E = p.num_experts;
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int lane = (int)lane_id();
+  const int kk = k / L;      // ids per lane
+  const int sub = lane % L;  // this lane's part of the token
+  const int epr = p.experts_per_rank;
+  const bool pow2 = (epr & (epr - 1)) == 0;
+  const int sh = 31 - __clz(epr);
+  const bool vec = (kk & 3) == 0;
+  constexpr int TPW = 32 / L;  // tokens per warp step
+  bool bad = false;
+  int rc0 = 0, rc1 = 0;        // tokens of ranks lane and lane + 32
+  for (int tb = t0 + warp * TPW; tb < t1; tb += nwarps * TPW) {
+    const int t = tb + lane / L;
+    MASK mask = 0;
+    if (t < t1) {
+      const int* ids = sids + (t - t0) * k + sub * kk;
+      for (int j0 = 0; j0 < kk; j0 += 4) {
+        int ev[4];
+        if (vec) {
+          const int4 a = *reinterpret_cast<const int4*>(ids + j0);
+          ev[0] = a.x; ev[1] = a.y; ev[2] = a.z; ev[3] = a.w;
+        } else {
+#pragma unroll
+          for (int b = 0; b < 4; ++b) ev[b] = (j0 + b < kk) ? ids[j0 + b] : -1;
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int e = ev[b];
+          if ((unsigned)(e + 1) > (unsigned)E) bad = true;  // e < -1 or e >= E
+          else if (e >= 0) mask |= (MASK)1 << (pow2 ? (e >> sh) : rank_of[e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) {  // OR over the token's lanes
+      if (sizeof(MASK) == 8) {
+        const unsigned long long m = (unsigned long long)mask;
+        const unsigned lo = __shfl_xor_sync(0xffffffffu, (unsigned)m, o);
+        const unsigned hi = __shfl_xor_sync(0xffffffffu, (unsigned)(m >> 32), o);
+        mask |= (MASK)(((unsigned long long)hi << 32) | lo);
+      } else {
+        mask |= (MASK)__shfl_xor_sync(0xffffffffu, (unsigned)mask, o);
+      }
+    }
+    const bool lead = sub == 0 && t < t1;
+    if (lead) masks[t - t0] = mask;
+    if (!lead) mask = 0;
+    for (int r = 0; r < R; ++r) {
+      const int n = __popc(__ballot_sync(0xffffffffu, (unsigned)(mask >> r) & 1u));
+      if (r == lane) rc0 += n;
+      if (r == lane + 32) rc1 += n;
+    }
+  }
+  if (lane < R) wrc[warp * R + lane] = rc0;
+  if (lane + 32 < R) wrc[warp * R + lane + 32] = rc1;
+  return bad;
+}
+
+// Ranks of the len pairs staged in sids among equal experts inside each
+// warp's contiguous run: whist[w * stride + e] counts the pairs of expert e in
+// warp w's run (rows zeroed by the caller), and sids[q] becomes
+// rank << 11 | (e + 1), or 0 for a pair without an expert. Within a 32-pair
+// step a lane finds its peers by matching the bits of its id with ballots;
+// the steps follow pair order, so ranks are in (t, j) order. Every thread of
+// the block must call it.
+__device__ void warp_ranks(int E, int len, int* sids, int* whist, int stride) {
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const unsigned lane = lane_id();
+  const unsigned lt = (1u << lane) - 1u;
+  const int per = (len + nwarps - 1) / nwarps;
+  const int w0 = per * warp;
+  const int w1 = min(w0 + per, len);
+  const int nb = E > 1 ? 32 - __clz(E - 1) : 0;  // bits of the largest id
+  int* wh = whist + warp * stride;
+  constexpr int S = 4;  // steps of 32 pairs whose masks are built together
+  for (int qb = w0; qb < w1; qb += 32 * S) {
+    int e[S];
+    unsigned m[S];
+#pragma unroll
+    for (int st = 0; st < S; ++st) {
+      const int q = qb + 32 * st + (int)lane;
+      int v = (q < w1) ? sids[q] : -1;
+      if ((unsigned)v >= (unsigned)E) v = -1;
+      e[st] = v;
+      m[st] = __ballot_sync(0xffffffffu, v >= 0);
+    }
+    for (int b = 0; b < nb; ++b) {
+#pragma unroll
+      for (int st = 0; st < S; ++st) {
+        const unsigned bit = ((unsigned)e[st] >> b) & 1u;
+        const unsigned v = __ballot_sync(0xffffffffu, bit);
+        m[st] &= bit ? v : ~v;
+      }
+    }
+#pragma unroll
+    for (int st = 0; st < S; ++st) {  // in pair order: counts carry over
+      const int q = qb + 32 * st + (int)lane;
+      int rank = 0;
+      if (e[st] >= 0) rank = wh[e[st]] + __popc(m[st] & lt);
+      __syncwarp();
+      if (e[st] >= 0 && (m[st] & lt) == 0) wh[e[st]] += __popc(m[st]);
+      __syncwarp();
+      if (q < w1) sids[q] = e[st] >= 0 ? ((rank << 11) | (e[st] + 1)) : 0;
+    }
+  }
+}
+
+// Stores v at the address of local_addr in the shared memory of cluster
+// block `rank`.
+__device__ __forceinline__ void st_cluster_s32(int* local_addr, unsigned rank, int v) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(local_addr);
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
+}
+
+// Shared memory of k_layout_cluster, in ints (MASK words rounded to ints).
+__host__ __device__ inline size_t cluster_smem_ints(int tpb, int k, int E, int R, int G, bool inv,
+                                                    size_t mask_bytes) {
+  const size_t E4 = (size_t)((E + 3) & ~3);
+  return (size_t)kClusterWarps * E4 + (size_t)tpb * k * (inv ? 2 : 1) + tpb * mask_bytes / 4 +
+         (size_t)G * E + (size_t)G * (R + 1) + (size_t)kClusterWarps * R + 4 * (size_t)E + 80;
+}
+
 // Everything in one launch: a cluster of G blocks (G <= 16), block c owning a
-// contiguous run of tokens. Each block stages its ids, counts them (rank mask
-// rows, per-warp histograms), then after a cluster barrier reads the other
-// blocks' counts through distributed shared memory to get the expert totals
-// and its own prefix; one scan gives the offsets, and the block ranks its
-// pairs. No workspace is used except the status word. A final cluster
-// barrier keeps every block's shared memory alive until the others have read
-// it.
-__global__ void __launch_bounds__(kClusterThreads) k_layout_cluster(LayoutParams p, int tokens_per_block) {
+// contiguous run of tokens.
+//  1. The block copies its ids to shared memory (16-byte asynchronous copies)
+//     while it clears its counters.
+//  2. Token pass: each token's rank mask (kept in shared memory) and per-rank
+//     token counts per warp.
+//  3. Pair pass: per-warp expert counts and each pair's rank among its warp's
+//     pairs of the same expert.
+//  4. Per expert, each warp's first offset in the block and the block's
+//     count; the block stores its counts into every cluster block's shared
+//     memory (block 0 also gets the rank counts), then one cluster barrier.
+//     Global stores all come after it, so the barrier's release does not wait
+//     for them, and no block reads another's memory after it, so there is no
+//     closing barrier.
+//  5. From the counts of all blocks: expert totals and this block's prefix;
+//     one block scan gives the expert offsets and, in the same pass, the
+//     offsets of the block's own pairs per expert. Block 0 writes the counts
+//     and offsets.
+//  6. slot_of in pair order and the block's pairs in slot order in shared
+//     memory (inv), then src_of_slot from inv, so both are coalesced stores
+//     (without room for inv, src_of_slot is scattered from step 6).
+// No workspace is used except the status word.
+template <typename MASK, int L>
+__global__ void __launch_bounds__(kClusterThreads)
+    k_layout_cluster(LayoutParams p, int tokens_per_block, int use_inv) {
   pdl_wait();
   pdl_trigger();
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) int smem[];
-  constexpr int NW = kClusterThreads / 32;
+  constexpr int NW = kClusterWarps;
   const int E = p.num_experts, R = p.num_ranks, k = p.topk;
   const int G = (int)cluster.num_blocks();
   const int c = (int)cluster.block_rank();
-  int* sids = smem;                          // [tokens_per_block * k] (a multiple of 4: aligned)
-  int* scratch = sids + tokens_per_block * k;  // 33 (+3 pad)
-  int* cnt = scratch + 36;      // [E] this block's expert counts
-  int* rcnt = cnt + E;          // [R] this block's token-in-rank counts
-  int* flag = rcnt + R;         // [1] invalid ids seen
-  int* base = flag + 1;         // [E]
-  int* rank_of = base + E;      // [E]
-  int* whist = rank_of + E;     // [NW][E]
-  const int t0 = min(c * tokens_per_block, p.num_tokens);
-  const int t1 = min(t0 + tokens_per_block, p.num_tokens);
+  const int tpb = tokens_per_block;  // a multiple of 4: every segment below stays 16-byte aligned
+  const int E4 = (E + 3) & ~3;
+  int* whist = smem;                  // [NW][E4] per-warp expert counts, then offsets
+  int* sids = whist + NW * E4;        // [tpb * k] ids, then packed ranks
+  unsigned* inv = reinterpret_cast<unsigned*>(sids + tpb * k);  // [tpb * k] if use_inv
+  MASK* masks = reinterpret_cast<MASK*>(sids + tpb * k * (use_inv ? 2 : 1));  // [tpb]
+  int* allcnt = reinterpret_cast<int*>(masks + tpb);  // [G][E] every block's expert counts
+  int* allr = allcnt + G * E;         // [G][R + 1] rank counts and invalid-id flag (block 0)
+  int* wrc = allr + G * (R + 1);      // [NW][R] per-warp rank counts
+  int* cnt = wrc + NW * R;            // [E] this block's expert counts
+  int* loff = cnt + E;                // [E] first position of expert e among the block's pairs
+  int* delta = loff + E;              // [E] slot = delta[e] + position
+  int* rank_of = delta + E;           // [E]
+  int* scratch = rank_of + E;         // [80]
+  __shared__ int s_bad;
+  const int t0 = min(c * tpb, p.num_tokens);
+  const int t1 = min(t0 + tpb, p.num_tokens);
   const int64_t p0 = (int64_t)t0 * k;
   const int len = (t1 - t0) * k;
 
-  for (int i = threadIdx.x; i < E + R + 1; i += blockDim.x) cnt[i] = 0;
-  for (int i = threadIdx.x; i < NW * E; i += blockDim.x) whist[i] = 0;
-  fill_rank_of(p, rank_of);
-  __syncthreads();
-  stage_ids(p, p0, p0 + len, sids, flag);
-  __syncthreads();
-  count_tokens<false>(p, t0, t1, sids, rank_of, cnt, rcnt);
-  warp_histograms(E, len, sids, whist, false);  // whist zeroed above; ends with a barrier
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {  // the block's expert counts
-    int v[NW];
-#pragma unroll
-    for (int w = 0; w < NW; ++w) v[w] = whist[w * E + e];
-    int sum = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) sum += v[w];
-    cnt[e] = sum;
-  }
-  cluster.sync();  // every block's cnt/rcnt/flag is final
-
-  // Expert totals and this block's prefix from all blocks' counts. Thread i
-  // owns experts [i*ept, i*ept + ept) (ept <= 2) and issues all its remote
-  // loads together, so the exchange costs one distributed-shared-memory round
-  // trip.
-  const int ept = (E + kClusterThreads - 1) / kClusterThreads;
-  const int e0 = threadIdx.x * ept;
-  int tot[2] = {0, 0}, pre[2] = {0, 0};
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int e = e0 + i;
-    if (i < ept && e < E) {
-      int v[kClusterMaxBlocks];
-#pragma unroll
-      for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(cnt + e, b) : 0;
-#pragma unroll
-      for (int b = 0; b < kClusterMaxBlocks; ++b) {
-        tot[i] += v[b];
-        pre[i] += (b < c) ? v[b] : 0;
+  // 1.
+  {
+    const int32_t* src = p.topk_idx + p0;
+    if ((((uintptr_t)src) & 15) == 0) {
+      const int nv = len / 4;
+      for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        const uint32_t sa = (uint32_t)__cvta_generic_to_shared(sids + 4 * i);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(src + 4 * i) : "memory");
       }
+      for (int i = 4 * nv + threadIdx.x; i < len; i += blockDim.x) sids[i] = src[i];
+    } else {
+      for (int i = threadIdx.x; i < len; i += blockDim.x) sids[i] = src[i];
     }
   }
-  int total;
-  int ex = block_exclusive_scan<kClusterThreads>(tot[0] + tot[1], scratch, &total);
+  for (int i = threadIdx.x; i < NW * E4 / 4; i += blockDim.x)
+    reinterpret_cast<int4*>(whist)[i] = make_int4(0, 0, 0, 0);
+  if (threadIdx.x == 0) s_bad = 0;
+  if (p.experts_per_rank & (p.experts_per_rank - 1)) fill_rank_of(p, rank_of);
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+
+  // 2. (reads the ids that step 3 overwrites: barrier between them)
+  if (token_masks<MASK, L>(p, t0, t1, sids, rank_of, masks, wrc)) s_bad = 1;
+  __syncthreads();
+  // 3.
+  warp_ranks(E, len, sids, whist, E4);
+  __syncthreads();
+
+  // 4.
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const int v = whist[w * E4 + e];
+      whist[w * E4 + e] = run;
+      run += v;
+    }
+    cnt[e] = run;
+    for (int b = 0; b < G; ++b) st_cluster_s32(allcnt + c * E + e, (unsigned)b, run);
+  }
+  for (int r = threadIdx.x; r <= R; r += blockDim.x) {
+    int s = 0;
+    if (r < R) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) s += wrc[w * R + r];
+    } else {
+      s = s_bad;
+    }
+    st_cluster_s32(allr + c * (R + 1) + r, 0u, s);
+  }
+  cluster.sync();  // every block's counts are in the shared memory of the blocks that need them
+
+  // 5.
+  const int ept = (E + kClusterThreads - 1) / kClusterThreads;  // <= 2
+  const int e0 = threadIdx.x * ept;
+  int tot[2] = {0, 0}, pre[2] = {0, 0}, own[2] = {0, 0};
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int e = e0 + i;
     if (i < ept && e < E) {
-      base[e] = ex + pre[i];
+      for (int b = 0; b < G; ++b) {
+        const int v = allcnt[b * E + e];
+        tot[i] += v;
+        pre[i] += (b < c) ? v : 0;
+      }
+      own[i] = cnt[e];
+    }
+  }
+  int total, nvalid;
+  int2 ex = block_exclusive_scan2<kClusterThreads>(tot[0] + tot[1], own[0] + own[1], scratch, &total,
+                                                   &nvalid);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int e = e0 + i;
+    if (i < ept && e < E) {
+      loff[e] = ex.y;
+      delta[e] = ex.x + pre[i] - ex.y;
       if (c == 0) {
         p.tokens_per_expert[e] = tot[i];
-        p.expert_offset[e] = ex;
-        if (e % p.experts_per_rank == 0) p.rank_offset[e / p.experts_per_rank] = ex;
+        p.expert_offset[e] = ex.x;
+        if (e % p.experts_per_rank == 0) p.rank_offset[e / p.experts_per_rank] = ex.x;
       }
-      ex += tot[i];
+      ex.x += tot[i];
+      ex.y += own[i];
     }
   }
   if (c == 0) {
-    for (int r = threadIdx.x; r < R; r += blockDim.x) {
-      int v[kClusterMaxBlocks];
-#pragma unroll
-      for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(rcnt + r, b) : 0;
-      int sum = 0;
-#pragma unroll
-      for (int b = 0; b < kClusterMaxBlocks; ++b) sum += v[b];
-      p.tokens_per_rank[r] = sum;
-    }
-    if (threadIdx.x == 0) {
-      int v[kClusterMaxBlocks];
-#pragma unroll
-      for (int b = 0; b < kClusterMaxBlocks; ++b) v[b] = (b < G) ? *cluster.map_shared_rank(flag, b) : 0;
-      int f = 0;
-#pragma unroll
-      for (int b = 0; b < kClusterMaxBlocks; ++b) f |= v[b];
-      p.expert_offset[E] = total;
-      p.rank_offset[R] = total;
-      *p.status = f ? MOE_ERR_DEVICE_IDS : MOE_OK;
+    for (int r = threadIdx.x; r <= R; r += blockDim.x) {
+      int s = 0;
+      for (int b = 0; b < G; ++b) s = (r < R) ? s + allr[b * (R + 1) + r] : (s | allr[b * (R + 1) + r]);
+      if (r < R) {
+        p.tokens_per_rank[r] = s;
+      } else {
+        p.expert_offset[E] = total;
+        p.rank_offset[R] = total;
+        *p.status = s ? MOE_ERR_DEVICE_IDS : MOE_OK;
+      }
     }
   }
-  __syncthreads();
-  assign_from_histograms<NW>(p, p0, len, sids, base, whist);
+  __syncthreads();  // loff and delta are final
+
+  // 6.
+  {
+    const int warp = threadIdx.x >> 5;
+    const int per = (len + NW - 1) / NW;
+    const int w0 = per * warp;
+    const int w1 = min(w0 + per, len);
+    const int* wh = whist + warp * E4;
+    for (int q = w0 + (int)lane_id(); q < w1; q += 32) {
+      const int v = sids[q];
+      const int e = (v & 2047) - 1;
+      int slot = -1;
+      if (e >= 0) {
+        const int i = loff[e] + wh[e] + (v >> 11);
+        slot = delta[e] + i;
+        if (use_inv) inv[i] = (unsigned)q | ((unsigned)(e + 1) << 21);
+        else if (p.src_of_slot) p.src_of_slot[slot] = (int32_t)(p0 + q);
+      }
+      p.slot_of[p0 + q] = slot;
+    }
+  }
+  {  // is_token_in_rank rows of the block's tokens
+    uint8_t* rows = p.is_token_in_rank + (int64_t)t0 * R;
+    const int nt = t1 - t0;
+    if ((R & 3) == 0 && (((uintptr_t)rows) & 3) == 0) {
+      const int wpr = R >> 2;
+      const bool wp2 = (wpr & (wpr - 1)) == 0;
+      const int ws = 31 - __clz(wpr);
+      for (int i = threadIdx.x; i < nt * wpr; i += blockDim.x) {
+        const int tt = wp2 ? (i >> ws) : (i / wpr);
+        const MASK m = masks[tt] >> ((i - tt * wpr) * 4);
+        reinterpret_cast<uint32_t*>(rows)[i] = (uint32_t)(m & 1) | (uint32_t)((m >> 1) & 1) << 8 |
+                                               (uint32_t)((m >> 2) & 1) << 16 |
+                                               (uint32_t)((m >> 3) & 1) << 24;
+      }
+    } else {
+      for (int i = threadIdx.x; i < nt * R; i += blockDim.x) {
+        const int tt = i / R;
+        rows[i] = (uint8_t)((masks[tt] >> (i - tt * R)) & 1);
+      }
+    }
+  }
+  if (use_inv) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < nvalid; i += blockDim.x) {
+      const unsigned v = inv[i];
+      const int e = (int)(v >> 21) - 1;
+      p.src_of_slot[delta[e] + i] = (int32_t)(p0 + (int)(v & ((1u << 21) - 1)));
+    }
+  }
   clear_src_tail(p, total);
-  cluster.sync();  // no block leaves while another may still read its counts
 }
 
 }  // namespace
@@ -489,25 +751,49 @@ size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks) {
 
 static cudaError_t set_smem(const void* fn, size_t bytes) { return ensure_dynamic_smem(fn, bytes); }
 
-// Cluster plan for a shape: blocks G and tokens per block. Up to 16 blocks
-// where the device schedules a non-portable cluster of 16 (looked up once per
-// device), else 8.
+// The cluster kernel's forms: 32- or 64-bit rank masks, 1, 2 or 4 lanes per
+// token in the token pass.
+static const void* cluster_kernel(bool wide, int lanes) {
+  if (wide) {
+    if (lanes == 4) return (const void*)k_layout_cluster<unsigned long long, 4>;
+    if (lanes == 2) return (const void*)k_layout_cluster<unsigned long long, 2>;
+    return (const void*)k_layout_cluster<unsigned long long, 1>;
+  }
+  if (lanes == 4) return (const void*)k_layout_cluster<uint32_t, 4>;
+  if (lanes == 2) return (const void*)k_layout_cluster<uint32_t, 2>;
+  return (const void*)k_layout_cluster<uint32_t, 1>;
+}
+
+// Cluster plan for a shape: blocks G, tokens per block, lanes per token in
+// the token pass, whether src_of_slot goes through shared memory, and the
+// dynamic shared memory. Up to 16 blocks where the device schedules a
+// non-portable cluster of 16 (looked up once per device), else 8.
 struct ClusterPlan {
-  int blocks, tokens_per_block;
+  int blocks, tokens_per_block, lanes;
+  bool wide, use_inv;
   size_t smem;
 };
 
 static int g_cluster_blocks[64];
 static std::once_flag g_cluster_once[64];
 
+// Allows every form of the cluster kernel the non-portable cluster size and
+// the largest shared memory it may use, then asks whether a cluster of 16
+// fits; once per device.
 static int max_cluster_blocks() {
   int dev = 0, sms = 0;
   if (!current_device(&dev, &sms) || dev >= 64) return kClusterPortableBlocks;
   std::call_once(g_cluster_once[dev], [dev] {
     int best = kClusterPortableBlocks;
-    if (cudaFuncSetAttribute((const void*)k_layout_cluster,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-        ensure_dynamic_smem((const void*)k_layout_cluster, kClusterMaxSmem) == cudaSuccess) {
+    bool ok = true;
+    for (int wide = 0; wide < 2; ++wide) {
+      for (int lanes = 1; lanes <= 4; lanes *= 2) {
+        const void* fn = cluster_kernel(wide != 0, lanes);
+        ok = ok && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+             ensure_dynamic_smem(fn, kClusterMaxSmem) == cudaSuccess;
+      }
+    }
+    if (ok) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(kClusterMaxBlocks);
       cfg.blockDim = dim3(kClusterThreads);
@@ -520,7 +806,7 @@ static int max_cluster_blocks() {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, (const void*)k_layout_cluster, &cfg) == cudaSuccess && n >= 1)
+      if (cudaOccupancyMaxActiveClusters(&n, cluster_kernel(false, 1), &cfg) == cudaSuccess && n >= 1)
         best = kClusterMaxBlocks;
     }
     cudaGetLastError();
@@ -529,7 +815,8 @@ static int max_cluster_blocks() {
   return g_cluster_blocks[dev];
 }
 
-static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int num_ranks, int gmax) {
+static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int num_ranks, bool want_inv,
+                                int gmax) {
   // about kPairsPerClusterBlock pairs per block, but small inputs still
   // spread over up to gmax blocks of at least kMinPairsPerClusterBlock
   const int64_t pairs = (int64_t)num_tokens * topk;
@@ -543,22 +830,29 @@ static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int n
   ClusterPlan cp;
   cp.blocks = g;
   cp.tokens_per_block = tpb;
-  cp.smem = (size_t)(36 + 3 * num_experts + num_ranks + 1 + (kClusterThreads / 32) * num_experts) * 4 +
-            (size_t)tpb * topk * 4;
+  cp.wide = num_ranks > 32;
+  // enough lanes per token that the token pass spreads over the block's warps
+  cp.lanes = (topk % 4 == 0 && tpb * 4 <= kClusterThreads) ? 4
+             : (topk % 2 == 0 && tpb * 2 <= kClusterThreads) ? 2 : 1;
+  const size_t mb = cp.wide ? 8 : 4;
+  cp.use_inv = want_inv &&
+               cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, true, mb) * 4 <= kClusterMaxSmem;
+  cp.smem = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, cp.use_inv, mb) * 4;
   return cp;
 }
 
 cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s) {
   const int E = p.num_experts, R = p.num_ranks;
-  const ClusterPlan cp = cluster_plan(p.num_tokens, p.topk, E, R, max_cluster_blocks());
+  const ClusterPlan cp = cluster_plan(p.num_tokens, p.topk, E, R, p.src_of_slot != nullptr, max_cluster_blocks());
   if (cp.smem <= kClusterMaxSmem) {
-    cudaError_t err = set_smem((const void*)k_layout_cluster, cp.smem);
+    const void* fn = cluster_kernel(cp.wide, cp.lanes);
+    cudaError_t err = set_smem(fn, cp.smem);
     if (err != cudaSuccess) return err;
     LayoutParams q = p;
     int tpb = cp.tokens_per_block;
-    void* args[] = {&q, &tpb};
-    return launch_pdl((const void*)k_layout_cluster, dim3((unsigned)cp.blocks), dim3(kClusterThreads),
-                      cp.smem, s, args, (unsigned)cp.blocks);
+    int use_inv = cp.use_inv ? 1 : 0;
+    void* args[] = {&q, &tpb, &use_inv};
+    return launch_pdl(fn, dim3((unsigned)cp.blocks), dim3(kClusterThreads), cp.smem, s, args, (unsigned)cp.blocks);
   }
   const size_t chunk_ids = (size_t)p.tokens_per_chunk * p.topk;
   const size_t smem_count = (size_t)(2 * E + R + 1) * 4 + chunk_ids * 4;

@@ -79,6 +79,12 @@ def test_rs_sizes(t):
     (33000, 3, 64, 4),
     (100000, 8, 256, 8),   # ids of a cluster block exceed shared memory: two-kernel path
     (90000, 8, 512, 16),   # two-kernel path, larger E
+    (4096, 1, 1, 1),       # one expert, one id a token: the pair pass is shortest here
+    (4096, 1, 2, 2),
+    (8192, 2, 4, 4),
+    (3000, 4, 8, 2),
+    (1000, 5, 128, 64),    # 64-bit rank masks, k not a multiple of 2
+    (777, 3, 120, 12),     # experts per rank not a power of two
 ])
 def test_ragged_and_extreme_shapes(n, k, e, r):
     g = np.random.default_rng(n * 31 + k)
@@ -137,3 +143,21 @@ def test_deterministic_repeat():
     b, _ = run_layout(c["topk_idx"], 256, 16)
     for key in KEYS:
         np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_without_src_of_slot():
+    """src_of_slot is optional: the other outputs are the same without it."""
+    from combine_moe_layout_03_gb300 import moe
+    c = synth.prefill_case(seed=5)
+    ids = c["topk_idx"]
+    d = moe.MoeDesc(ids.shape[0], ids.shape[1], 256, 8, 8)
+    out = moe.layout_outputs(d, DEV)
+    del out["src_of_slot"]
+    out = moe.moe_layout(d, dev_i32(ids), out=out)
+    torch.cuda.synchronize()
+    assert moe.moe_layout_status(out["workspace"]) == moe.MOE_OK
+    ref = oracle.layout(ids, 256, 8)
+    for key in KEYS:
+        if key == "src_of_slot":
+            continue
+        np.testing.assert_array_equal(host(out[key]).reshape(ref[key].shape), ref[key], err_msg=key)
