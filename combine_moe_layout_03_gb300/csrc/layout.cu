@@ -532,7 +532,9 @@ __host__ __device__ inline size_t cluster_smem_ints(int tpb, int k, int E, int R
 }
 
 // Everything in one launch: a cluster of G blocks (G <= 16), block c owning a
-// contiguous run of tokens.
+// contiguous run of tokens. Every block arrives at a first cluster barrier on
+// entry and waits on it before its first remote store, so all blocks have
+// started by then; the exchange below uses a second one.
 //  1. The block copies its ids to shared memory (16-byte asynchronous copies)
 //     while it clears its counters.
 //  2. Token pass: each token's rank mask (kept in shared memory) and per-rank
@@ -558,6 +560,9 @@ __global__ void __launch_bounds__(kClusterThreads)
     k_layout_cluster(LayoutParams p, int tokens_per_block, int use_inv) {
   pdl_wait();
   pdl_trigger();
+  // Remote shared memory may be written only once every block of the cluster
+  // has started: arrive now, wait just before the first remote store.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) int smem[];
@@ -614,6 +619,7 @@ __global__ void __launch_bounds__(kClusterThreads)
   __syncthreads();
 
   // 4.
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every block has started
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
 #pragma unroll
