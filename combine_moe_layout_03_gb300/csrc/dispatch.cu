@@ -155,7 +155,7 @@ __device__ __forceinline__ void quant_nvfp4(const uint8_t* row, int H, uint8_t* 
 // griddepcontrol.wait, overlapping the layout; only slot_of, the layout's
 // output, is read after it.
 template <int OUT_KIND, bool EARLY = false>
-__global__ void __launch_bounds__(kDispatchThreads) k_dispatch(DispatchParams p) {
+__global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch(DispatchParams p) {
   if (!EARLY) {
     pdl_wait();
     pdl_trigger();
