@@ -105,3 +105,30 @@ def test_fused_rejects_bad_dispatch_argument_before_the_layout():
                                     dev_bf16(c["hidden_bf16"]), None, lay, ws, small)()
     torch.cuda.synchronize()
     assert (host(lay["slot_of"]) == 77).all()  # the layout did not run
+
+
+@pytest.mark.parametrize("out_kind,hidden,n", [
+    (oracle.FP8_E4M3_B128, 128, 37),      # one group: a partial wave of one half-warp
+    (oracle.FP8_E4M3_B128, 1152, 300),    # nine groups: a full wave and a partial one
+    (oracle.FP8_E4M3_B128, 7168, 64),
+    (oracle.FP8_E4M3_B128, 16384, 40),    # largest hidden size
+    (oracle.NVFP4_B16, 16, 50),           # one group of 16
+    (oracle.NVFP4_B16, 48, 50),
+    (oracle.NVFP4_B16, 1040, 120),
+    (oracle.NVFP4_B16, 7168, 64),
+    (oracle.NVFP4_B16, 16384, 40),
+    (oracle.FP8_E4M3_UE8M0, 128, 37),
+    (oracle.FP8_E4M3_UE8M0, 7168, 64),
+    (oracle.FP8_E4M3_UE8M0, 16384, 40),
+])
+def test_fused_quantised_rows_every_width(out_kind, hidden, n):
+    """The fused call quantises each row in place in its record image; every
+    record of every width must still equal the oracle's."""
+    c = synth.prefill_case(seed=hidden + n, n=n, hidden=hidden)
+    x = c["hidden_bf16"].copy()
+    x[0] = 0                        # an all-zero row
+    x[1, : min(hidden, 128)] = 0x7F7F  # the largest finite BF16
+    x[2, ::3] = 0x8000               # negative zeros
+    x[3, : min(hidden, 64)] = 0x0001  # subnormals
+    c["hidden_bf16"] = x
+    _check(c, 256, 8, oracle.BF16, out_kind, x, dev_bf16(x))
