@@ -470,8 +470,11 @@ __device__ bool token_masks(const LayoutParams& p, int t0, int t1, const int* si
 // warp w's run (rows zeroed by the caller), and sids[q] becomes
 // rank << 11 | (e + 1), or 0 for a pair without an expert. Within a 32-pair
 // step a lane finds its peers by matching the bits of its id with ballots;
-// the steps follow pair order, so ranks are in (t, j) order. Every thread of
-// the block must call it.
+// the steps follow pair order, so ranks are in (t, j) order. S steps have
+// their ballots interleaved (the caller picks S no larger than a warp's run
+// needs: empty steps would cost their ballots too). Every thread of the
+// block must call it.
+template <int S>
 __device__ void warp_ranks(int E, int len, int* sids, int* whist, int stride) {
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const unsigned lane = lane_id();
@@ -481,7 +484,6 @@ __device__ void warp_ranks(int E, int len, int* sids, int* whist, int stride) {
   const int w1 = min(w0 + per, len);
   const int nb = E > 1 ? 32 - __clz(E - 1) : 0;  // bits of the largest id
   int* wh = whist + warp * stride;
-  constexpr int S = 4;  // steps of 32 pairs whose masks are built together
   for (int qb = w0; qb < w1; qb += 32 * S) {
     int e[S];
     unsigned m[S];
@@ -615,7 +617,15 @@ __global__ void __launch_bounds__(kClusterThreads)
   if (token_masks<MASK, L>(p, t0, t1, sids, rank_of, masks, wrc)) s_bad = 1;
   __syncthreads();
   // 3.
-  warp_ranks(E, len, sids, whist, E4);
+  {
+    const int per = (len + NW - 1) / NW;  // pairs in a warp's run
+    if (per <= 32)
+      warp_ranks<1>(E, len, sids, whist, E4);
+    else if (per <= 64)
+      warp_ranks<2>(E, len, sids, whist, E4);
+    else
+      warp_ranks<4>(E, len, sids, whist, E4);
+  }
   __syncthreads();
 
   // 4.
