@@ -563,8 +563,11 @@ __global__ void __launch_bounds__(kClusterThreads)
   pdl_wait();
   pdl_trigger();
   // Remote shared memory may be written only once every block of the cluster
-  // has started: arrive now, wait just before the first remote store.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  // has started: arrive now, wait just before the first remote store. A
+  // cluster of one block exchanges through its own shared memory and needs
+  // neither cluster barrier.
+  const bool multi = cooperative_groups::this_cluster().num_blocks() > 1;
+  if (multi) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) int smem[];
@@ -629,7 +632,7 @@ __global__ void __launch_bounds__(kClusterThreads)
   __syncthreads();
 
   // 4.
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every block has started
+  if (multi) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every block has started
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
 #pragma unroll
@@ -639,7 +642,11 @@ __global__ void __launch_bounds__(kClusterThreads)
       run += v;
     }
     cnt[e] = run;
-    for (int b = 0; b < G; ++b) st_cluster_s32(allcnt + c * E + e, (unsigned)b, run);
+    if (multi) {
+      for (int b = 0; b < G; ++b) st_cluster_s32(allcnt + c * E + e, (unsigned)b, run);
+    } else {
+      allcnt[e] = run;
+    }
   }
   for (int r = threadIdx.x; r <= R; r += blockDim.x) {
     int s = 0;
@@ -649,9 +656,15 @@ __global__ void __launch_bounds__(kClusterThreads)
     } else {
       s = s_bad;
     }
-    st_cluster_s32(allr + c * (R + 1) + r, 0u, s);
+    if (multi)
+      st_cluster_s32(allr + c * (R + 1) + r, 0u, s);
+    else
+      allr[r] = s;
   }
-  cluster.sync();  // every block's counts are in the shared memory of the blocks that need them
+  if (multi)
+    cluster.sync();  // every block's counts are in the shared memory of the blocks that need them
+  else
+    __syncthreads();
 
   // 5.
   const int ept = (E + kClusterThreads - 1) / kClusterThreads;  // <= 2
