@@ -7,6 +7,7 @@ load time). Rebuilds only when a source or header is newer than the library.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -46,10 +47,21 @@ def needs_build() -> bool:
 
 
 def build_library(force: bool = False, ptxas_verbose: bool = False) -> str:
+    """Builds libmoe.so if a source is newer. Several processes may call it at
+    once (one per rank under torchrun): a file lock lets one compile while the
+    others wait and then find the library up to date."""
     if not force and not needs_build():
         return LIB
-    nvcc = _nvcc()
     os.makedirs(OBJDIR, exist_ok=True)
+    with open(os.path.join(OBJDIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not needs_build():
+            return LIB
+        return _compile_and_link(ptxas_verbose)
+
+
+def _compile_and_link(ptxas_verbose: bool) -> str:
+    nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
 
     def compile_one(src):
@@ -65,7 +77,7 @@ def build_library(force: bool = False, ptxas_verbose: bool = False) -> str:
     if ptxas_verbose:
         for _, log in results:
             print(log)
-    tmp = LIB + ".tmp"
+    tmp = f"{LIB}.{os.getpid()}.tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

@@ -7,6 +7,7 @@ and its binding) never does. All arrays are numpy arrays on the host.
 from __future__ import annotations
 
 import ctypes
+import fcntl
 import os
 import subprocess
 
@@ -26,11 +27,22 @@ def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so with gcc (no fast-math, no FMA
     contraction, no host-specific flags)."""
     newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
-        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-               "-shared", "-Wall", "-o", _LIB + ".tmp", _SRC, "-lm"]
-        subprocess.check_call(cmd)
-        os.replace(_LIB + ".tmp", _LIB)
+
+    def stale():
+        return force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest
+
+    if stale():
+        # processes of a spawned pool may build at once: one compiles, the
+        # others wait on the lock and find the library built
+        with open(_LIB + ".lock", "w") as lock:
+            fcntl.flock(lock, fcntl.LOCK_EX)
+            if stale():
+                tmp = f"{_LIB}.{os.getpid()}.tmp"
+                cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                       "-shared", "-Wall", "-o", tmp, _SRC, "-lm"]
+                subprocess.check_call(cmd)
+                os.replace(tmp, _LIB)
+                force = False
     return _LIB
 
 
