@@ -154,8 +154,11 @@ __device__ __forceinline__ void quant_nvfp4(const uint8_t* row, int H, uint8_t* 
 // rows -- inputs the layout kernel does not write -- happen before
 // griddepcontrol.wait, overlapping the layout; only slot_of, the layout's
 // output, is read after it.
+// Eight resident blocks per SM need at most 32 registers a thread; the NVFP4
+// quantiser would spill there, so it keeps six (40 registers).
 template <int OUT_KIND, bool EARLY = false>
-__global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch(DispatchParams p) {
+__global__ void __launch_bounds__(kDispatchThreads, OUT_KIND == MOE_PAYLOAD_NVFP4_B16 ? 6 : 8)
+    k_dispatch(DispatchParams p) {
   if (!EARLY) {
     pdl_wait();
     pdl_trigger();
