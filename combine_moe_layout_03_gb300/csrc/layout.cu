@@ -516,6 +516,45 @@ __device__ void warp_ranks(int E, int len, int* sids, int* whist, int stride) {
   }
 }
 
+// The same ranks and counts as warp_ranks, with a lane's peers (the lanes of
+// its 32-pair step holding the same expert) found through shared memory
+// instead of ballots: every lane ORs its bit into mb[e] (the warp's row of
+// masks, zero between steps), reads the complete mask back, and the lowest
+// lane of the group adds the group to the count and clears the mask. The OR
+// does not depend on the order of the lanes' atomics, so the result is
+// deterministic; one atomic, one load and one store per pair replace a
+// ballot per bit of the id, which bounds the pass by warp votes otherwise.
+__device__ void warp_ranks_or(int E, int len, int* sids, int* whist, unsigned* mb, int stride) {
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const unsigned lane = lane_id();
+  const unsigned lt = (1u << lane) - 1u;
+  const int per = (len + nwarps - 1) / nwarps;
+  const int w0 = per * warp;
+  const int w1 = min(w0 + per, len);
+  int* wh = whist + warp * stride;
+  unsigned* m = mb + warp * stride;
+  for (int q0 = w0; q0 < w1; q0 += 32) {
+    const int q = q0 + (int)lane;
+    int e = (q < w1) ? sids[q] : -1;
+    if ((unsigned)e >= (unsigned)E) e = -1;
+    if (e >= 0) atomicOr(&m[e], 1u << lane);
+    __syncwarp();
+    unsigned peers = 0;
+    int rank = 0;
+    if (e >= 0) {
+      peers = m[e];
+      rank = wh[e] + __popc(peers & lt);
+    }
+    __syncwarp();
+    if (e >= 0 && (peers & lt) == 0) {  // the group's lowest lane
+      wh[e] += __popc(peers);
+      m[e] = 0u;
+    }
+    __syncwarp();
+    if (q < w1) sids[q] = e >= 0 ? ((rank << 11) | (e + 1)) : 0;
+  }
+}
+
 // Stores v at the address of local_addr in the shared memory of cluster
 // block `rank`.
 __device__ __forceinline__ void st_cluster_s32(int* local_addr, unsigned rank, int v) {
@@ -527,9 +566,10 @@ __device__ __forceinline__ void st_cluster_s32(int* local_addr, unsigned rank, i
 
 // Shared memory of k_layout_cluster, in ints (MASK words rounded to ints).
 __host__ __device__ inline size_t cluster_smem_ints(int tpb, int k, int E, int R, int G, bool inv,
-                                                    size_t mask_bytes) {
+                                                    size_t mask_bytes, bool peer_masks) {
   const size_t E4 = (size_t)((E + 3) & ~3);
-  return (size_t)kClusterWarps * E4 + (size_t)tpb * k * (inv ? 2 : 1) + tpb * mask_bytes / 4 +
+  return (size_t)kClusterWarps * E4 * (peer_masks ? 2 : 1) + (size_t)tpb * k * (inv ? 2 : 1) +
+         tpb * mask_bytes / 4 +
          (size_t)G * E + (size_t)G * (R + 1) + (size_t)kClusterWarps * R + 4 * (size_t)E + 80;
 }
 
@@ -559,7 +599,7 @@ __host__ __device__ inline size_t cluster_smem_ints(int tpb, int k, int E, int R
 // No workspace is used except the status word.
 template <typename MASK, int L>
 __global__ void __launch_bounds__(kClusterThreads)
-    k_layout_cluster(LayoutParams p, int tokens_per_block, int use_inv) {
+    k_layout_cluster(LayoutParams p, int tokens_per_block, int use_inv, int use_or) {
   pdl_wait();
   pdl_trigger();
   // Remote shared memory may be written only once every block of the cluster
@@ -578,7 +618,8 @@ __global__ void __launch_bounds__(kClusterThreads)
   const int tpb = tokens_per_block;  // a multiple of 4: every segment below stays 16-byte aligned
   const int E4 = (E + 3) & ~3;
   int* whist = smem;                  // [NW][E4] per-warp expert counts, then offsets
-  int* sids = whist + NW * E4;        // [tpb * k] ids, then packed ranks
+  unsigned* mb = reinterpret_cast<unsigned*>(whist + NW * E4);  // [NW][E4] peer masks if use_or
+  int* sids = whist + NW * E4 * (use_or ? 2 : 1);  // [tpb * k] ids, then packed ranks
   unsigned* inv = reinterpret_cast<unsigned*>(sids + tpb * k);  // [tpb * k] if use_inv
   MASK* masks = reinterpret_cast<MASK*>(sids + tpb * k * (use_inv ? 2 : 1));  // [tpb]
   int* allcnt = reinterpret_cast<int*>(masks + tpb);  // [G][E] every block's expert counts
@@ -609,8 +650,8 @@ __global__ void __launch_bounds__(kClusterThreads)
       for (int i = threadIdx.x; i < len; i += blockDim.x) sids[i] = src[i];
     }
   }
-  for (int i = threadIdx.x; i < NW * E4 / 4; i += blockDim.x)
-    reinterpret_cast<int4*>(whist)[i] = make_int4(0, 0, 0, 0);
+  for (int i = threadIdx.x; i < NW * E4 * (use_or ? 2 : 1) / 4; i += blockDim.x)
+    reinterpret_cast<int4*>(whist)[i] = make_int4(0, 0, 0, 0);  // counts and peer masks
   if (threadIdx.x == 0) s_bad = 0;
   if (p.experts_per_rank & (p.experts_per_rank - 1)) fill_rank_of(p, rank_of);
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
@@ -622,7 +663,9 @@ __global__ void __launch_bounds__(kClusterThreads)
   // 3.
   {
     const int per = (len + NW - 1) / NW;  // pairs in a warp's run
-    if (per <= 32)
+    if (use_or)
+      warp_ranks_or(E, len, sids, whist, mb, E4);
+    else if (per <= 32)
       warp_ranks<1>(E, len, sids, whist, E4);
     else if (per <= 64)
       warp_ranks<2>(E, len, sids, whist, E4);
@@ -799,7 +842,7 @@ static const void* cluster_kernel(bool wide, int lanes) {
 // non-portable cluster of 16 (looked up once per device), else 8.
 struct ClusterPlan {
   int blocks, tokens_per_block, lanes;
-  bool wide, use_inv;
+  bool wide, use_inv, use_or;
   size_t smem;
 };
 
@@ -864,9 +907,12 @@ static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int n
   cp.lanes = (topk % 4 == 0 && tpb * 4 <= kClusterThreads) ? 4
              : (topk % 2 == 0 && tpb * 2 <= kClusterThreads) ? 2 : 1;
   const size_t mb = cp.wide ? 8 : 4;
-  cp.use_inv = want_inv &&
-               cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, true, mb) * 4 <= kClusterMaxSmem;
-  cp.smem = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, cp.use_inv, mb) * 4;
+  // peer masks in shared memory when they fit, then the inverse map for
+  // coalesced src_of_slot stores when that fits too
+  cp.use_or = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, false, mb, true) * 4 <= kClusterMaxSmem;
+  cp.use_inv = want_inv && cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, true, mb, cp.use_or) * 4 <=
+                               kClusterMaxSmem;
+  cp.smem = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, cp.use_inv, mb, cp.use_or) * 4;
   return cp;
 }
 
@@ -879,8 +925,8 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     LayoutParams q = p;
     int tpb = cp.tokens_per_block;
-    int use_inv = cp.use_inv ? 1 : 0;
-    void* args[] = {&q, &tpb, &use_inv};
+    int use_inv = cp.use_inv ? 1 : 0, use_or = cp.use_or ? 1 : 0;
+    void* args[] = {&q, &tpb, &use_inv, &use_or};
     return launch_pdl(fn, dim3((unsigned)cp.blocks), dim3(kClusterThreads), cp.smem, s, args, (unsigned)cp.blocks);
   }
   const size_t chunk_ids = (size_t)p.tokens_per_chunk * p.topk;
