@@ -582,7 +582,8 @@ __host__ __device__ inline size_t cluster_smem_ints(int tpb, int k, int E, int R
 //  2. Token pass: each token's rank mask (kept in shared memory) and per-rank
 //     token counts per warp.
 //  3. Pair pass: per-warp expert counts and each pair's rank among its warp's
-//     pairs of the same expert.
+//     pairs of the same expert (peer masks through shared-memory atomics, or
+//     ballots where the mask rows do not fit).
 //  4. Per expert, each warp's first offset in the block and the block's
 //     count; the block stores its counts into every cluster block's shared
 //     memory (block 0 also gets the rank counts), then one cluster barrier.
@@ -602,19 +603,19 @@ __global__ void __launch_bounds__(kClusterThreads)
     k_layout_cluster(LayoutParams p, int tokens_per_block, int use_inv, int use_or) {
   pdl_wait();
   pdl_trigger();
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int G = (int)cluster.num_blocks();
+  const int c = (int)cluster.block_rank();
   // Remote shared memory may be written only once every block of the cluster
   // has started: arrive now, wait just before the first remote store. A
   // cluster of one block exchanges through its own shared memory and needs
   // neither cluster barrier.
-  const bool multi = cooperative_groups::this_cluster().num_blocks() > 1;
+  const bool multi = G > 1;
   if (multi) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  namespace cg = cooperative_groups;
-  cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) int smem[];
   constexpr int NW = kClusterWarps;
   const int E = p.num_experts, R = p.num_ranks, k = p.topk;
-  const int G = (int)cluster.num_blocks();
-  const int c = (int)cluster.block_rank();
   const int tpb = tokens_per_block;  // a multiple of 4: every segment below stays 16-byte aligned
   const int E4 = (E + 3) & ~3;
   int* whist = smem;                  // [NW][E4] per-warp expert counts, then offsets
