@@ -581,6 +581,22 @@ def _timed(fn, K, flush, flush_read, stream):
     return statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
 
 
+def _timed_b2b(fns, K, stream):
+    """Mean device time per call of K calls issued back to back (the pages'
+    method: events around many repeats), cycling through fns, which work on
+    separate buffer copies whose total exceeds L2 so that every call reads
+    from DRAM; in microseconds."""
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for i in range(K):
+        fns[i % len(fns)]()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / K
+
+
 def run_decode_sweep(args, rank, world):
     """The decode step at N = 1, 2, 4, ..., 256 tokens (raw NVFP4 payload,
     top-8 of 256, R=8; the combine grouped by rank where N % R == 0): eager
@@ -660,10 +676,29 @@ def run_rs_sweep(args, rank, world):
         us_f = _timed(fused, K, flush, flush_read, stream)
         b_r = (r * n * h + n * h) * 2            # R partials in, the sum out
         b_f = (k * n * h + n * h) * 2 + 12 * k * n  # k rows in, the sum out, pair info
+        # back to back over copies of the inputs and outputs that together
+        # exceed twice the L2
+        copies = max(2, -(-2 * L2_FLUSH_BYTES // min(b_r, b_f)))
+        parts = [part] + [part.clone() for _ in range(copies - 1)]
+        ys = [y] + [y.clone() for _ in range(copies - 1)]
+        outs = [out] + [torch.empty_like(out) for _ in range(copies - 1)]
+        ranks_b = [moe.prepare_combine(d, moe.MOE_COMBINE_RANKS, parts[i], None, None, None, outs[i])
+                   for i in range(copies)]
+        fused_b = [moe.prepare_combine(d, moe.MOE_COMBINE_TOPK_RANKS, ys[i], ids, w, lay["slot_of"], outs[i])
+                   for i in range(copies)]
+        for f in ranks_b + fused_b:
+            f()
+        us_rb = _timed_b2b(ranks_b, K, stream)
+        us_fb = _timed_b2b(fused_b, K, stream)
         rows.append({"tokens_per_rank": t, "out_mib_per_rank": t * h * 2 / 2 ** 20,
                      "rank_sum_us": round(us_r, 2), "rank_sum_frac": round(b_r / us_r / 1e3 / peak, 3),
-                     "topk_ranks_us": round(us_f, 2), "topk_ranks_frac": round(b_f / us_f / 1e3 / peak, 3)})
-        launches += 2 * K
+                     "topk_ranks_us": round(us_f, 2), "topk_ranks_frac": round(b_f / us_f / 1e3 / peak, 3),
+                     "rank_sum_us_back_to_back": round(us_rb, 2),
+                     "rank_sum_frac_back_to_back": round(b_r / us_rb / 1e3 / peak, 3),
+                     "topk_ranks_us_back_to_back": round(us_fb, 2),
+                     "topk_ranks_frac_back_to_back": round(b_f / us_fb / 1e3 / peak, 3)})
+        del parts, ys, outs, ranks_b, fused_b
+        launches += 4 * K
     clk = clocks.stop()
     last = rows[-1]
     return {
@@ -675,7 +710,8 @@ def run_rs_sweep(args, rank, world):
         "config": {"workload": "reduce-scatter sweep: R=4, H=8192, 32..512 tokens per rank; rank sum "
                                "of BF16 partials and top-8 weighted reduction grouped by rank "
                                "(value at 512 tokens per rank, grouped form)",
-                   "l2": "flushed before every timed call"},
+                   "l2": "flushed before every timed call; the back-to-back columns cycle through "
+                         "copies of the inputs larger than twice the L2 instead"},
         "sweep": rows, "gpu_launches": launches, "clocks": clk,
         "pages_context_us": {"0.5": [42.4, 35.6], "1": [43.1, 37.1], "2": [42.3, 37.4],
                              "4": [51.6, 43.5], "8": [84.8, 76.7],
