@@ -834,9 +834,26 @@ def run_ours(args, spec, rank, world):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if getattr(st, "lay", None) is not None and "tokens_per_expert" in st.lay:
+        line["routing"] = routing_stats(st.lay["tokens_per_expert"], st.lay["tokens_per_rank"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, budget_s=args.cpu_seconds)
     return line
+
+
+def routing_stats(tokens_per_expert, tokens_per_rank) -> dict:
+    """Load balance of the first input set's routing, from the layout kernel's
+    own outputs (read once, after the timed steps): pairs per expert (max,
+    mean, max/mean, experts with none) and tokens per rank (max, mean)."""
+    tpe = tokens_per_expert.cpu().numpy().astype(np.float64)
+    tpr = tokens_per_rank.cpu().numpy().astype(np.float64)
+    mean = float(tpe.mean()) if tpe.size else 0.0
+    return {"pairs_per_expert_max": int(tpe.max()) if tpe.size else 0,
+            "pairs_per_expert_mean": round(mean, 2),
+            "expert_load_max_over_mean": round(float(tpe.max()) / mean, 3) if mean > 0 else None,
+            "empty_experts": int((tpe == 0).sum()),
+            "tokens_per_rank_max": int(tpr.max()) if tpr.size else 0,
+            "tokens_per_rank_mean": round(float(tpr.mean()), 2) if tpr.size else 0.0}
 
 
 def measure_e2e(st: Step, spec: dict, dev, K: int, W: int, seed: int = 0) -> dict:

@@ -92,3 +92,17 @@ def test_all_cores_baseline_runs_the_oracle_in_spawned_workers():
     finally:
         pool.close()
     assert done == 64
+
+
+def test_routing_stats_from_layout_counts():
+    """The bench line's load-balance summary of a routing: pairs per expert
+    (max, mean, max/mean, empty experts) and tokens per rank."""
+    import torch
+    import bench
+    got = bench.routing_stats(torch.tensor([0, 5, 3, 0], dtype=torch.int32),
+                              torch.tensor([6, 2], dtype=torch.int32))
+    assert got == {"pairs_per_expert_max": 5, "pairs_per_expert_mean": 2.0,
+                   "expert_load_max_over_mean": 2.5, "empty_experts": 2,
+                   "tokens_per_rank_max": 6, "tokens_per_rank_mean": 4.0}
+    none = bench.routing_stats(torch.zeros(4, dtype=torch.int32), torch.zeros(2, dtype=torch.int32))
+    assert none["expert_load_max_over_mean"] is None and none["empty_experts"] == 4
