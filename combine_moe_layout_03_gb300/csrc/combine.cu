@@ -433,7 +433,11 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   const int chunks = p.hidden_size / 8;
   const int steps_per_token = (chunks + 31) / 32;  // warp steps of 32 chunks
   const int g = p.group_by_rank ? 1 : 0;
-  const int per_unit = steps_per_token < 2 ? steps_per_token : 2;
+  // Units of one step when there is a resident warp for every one (each warp
+  // then waits on one round of expert-row loads instead of two), else two.
+  const int64_t resident_warps = (int64_t)di->sms * di->topk_blocks[g] * kCombineWarps;
+  const int per_unit =
+      steps_per_token < 2 || (int64_t)p.num_tokens * steps_per_token <= resident_warps ? 1 : 2;
   const int chunks_per_unit = per_unit * 32;
   const int units_per_token = (chunks + chunks_per_unit - 1) / chunks_per_unit;
   const int64_t num_units = (int64_t)p.num_tokens * units_per_token;
