@@ -1,0 +1,135 @@
+/* A plain C11 caller of the device path: reads one workload's inputs from
+ * files, allocates device memory with the CUDA runtime, runs moe_layout,
+ * moe_dispatch (BF16 rows to FP8 records) and moe_combine (grouped by rank)
+ * through libmoe.so on the default stream, and writes slot_of, the records
+ * and the combined rows back to files for the test that builds and runs it
+ * (tests/test_gpu_c_consumer.py) to check against the oracle.
+ *   device_path DIR   with DIR/meta.txt = "N k E R H P" and ids.bin, w.bin,
+ *   x.bin (bf16 bits), y.bin (bf16 bits, P rows) */
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "moe.h"
+
+static int fail(const char* what, int code) {
+  fprintf(stderr, "%s failed: %d (%s)\n", what, code, code < 0 ? moe_strerror(code) : "cuda");
+  return 1;
+}
+
+static void* read_file(const char* dir, const char* name, size_t bytes) {
+  char path[1024];
+  snprintf(path, sizeof path, "%s/%s", dir, name);
+  FILE* f = fopen(path, "rb");
+  if (!f) return NULL;
+  void* p = malloc(bytes ? bytes : 1);
+  size_t got = fread(p, 1, bytes, f);
+  fclose(f);
+  if (got != bytes) {
+    free(p);
+    return NULL;
+  }
+  return p;
+}
+
+static int write_file(const char* dir, const char* name, const void* p, size_t bytes) {
+  char path[1024];
+  snprintf(path, sizeof path, "%s/%s", dir, name);
+  FILE* f = fopen(path, "wb");
+  if (!f) return 1;
+  size_t put = fwrite(p, 1, bytes, f);
+  fclose(f);
+  return put != bytes;
+}
+
+#define CUDA(x)                                  \
+  do {                                           \
+    cudaError_t e_ = (x);                        \
+    if (e_ != cudaSuccess) return fail(#x, (int)e_); \
+  } while (0)
+
+int main(int argc, char** argv) {
+  if (argc != 2) return fail("usage: device_path DIR", -1);
+  const char* dir = argv[1];
+  char path[1024];
+  snprintf(path, sizeof path, "%s/meta.txt", dir);
+  FILE* m = fopen(path, "r");
+  if (!m) return fail("meta.txt", -1);
+  int n, k, e, r, h, p;
+  if (fscanf(m, "%d %d %d %d %d %d", &n, &k, &e, &r, &h, &p) != 6) return fail("meta.txt", -1);
+  fclose(m);
+
+  const size_t pairs = (size_t)n * k;
+  int32_t* ids = read_file(dir, "ids.bin", pairs * 4);
+  float* w = read_file(dir, "w.bin", pairs * 4);
+  uint16_t* x = read_file(dir, "x.bin", (size_t)n * h * 2);
+  uint16_t* y = read_file(dir, "y.bin", (size_t)p * h * 2);
+  if (!ids || !w || !x || !y) return fail("input files", -1);
+
+  moe_desc_t d;
+  memset(&d, 0, sizeof d);
+  d.num_tokens = n;
+  d.topk = k;
+  d.num_experts = e;
+  d.num_ranks = r;
+  d.hidden = h;
+  d.in_kind = MOE_PAYLOAD_BF16;
+  d.out_kind = MOE_PAYLOAD_FP8_E4M3_B128;
+  moe_record_layout_t lay;
+  int rc = moe_record_layout(&d, &lay);
+  if (rc) return fail("moe_record_layout", rc);
+  const size_t ws_bytes = moe_workspace_size(&d);
+  const size_t rec_bytes = pairs * (size_t)lay.record_bytes;
+
+  int32_t *d_ids, *d_tpe, *d_tpr, *d_eo, *d_ro, *d_slot, *d_src;
+  uint8_t *d_mask, *d_rec;
+  float* d_w;
+  void *d_x, *d_y, *d_out, *d_ws;
+  CUDA(cudaMalloc((void**)&d_ids, pairs * 4));
+  CUDA(cudaMalloc((void**)&d_w, pairs * 4));
+  CUDA(cudaMalloc(&d_x, (size_t)n * h * 2));
+  CUDA(cudaMalloc(&d_y, (size_t)(p ? p : 1) * h * 2));
+  CUDA(cudaMalloc(&d_out, (size_t)n * h * 2));
+  CUDA(cudaMalloc((void**)&d_tpe, (size_t)e * 4));
+  CUDA(cudaMalloc((void**)&d_tpr, (size_t)r * 4));
+  CUDA(cudaMalloc((void**)&d_mask, (size_t)n * r));
+  CUDA(cudaMalloc((void**)&d_eo, (size_t)(e + 1) * 4));
+  CUDA(cudaMalloc((void**)&d_ro, (size_t)(r + 1) * 4));
+  CUDA(cudaMalloc((void**)&d_slot, pairs * 4));
+  CUDA(cudaMalloc((void**)&d_src, pairs * 4));
+  CUDA(cudaMalloc((void**)&d_rec, rec_bytes));
+  CUDA(cudaMalloc(&d_ws, ws_bytes));
+  CUDA(cudaMemcpy(d_ids, ids, pairs * 4, cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(d_w, w, pairs * 4, cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(d_x, x, (size_t)n * h * 2, cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(d_y, y, (size_t)p * h * 2, cudaMemcpyHostToDevice));
+
+  rc = moe_layout(&d, d_ids, d_tpe, d_tpr, d_mask, d_eo, d_ro, d_slot, d_src, d_ws, ws_bytes, NULL);
+  if (rc) return fail("moe_layout", rc);
+  int32_t status = -100;
+  rc = moe_layout_status(d_ws, &status, NULL);
+  if (rc || status) return fail("moe_layout_status", rc ? rc : status);
+  rc = moe_dispatch(&d, d_ids, d_w, d_x, NULL, d_slot, d_rec, rec_bytes, NULL);
+  if (rc) return fail("moe_dispatch", rc);
+  moe_desc_t dc = d;
+  dc.in_kind = MOE_PAYLOAD_BF16;
+  dc.out_kind = MOE_PAYLOAD_BF16;
+  rc = moe_combine(&dc, MOE_COMBINE_TOPK_RANKS, d_y, (int64_t)p, d_ids, d_w, d_slot, d_out, NULL);
+  if (rc) return fail("moe_combine", rc);
+  CUDA(cudaDeviceSynchronize());
+
+  int32_t* slot = malloc(pairs * 4);
+  uint8_t* rec = malloc((size_t)p * lay.record_bytes + 1);
+  uint16_t* out = malloc((size_t)n * h * 2);
+  CUDA(cudaMemcpy(slot, d_slot, pairs * 4, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(rec, d_rec, (size_t)p * lay.record_bytes, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(out, d_out, (size_t)n * h * 2, cudaMemcpyDeviceToHost));
+  if (write_file(dir, "slot_of.bin", slot, pairs * 4) ||
+      write_file(dir, "records.bin", rec, (size_t)p * lay.record_bytes) ||
+      write_file(dir, "out.bin", out, (size_t)n * h * 2))
+    return fail("output files", -1);
+  printf("ok records=%d record_bytes=%d\n", p, (int)lay.record_bytes);
+  return 0;
+}

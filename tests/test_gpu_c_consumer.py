@@ -1,0 +1,59 @@
+"""The device path from a plain C program: tests/c/device_path.c, built with
+the CUDA toolkit's compiler against include/moe.h and libmoe.so, allocates
+its own device memory, runs moe_layout, moe_dispatch (FP8 records) and
+moe_combine (grouped by rank) on inputs this test writes, and its slot map,
+records and combined rows equal the oracle's."""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from combine_moe_layout_03_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PKG = os.path.join(ROOT, "combine_moe_layout_03_gb300")
+
+
+def test_c_program_runs_the_device_path(tmp_path):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not os.path.exists(nvcc) or cc is None:
+        pytest.skip("no CUDA toolkit or C compiler")
+    cuda = os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    cuda_lib = next(d for d in (os.path.join(cuda, "lib64"), os.path.join(cuda, "lib"))
+                    if os.path.exists(os.path.join(d, "libcudart.so")))
+    from combine_moe_layout_03_gb300 import build
+    build.build_library()
+    exe = str(tmp_path / "device_path")
+    subprocess.check_call([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           "-I", os.path.join(cuda, "include"), os.path.join(ROOT, "tests", "c", "device_path.c"),
+                           "-o", exe, "-L", PKG, "-lmoe", "-L", cuda_lib, "-lcudart",
+                           f"-Wl,-rpath,{PKG}", f"-Wl,-rpath,{cuda_lib}"])
+
+    c = synth.prefill_case(seed=31, n=512, hidden=1024)
+    n, k, e, r, h = 512, 8, 256, 8, 1024
+    ids, w, x = c["topk_idx"], c["topk_weights"], c["hidden_bf16"]
+    lay = oracle.layout(ids, e, r)
+    P = lay["num_pairs"]
+    y = synth.bf16_normal(np.random.default_rng(32), (P, h))
+    d = tmp_path / "io"
+    d.mkdir()
+    (d / "meta.txt").write_text(f"{n} {k} {e} {r} {h} {P}\n")
+    ids.astype(np.int32).tofile(d / "ids.bin")
+    w.astype(np.float32).tofile(d / "w.bin")
+    x.astype(np.uint16).tofile(d / "x.bin")
+    y.astype(np.uint16).tofile(d / "y.bin")
+    run = subprocess.run([exe, str(d)], capture_output=True, text=True)
+    assert run.returncode == 0, run.stderr
+
+    slot = np.fromfile(d / "slot_of.bin", dtype=np.int32).reshape(n, k)
+    np.testing.assert_array_equal(slot, lay["slot_of"])
+    want = oracle.dispatch(ids, w, x, None, lay["slot_of"], P, oracle.BF16, oracle.FP8_E4M3_B128, h)
+    got = np.fromfile(d / "records.bin", dtype=np.uint8).reshape(P, -1)
+    np.testing.assert_array_equal(got, want)
+    out = np.fromfile(d / "out.bin", dtype=np.uint16).reshape(n, h)
+    np.testing.assert_array_equal(out, oracle.combine_topk_ranks(y, ids, w, lay["slot_of"], e, r, h))
