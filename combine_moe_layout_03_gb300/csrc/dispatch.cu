@@ -19,6 +19,8 @@
 // kernel later, so they should not linger dirty in L2 for the next kernel to
 // write back. The token's input is
 // read once and k records are written: the kernel is write-bound.
+#include <cstdlib>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -149,22 +151,167 @@ __device__ __forceinline__ void quant_nvfp4(const uint8_t* row, int H, uint8_t* 
   }
 }
 
-// EARLY (used only right after this library's own layout kernel, in
-// moe_layout_dispatch): the row copy, its quantisation and the id and weight
-// rows -- inputs the layout kernel does not write -- happen before
-// griddepcontrol.wait, overlapping the layout; only slot_of, the layout's
-// output, is read after it.
-// Eight resident blocks per SM need at most 32 registers a thread; the NVFP4
-// quantiser would spill there, so it keeps six (40 registers).
-template <int OUT_KIND, bool EARLY = false>
-__global__ void __launch_bounds__(kDispatchThreads, OUT_KIND == MOE_PAYLOAD_NVFP4_B16 ? 6 : 8)
-    k_dispatch(DispatchParams p) {
-  if (!EARLY) {
+// Routing layout of a small routing (N*k <= kFusedMaxPairs) computed inside
+// the dispatch kernel, so that a decode-sized moe_layout_dispatch is one
+// launch. Every block reads all N*k ids (at most 2 KB, from L2 after the
+// first block) while its token row is still in flight, and builds two expert
+// histograms in shared memory: all pairs, and the pairs of tokens before its
+// own. One block scan of the first gives the expert offsets, so pair j of
+// token t goes to
+//   slot = expert_offset[e] + (pairs of earlier tokens with expert e)
+//          + (j' < j of token t with expert e)
+// -- the stable counting sort of the layout, computed per block with no
+// grid-wide exchange. Block 0 also writes the global outputs (counts,
+// offsets, tokens per rank, the status word); each block writes its token's
+// slot_of row, is_token_in_rank row and src_of_slot entries, and a share of
+// the src_of_slot tail (-1 beyond P). Ids outside [-1, E) count as -1 and
+// raise the status word, as in the layout kernels. Above 512 pairs the
+// redundant per-block histograms cost more than the separate layout kernel
+// (whose run the dispatch's row loads overlap) and the two kernels are used.
+constexpr int kFusedMaxPairs = 512;
+constexpr int kFusedPairsPerThread = kFusedMaxPairs / kDispatchThreads;
+constexpr int kFusedExpertsPerThread = (MOE_MAX_EXPERTS + kDispatchThreads - 1) / kDispatchThreads;
+constexpr int kFusedScratch = 48;  // block scan scratch [0, 33); [47] invalid-id flag
+
+// ints of shared memory before the block-0 mask array (kept even, so the
+// 64-bit masks that follow stay 8-byte aligned)
+__host__ __device__ __forceinline__ int fused_hist_ints(int E, int R) {
+  return (2 * E + R + kFusedScratch + 1) & ~1;
+}
+
+__device__ void fused_layout(const LayoutParams& lp, int t, const int* own_ids, int* hist,
+                             int* s_slot, int64_t capacity) {
+  constexpr int NT = kDispatchThreads;
+  const int N = lp.num_tokens, k = lp.topk, E = lp.num_experts, R = lp.num_ranks;
+  const int El = lp.experts_per_rank;
+  const int NK = N * k;
+  const int tid = threadIdx.x;
+  const bool lead = blockIdx.x == 0;
+  int* hall = hist;          // [E] pairs per expert, then the expert offsets
+  int* hbef = hist + E;      // [E] pairs per expert among tokens before t
+  int* trank = hbef + E;     // [R] tokens per rank (block 0)
+  int* scratch = trank + R;  // [kFusedScratch]
+  unsigned long long* masks = reinterpret_cast<unsigned long long*>(hist + fused_hist_ints(E, R));
+
+  // every id load in flight at once
+  int ev[kFusedPairsPerThread];
+#pragma unroll
+  for (int i = 0; i < kFusedPairsPerThread; ++i) {
+    const int q = tid + i * NT;
+    ev[i] = q < NK ? lp.topk_idx[q] : -1;
+  }
+  for (int i = tid; i < 2 * E + R; i += NT) hist[i] = 0;
+  if (lead)
+    for (int u = tid; u < N; u += NT) masks[u] = 0ull;
+  if (tid == 0) scratch[kFusedScratch - 1] = 0;
+  __syncthreads();
+
+  bool bad = false;
+  const int before = t * k;
+#pragma unroll
+  for (int i = 0; i < kFusedPairsPerThread; ++i) {
+    const int q = tid + i * NT;
+    const int e = ev[i];
+    if (e < -1 || e >= E) {
+      bad = true;
+    } else if (e >= 0) {
+      atomicAdd(&hall[e], 1);
+      if (q < before) atomicAdd(&hbef[e], 1);
+      if (lead) atomicOr(&masks[q / k], 1ull << (e / El));
+    }
+  }
+  if (bad) scratch[kFusedScratch - 1] = 1;
+  __syncthreads();
+
+  if (lead) {
+    for (int u = tid; u < N; u += NT) {
+      unsigned long long m = masks[u];
+      while (m) {
+        atomicAdd(&trank[__ffsll((long long)m) - 1], 1);
+        m &= m - 1;
+      }
+    }
+  }
+  // expert offsets: thread tid owns experts [tid*m, tid*m + m)
+  const int m = (E + NT - 1) / NT;
+  int c[kFusedExpertsPerThread];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < kFusedExpertsPerThread; ++i) {
+    const int e = tid * m + i;
+    c[i] = (i < m && e < E) ? hall[e] : 0;
+    sum += c[i];
+  }
+  int P = 0;
+  int ex = block_exclusive_scan<NT>(sum, scratch, &P);  // ends with a barrier
+#pragma unroll
+  for (int i = 0; i < kFusedExpertsPerThread; ++i) {
+    const int e = tid * m + i;
+    if (i < m && e < E) {
+      if (lead) {
+        lp.tokens_per_expert[e] = c[i];
+        lp.expert_offset[e] = ex;
+        if (e % El == 0) lp.rank_offset[e / El] = ex;
+      }
+      hall[e] = ex;
+      ex += c[i];
+    }
+  }
+  if (lead) {
+    if (tid < R) lp.tokens_per_rank[tid] = trank[tid];
+    if (tid == 0) {
+      lp.expert_offset[E] = P;
+      lp.rank_offset[R] = P;
+      *lp.status = scratch[kFusedScratch - 1] ? MOE_ERR_DEVICE_IDS : MOE_OK;
+    }
+  }
+  __syncthreads();
+
+  if (tid < k) {
+    const int j = tid;
+    const int e = own_ids[j];
+    int s = -1;
+    if (e >= 0 && e < E) {
+      s = hall[e] + hbef[e];
+      for (int jj = 0; jj < j; ++jj) s += own_ids[jj] == e;
+    }
+    lp.slot_of[(int64_t)t * k + j] = s;
+    if (lp.src_of_slot && s >= 0) lp.src_of_slot[s] = t * k + j;
+    s_slot[j] = (s >= 0 && (int64_t)s < capacity) ? s : -1;
+  }
+  if (tid < R) {
+    bool in = false;
+    for (int jj = 0; jj < k; ++jj) {
+      const int e = own_ids[jj];
+      in |= e >= 0 && e < E && e / El == tid;
+    }
+    lp.is_token_in_rank[(int64_t)t * R + tid] = in ? 1 : 0;
+  }
+  if (lp.src_of_slot)
+    for (int s = P + blockIdx.x * NT + tid; s < NK; s += gridDim.x * NT) lp.src_of_slot[s] = -1;
+}
+
+// How a dispatch block learns its slots:
+//  kSlotsAfterWait  read slot_of after griddepcontrol.wait (moe_dispatch);
+//  kSlotsEarly      only right after this library's own layout kernel (in
+//                   moe_layout_dispatch): the row copy, its quantisation and
+//                   the id and weight rows -- inputs the layout kernel does
+//                   not write -- happen before griddepcontrol.wait,
+//                   overlapping the layout; only slot_of, the layout's
+//                   output, is read after it;
+//  kSlotsFused      computed in the block (fused_layout) while the row copy
+//                   is in flight (moe_layout_dispatch of a small routing).
+constexpr int kSlotsAfterWait = 0, kSlotsEarly = 1, kSlotsFused = 2;
+
+template <int OUT_KIND, int SLOTS>
+__device__ __forceinline__ void dispatch_token(const DispatchParams& p, const LayoutParams* lp) {
+  if (SLOTS != kSlotsEarly) {
     pdl_wait();
     pdl_trigger();
   }
   // Dynamic shared memory: the record body (record bytes [16, record_bytes)),
-  // then, for the quantising kinds, the staged BF16 input row.
+  // then, for the quantising kinds, the staged BF16 input row, then (fused
+  // layout) the histograms.
   extern __shared__ __align__(128) uint8_t img[];
   __shared__ int s_slot[MOE_MAX_TOPK];
   __shared__ int s_expert[MOE_MAX_TOPK];
@@ -190,7 +337,7 @@ __global__ void __launch_bounds__(kDispatchThreads, OUT_KIND == MOE_PAYLOAD_NVFP
   // slots, ids and weights of this token
   if (threadIdx.x < k) {
     const int64_t q = (int64_t)t * k + threadIdx.x;
-    if (!EARLY) {
+    if (SLOTS == kSlotsAfterWait) {
       const int s = p.slot_of[q];
       s_slot[threadIdx.x] = (s >= 0 && (int64_t)s < p.record_capacity) ? s : -1;
     }
@@ -204,6 +351,11 @@ __global__ void __launch_bounds__(kDispatchThreads, OUT_KIND == MOE_PAYLOAD_NVFP
   zero_bytes(img, op + p.payload_bytes, os);
   zero_bytes(img, os + p.scale_bytes, body);
 
+  if (SLOTS == kSlotsFused) {
+    const int hist_off = (body + (kQuant ? p.in_row_bytes : 0) + 15) & ~15;
+    fused_layout(*lp, t, s_expert, reinterpret_cast<int*>(img + hist_off), s_slot, p.record_capacity);
+  }
+
   cp_async_wait_all();
   __syncthreads();
   if (OUT_KIND == MOE_PAYLOAD_FP8_E4M3_B128) {
@@ -215,7 +367,7 @@ __global__ void __launch_bounds__(kDispatchThreads, OUT_KIND == MOE_PAYLOAD_NVFP
   }
 
   fence_proxy_async_smem();
-  if (EARLY) {
+  if (SLOTS == kSlotsEarly) {
     pdl_wait();  // the layout has completed: slot_of is final
     pdl_trigger();
     if (threadIdx.x < k) {
@@ -236,6 +388,21 @@ __global__ void __launch_bounds__(kDispatchThreads, OUT_KIND == MOE_PAYLOAD_NVFP
       bulk_wait_read_all();
     }
   }
+}
+
+// Eight resident blocks per SM need at most 32 registers a thread; the NVFP4
+// quantiser would spill there, so it keeps six (40 registers).
+template <int OUT_KIND, bool EARLY = false>
+__global__ void __launch_bounds__(kDispatchThreads, OUT_KIND == MOE_PAYLOAD_NVFP4_B16 ? 6 : 8)
+    k_dispatch(DispatchParams p) {
+  dispatch_token<OUT_KIND, EARLY ? kSlotsEarly : kSlotsAfterWait>(p, nullptr);
+}
+
+// Layout and dispatch of a small routing in one launch (decode sizes: at most
+// kFusedMaxPairs pairs, so at most that many blocks).
+template <int OUT_KIND>
+__global__ void __launch_bounds__(kDispatchThreads, 4) k_layout_dispatch_small(DispatchParams p, LayoutParams lp) {
+  dispatch_token<OUT_KIND, kSlotsFused>(p, &lp);
 }
 
 // One record per (token, destination rank) instead of per (token, expert)
@@ -412,6 +579,45 @@ cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, 
   if (err != cudaSuccess) return err;
   DispatchParams q = p;
   void* args[] = {&q};
+  return launch_pdl(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), smem, s, args);
+}
+
+namespace {
+size_t layout_dispatch_small_smem(const DispatchParams& p, int out_kind, int num_experts, int num_ranks) {
+  const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16 ||
+                     out_kind == MOE_PAYLOAD_FP8_E4M3_UE8M0;
+  const size_t hist_off = ((size_t)(p.record_bytes - 16) + (quant ? (size_t)p.in_row_bytes : 0) + 15) & ~(size_t)15;
+  return hist_off + 4 * (size_t)fused_hist_ints(num_experts, num_ranks) + 8 * (size_t)p.num_tokens;
+}
+constexpr size_t kFusedMaxSmem = 200 * 1024;
+}  // namespace
+
+bool layout_dispatch_small_fits(const DispatchParams& p, int out_kind, int num_experts, int num_ranks) {
+  static const bool on = [] {
+    const char* v = getenv("MOE_FUSED_LAYOUT");
+    return !(v && v[0] == '0' && v[1] == '\0');
+  }();
+  return on && p.num_tokens > 0 && (int64_t)p.num_tokens * p.topk <= kFusedMaxPairs &&
+         num_experts <= MOE_MAX_EXPERTS &&
+         layout_dispatch_small_smem(p, out_kind, num_experts, num_ranks) <= kFusedMaxSmem;
+}
+
+cudaError_t launch_layout_dispatch_small(const DispatchParams& p, const LayoutParams& lp, int out_kind,
+                                         cudaStream_t s) {
+  const size_t smem = layout_dispatch_small_smem(p, out_kind, lp.num_experts, lp.num_ranks);
+  const void* fn = nullptr;
+  switch (out_kind) {
+    case MOE_PAYLOAD_BF16: fn = (const void*)k_layout_dispatch_small<MOE_PAYLOAD_BF16>; break;
+    case MOE_PAYLOAD_FP8_E4M3_B128: fn = (const void*)k_layout_dispatch_small<MOE_PAYLOAD_FP8_E4M3_B128>; break;
+    case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_layout_dispatch_small<MOE_PAYLOAD_NVFP4_B16>; break;
+    case MOE_PAYLOAD_FP8_E4M3_UE8M0: fn = (const void*)k_layout_dispatch_small<MOE_PAYLOAD_FP8_E4M3_UE8M0>; break;
+    default: fn = (const void*)k_layout_dispatch_small<MOE_PAYLOAD_RAW>; break;
+  }
+  cudaError_t err = ensure_dynamic_smem(fn, smem);
+  if (err != cudaSuccess) return err;
+  DispatchParams q = p;
+  LayoutParams l = lp;
+  void* args[] = {&q, &l};
   return launch_pdl(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), smem, s, args);
 }
 

@@ -168,6 +168,48 @@ int record_layout(const moe_desc_t* d, moe_record_layout_t* o) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Validates moe_layout's arguments and fills its launch parameters (also
+// for num_tokens == 0, when only the counts and the status word are written).
+int layout_params(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* tokens_per_expert,
+                  int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
+                  int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot, void* workspace,
+                  size_t ws_bytes, moe::LayoutParams* p) {
+  int rc = check_desc(desc);
+  if (rc != MOE_OK) return rc;
+  const int N = desc->num_tokens, E = desc->num_experts, R = desc->num_ranks;
+  if (!tokens_per_expert || !tokens_per_rank || !expert_offset || !rank_offset || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!topk_idx || !is_token_in_rank || !slot_of)) return MOE_ERR_INVALID_ARG;
+  const void* ints[] = {topk_idx, tokens_per_expert, tokens_per_rank, expert_offset,
+                        rank_offset, slot_of, src_of_slot};
+  for (const void* q : ints)
+    if (!aligned(q, 4)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(workspace, 256)) return MOE_ERR_ALIGNMENT;
+  const size_t need = moe::layout_workspace_bytes(N, E, R);
+  if (ws_bytes < need) return MOE_ERR_CAPACITY;
+  uint8_t* ws = (uint8_t*)workspace;
+  p->topk_idx = topk_idx;
+  p->tokens_per_expert = tokens_per_expert;
+  p->tokens_per_rank = tokens_per_rank;
+  p->is_token_in_rank = is_token_in_rank;
+  p->expert_offset = expert_offset;
+  p->rank_offset = rank_offset;
+  p->slot_of = slot_of;
+  p->src_of_slot = src_of_slot;
+  p->num_tokens = N;
+  p->topk = desc->topk;
+  p->num_experts = E;
+  p->num_ranks = R;
+  p->experts_per_rank = E / R;
+  p->tokens_per_chunk = moe::kLayoutTokensPerChunk;
+  p->num_chunks = (N + moe::kLayoutTokensPerChunk - 1) / moe::kLayoutTokensPerChunk;
+  p->status = (int32_t*)ws;
+  p->chunk_hist = (int32_t*)(ws + 256);
+  p->chunk_rank = p->chunk_hist + (size_t)p->num_chunks * E;
+  p->chunk_flag = p->chunk_rank + (size_t)p->num_chunks * R;
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -200,50 +242,20 @@ int moe_layout(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* tokens_
                int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
                int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot, void* workspace,
                size_t ws_bytes, moe_stream_t stream) {
-  int rc = check_desc(desc);
+  moe::LayoutParams p;
+  int rc = layout_params(desc, topk_idx, tokens_per_expert, tokens_per_rank, is_token_in_rank,
+                         expert_offset, rank_offset, slot_of, src_of_slot, workspace, ws_bytes, &p);
   if (rc != MOE_OK) return rc;
-  const int N = desc->num_tokens, E = desc->num_experts, R = desc->num_ranks;
-  if (!tokens_per_expert || !tokens_per_rank || !expert_offset || !rank_offset || !workspace)
-    return MOE_ERR_INVALID_ARG;
-  if (N > 0 && (!topk_idx || !is_token_in_rank || !slot_of)) return MOE_ERR_INVALID_ARG;
-  const void* ints[] = {topk_idx, tokens_per_expert, tokens_per_rank, expert_offset,
-                        rank_offset, slot_of, src_of_slot};
-  for (const void* q : ints)
-    if (!aligned(q, 4)) return MOE_ERR_ALIGNMENT;
-  if (!aligned(workspace, 256)) return MOE_ERR_ALIGNMENT;
-  const size_t need = moe::layout_workspace_bytes(N, E, R);
-  if (ws_bytes < need) return MOE_ERR_CAPACITY;
   cudaStream_t s = (cudaStream_t)stream;
-
-  uint8_t* ws = (uint8_t*)workspace;
-  if (N == 0) {  // nothing routed: zero counts and offsets
+  if (p.num_tokens == 0) {  // nothing routed: zero counts and offsets
+    const int E = p.num_experts, R = p.num_ranks;
     cudaError_t e = cudaMemsetAsync(tokens_per_expert, 0, (size_t)E * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(tokens_per_rank, 0, (size_t)R * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(expert_offset, 0, (size_t)(E + 1) * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(rank_offset, 0, (size_t)(R + 1) * 4, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, 4, s);  // status = MOE_OK
+    if (e == cudaSuccess) e = cudaMemsetAsync(p.status, 0, 4, s);  // status = MOE_OK
     return cuda_status(e);
   }
-  moe::LayoutParams p;
-  p.topk_idx = topk_idx;
-  p.tokens_per_expert = tokens_per_expert;
-  p.tokens_per_rank = tokens_per_rank;
-  p.is_token_in_rank = is_token_in_rank;
-  p.expert_offset = expert_offset;
-  p.rank_offset = rank_offset;
-  p.slot_of = slot_of;
-  p.src_of_slot = src_of_slot;
-  p.num_tokens = N;
-  p.topk = desc->topk;
-  p.num_experts = E;
-  p.num_ranks = R;
-  p.experts_per_rank = E / R;
-  p.tokens_per_chunk = moe::kLayoutTokensPerChunk;
-  p.num_chunks = (N + moe::kLayoutTokensPerChunk - 1) / moe::kLayoutTokensPerChunk;
-  p.status = (int32_t*)ws;
-  p.chunk_hist = (int32_t*)(ws + 256);
-  p.chunk_rank = p.chunk_hist + (size_t)p.num_chunks * E;
-  p.chunk_flag = p.chunk_rank + (size_t)p.num_chunks * R;
   return cuda_status(moe::launch_layout(p, s));
 }
 
@@ -329,6 +341,13 @@ int moe_layout_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const f
   int rc = dispatch_params(desc, topk_idx, topk_weights, hidden, scales, slot_of, records,
                            records_bytes, &p, &empty);
   if (rc != MOE_OK) return rc;
+  if (!empty && moe::layout_dispatch_small_fits(p, desc->out_kind, desc->num_experts, desc->num_ranks)) {
+    moe::LayoutParams lp;
+    rc = layout_params(desc, topk_idx, tokens_per_expert, tokens_per_rank, is_token_in_rank,
+                       expert_offset, rank_offset, slot_of, src_of_slot, workspace, ws_bytes, &lp);
+    if (rc != MOE_OK) return rc;
+    return cuda_status(moe::launch_layout_dispatch_small(p, lp, desc->out_kind, (cudaStream_t)stream));
+  }
   rc = moe_layout(desc, topk_idx, tokens_per_expert, tokens_per_rank, is_token_in_rank,
                   expert_offset, rank_offset, slot_of, src_of_slot, workspace, ws_bytes, stream);
   if (rc != MOE_OK || empty) return rc;

@@ -212,9 +212,13 @@ int moe_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* t
  * is then known to be this call's own layout kernel, which writes none of
  * the dispatch's inputs, the dispatch loads and quantises its token rows
  * while the layout still runs and reads only slot_of after it (programmatic
- * dependent launch; with MOE_PDL=0 the two run in plain order). Arguments are
- * those of the two calls; all of them are checked before anything is
- * launched. Errors: as moe_layout and moe_dispatch. */
+ * dependent launch; with MOE_PDL=0 the two run in plain order). A routing of
+ * at most 512 pairs (N*k; decode batches up to 64 tokens of top-8) runs as a
+ * single kernel instead, each of whose blocks computes the layout from all
+ * ids while its token row loads (MOE_FUSED_LAYOUT=0 in the environment keeps
+ * the two kernels). Arguments are those of the two calls; all of them are
+ * checked before anything is launched. Errors: as moe_layout and
+ * moe_dispatch. */
 int moe_layout_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* topk_weights,
                         const void* hidden, const void* scales, int32_t* tokens_per_expert,
                         int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
