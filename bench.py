@@ -244,6 +244,13 @@ def layout_launches(n: int, k: int, e: int, r: int) -> int:
     return 1 if smem <= 200 * 1024 else 2
 
 
+def single_kernel_layout_dispatch(n: int, k: int, e: int) -> bool:
+    """Whether moe_layout_dispatch runs as one kernel (a routing of at most
+    512 pairs; MOE_FUSED_LAYOUT=0 turns it off). Mirrors dispatch.cu; the
+    shared-memory bound there holds for every workload here."""
+    return os.environ.get("MOE_FUSED_LAYOUT") != "0" and 0 < n * k <= 512 and e <= 1024
+
+
 class Step:
     """Resident buffers and the three calls of one step."""
 
@@ -314,6 +321,8 @@ class Step:
         # overlaps the layout (the breakdown loop times the two separately)
         self.layout_dispatch = moe.prepare_layout_dispatch(self.desc, self.ids, self.w, self.x, self.sc,
                                                            self.lay, self.ws, self.records)
+        if single_kernel_layout_dispatch(n, k, e):
+            self.launches_per_step = 1 + 1
         if spec.get("norm"):
             from combine_moe_layout_03_gb300 import synth
             self.residual = torch.from_numpy(synth.bf16_normal(synth.rng_for(seed, 12), (n, h))
