@@ -245,10 +245,16 @@ def layout_launches(n: int, k: int, e: int, r: int) -> int:
 
 
 def single_kernel_layout_dispatch(n: int, k: int, e: int) -> bool:
-    """Whether moe_layout_dispatch runs as one kernel (a routing of at most
-    512 pairs; MOE_FUSED_LAYOUT=0 turns it off). Mirrors dispatch.cu; the
-    shared-memory bound there holds for every workload here."""
-    return os.environ.get("MOE_FUSED_LAYOUT") != "0" and 0 < n * k <= 512 and e <= 1024
+    """Whether moe_layout_dispatch runs as one kernel: a routing of at most
+    2048 pairs, or of MOE_FUSED_LAYOUT=p pairs (at most 2048; 0 turns it off).
+    Mirrors dispatch.cu; the shared-memory bound there holds for every
+    workload here."""
+    v = os.environ.get("MOE_FUSED_LAYOUT")
+    try:
+        limit = 2048 if not v else min(max(int(v), 0), 2048)
+    except ValueError:
+        limit = 0
+    return 0 < n * k <= limit and e <= 1024
 
 
 class Step:
@@ -797,6 +803,23 @@ def run_ours(args, spec, rank, world):
     achieved = {name: bpt[name] * n / (kern[name] / 1e3) / 1e9 if kern[name] > 0 else 0.0
                 for name in kern}
     step_bytes = sum(bpt.values()) * n
+    # where layout and dispatch run as one kernel, that call alone as well
+    single = None
+    if getattr(st, "layout_dispatch", None) is not None and \
+            single_kernel_layout_dispatch(n, spec["topk"], spec["num_experts"]):
+        es = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            flush_read.sum()
+            es[i][0].record(stream)
+            sets[i % S].layout_dispatch()
+            es[i][1].record(stream)
+        torch.cuda.synchronize()
+        t1 = statistics.mean(es[i][0].elapsed_time(es[i][1]) for i in range(K))
+        gbs = (bpt["layout"] + bpt["dispatch"]) * n / (t1 / 1e3) / 1e9
+        single = {"kernel": "k_layout_dispatch_small", "us": round(t1 * 1e3, 2), "gbs": round(gbs, 1),
+                  "frac": round(gbs / peaks["hbm_gbs"], 4),
+                  "traffic": recorded_traffic("layout_dispatch_small", spec["name"])}
     # the three timed calls under their own names (the backward step's are
     # the cached handle, combine backward and dispatch backward)
     label = dict(zip(("layout", "dispatch", "combine"),
@@ -841,6 +864,8 @@ def run_ours(args, spec, rank, world):
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
+    if single is not None:
+        line["layout_dispatch_one_kernel"] = single
     if e2e is not None:
         line["e2e"] = e2e
     if getattr(st, "lay", None) is not None and "tokens_per_expert" in st.lay:

@@ -151,47 +151,41 @@ __device__ __forceinline__ void quant_nvfp4(const uint8_t* row, int H, uint8_t* 
   }
 }
 
-// Routing layout of a small routing (N*k <= kFusedMaxPairs) computed inside
-// the dispatch kernel, so that a decode-sized moe_layout_dispatch is one
-// launch. Every block reads all N*k ids (at most 2 KB, from L2 after the
-// first block) while its token row is still in flight, and builds two expert
-// histograms in shared memory: all pairs, and the pairs of tokens before its
-// own. One block scan of the first gives the expert offsets, so pair j of
-// token t goes to
+// Routing layout of a small routing computed inside the dispatch kernel, so
+// that a decode-sized moe_layout_dispatch is one launch. Every block reads
+// all N*k ids (a few KB, from L2 after the first block) while its token row
+// is still in flight, keeps them in shared memory and builds two expert
+// histograms there: all pairs, and the pairs of tokens before its own. One
+// block scan of the first gives the expert offsets, so pair j of token t goes
+// to
 //   slot = expert_offset[e] + (pairs of earlier tokens with expert e)
 //          + (j' < j of token t with expert e)
 // -- the stable counting sort of the layout, computed per block with no
-// grid-wide exchange. Block 0 also writes the global outputs (counts,
-// offsets, tokens per rank, the status word); each block writes its token's
-// slot_of row, is_token_in_rank row and src_of_slot entries, and a share of
-// the src_of_slot tail (-1 beyond P). Ids outside [-1, E) count as -1 and
-// raise the status word, as in the layout kernels. Above 512 pairs the
-// redundant per-block histograms cost more than the separate layout kernel
-// (whose run the dispatch's row loads overlap) and the two kernels are used.
-constexpr int kFusedMaxPairs = 512;
+// grid-wide exchange. Block 0 writes the expert counts and offsets and the
+// status word; block b counts the tokens of ranks b, b + N, ... (one barrier
+// count per rank); each block writes its token's slot_of row,
+// is_token_in_rank row and src_of_slot entries, and a share of the
+// src_of_slot tail (-1 beyond P). Ids outside [-1, E) count as -1 and raise
+// the status word, as in the layout kernels.
+constexpr int kFusedMaxPairs = 2048;      // what the kernel can take
+constexpr int kFusedDefaultPairs = 2048;  // where the host sends it by default
 constexpr int kFusedPairsPerThread = kFusedMaxPairs / kDispatchThreads;
 constexpr int kFusedExpertsPerThread = (MOE_MAX_EXPERTS + kDispatchThreads - 1) / kDispatchThreads;
 constexpr int kFusedScratch = 48;  // block scan scratch [0, 33); [47] invalid-id flag
 
-// ints of shared memory before the block-0 mask array (kept even, so the
-// 64-bit masks that follow stay 8-byte aligned)
-__host__ __device__ __forceinline__ int fused_hist_ints(int E, int R) {
-  return (2 * E + R + kFusedScratch + 1) & ~1;
-}
+// shared ints before the staged ids: the two histograms and the scratch
+__host__ __device__ __forceinline__ int fused_hist_ints(int E) { return 2 * E + kFusedScratch; }
 
-__device__ void fused_layout(const LayoutParams& lp, int t, const int* own_ids, int* hist,
-                             int* s_slot, int64_t capacity) {
+__device__ void fused_layout(const LayoutParams& lp, int t, int* hist, int* s_slot, int64_t capacity) {
   constexpr int NT = kDispatchThreads;
   const int N = lp.num_tokens, k = lp.topk, E = lp.num_experts, R = lp.num_ranks;
   const int El = lp.experts_per_rank;
   const int NK = N * k;
   const int tid = threadIdx.x;
-  const bool lead = blockIdx.x == 0;
-  int* hall = hist;          // [E] pairs per expert, then the expert offsets
-  int* hbef = hist + E;      // [E] pairs per expert among tokens before t
-  int* trank = hbef + E;     // [R] tokens per rank (block 0)
-  int* scratch = trank + R;  // [kFusedScratch]
-  unsigned long long* masks = reinterpret_cast<unsigned long long*>(hist + fused_hist_ints(E, R));
+  int* hall = hist;              // [E] pairs per expert, then the expert offsets
+  int* hbef = hist + E;          // [E] pairs per expert among tokens before t
+  int* scratch = hbef + E;       // [kFusedScratch]
+  int* sids = scratch + kFusedScratch;  // [NK] ids, invalid ones as -1
 
   // every id load in flight at once
   int ev[kFusedPairsPerThread];
@@ -200,9 +194,7 @@ __device__ void fused_layout(const LayoutParams& lp, int t, const int* own_ids, 
     const int q = tid + i * NT;
     ev[i] = q < NK ? lp.topk_idx[q] : -1;
   }
-  for (int i = tid; i < 2 * E + R; i += NT) hist[i] = 0;
-  if (lead)
-    for (int u = tid; u < N; u += NT) masks[u] = 0ull;
+  for (int i = tid; i < 2 * E; i += NT) hist[i] = 0;
   if (tid == 0) scratch[kFusedScratch - 1] = 0;
   __syncthreads();
 
@@ -211,27 +203,43 @@ __device__ void fused_layout(const LayoutParams& lp, int t, const int* own_ids, 
 #pragma unroll
   for (int i = 0; i < kFusedPairsPerThread; ++i) {
     const int q = tid + i * NT;
-    const int e = ev[i];
+    int e = ev[i];
     if (e < -1 || e >= E) {
       bad = true;
+      e = -1;
     } else if (e >= 0) {
       atomicAdd(&hall[e], 1);
       if (q < before) atomicAdd(&hbef[e], 1);
-      if (lead) atomicOr(&masks[q / k], 1ull << (e / El));
     }
+    if (q < NK) sids[q] = e;
   }
   if (bad) scratch[kFusedScratch - 1] = 1;
   __syncthreads();
 
-  if (lead) {
-    for (int u = tid; u < N; u += NT) {
-      unsigned long long m = masks[u];
-      while (m) {
-        atomicAdd(&trank[__ffsll((long long)m) - 1], 1);
-        m &= m - 1;
+  // ranks b, b + N, ...: tokens with a pair on the rank. With more tokens
+  // than threads N > NT > R, so such a block has one rank.
+  if ((int)blockIdx.x < R) {
+    int total = 0;
+    for (int ub = 0; ub < N; ub += NT) {
+      const int u = ub + tid;
+      unsigned long long mask = 0ull;
+      if (u < N)
+        for (int j = 0; j < k; ++j) {
+          const int e = sids[u * k + j];
+          if (e >= 0) mask |= 1ull << (e / El);
+        }
+      for (int r = blockIdx.x; r < R; r += N) {
+        const int c = __syncthreads_count((int)((mask >> r) & 1ull));
+        if (N <= NT) {
+          if (tid == 0) lp.tokens_per_rank[r] = c;
+        } else {
+          total += c;
+        }
       }
     }
+    if (N > NT && tid == 0) lp.tokens_per_rank[blockIdx.x] = total;
   }
+
   // expert offsets: thread tid owns experts [tid*m, tid*m + m)
   const int m = (E + NT - 1) / NT;
   int c[kFusedExpertsPerThread];
@@ -244,6 +252,7 @@ __device__ void fused_layout(const LayoutParams& lp, int t, const int* own_ids, 
   }
   int P = 0;
   int ex = block_exclusive_scan<NT>(sum, scratch, &P);  // ends with a barrier
+  const bool lead = blockIdx.x == 0;
 #pragma unroll
   for (int i = 0; i < kFusedExpertsPerThread; ++i) {
     const int e = tid * m + i;
@@ -257,23 +266,20 @@ __device__ void fused_layout(const LayoutParams& lp, int t, const int* own_ids, 
       ex += c[i];
     }
   }
-  if (lead) {
-    if (tid < R) lp.tokens_per_rank[tid] = trank[tid];
-    if (tid == 0) {
-      lp.expert_offset[E] = P;
-      lp.rank_offset[R] = P;
-      *lp.status = scratch[kFusedScratch - 1] ? MOE_ERR_DEVICE_IDS : MOE_OK;
-    }
+  if (lead && tid == 0) {
+    lp.expert_offset[E] = P;
+    lp.rank_offset[R] = P;
+    *lp.status = scratch[kFusedScratch - 1] ? MOE_ERR_DEVICE_IDS : MOE_OK;
   }
   __syncthreads();
 
   if (tid < k) {
     const int j = tid;
-    const int e = own_ids[j];
+    const int e = sids[t * k + j];
     int s = -1;
-    if (e >= 0 && e < E) {
+    if (e >= 0) {
       s = hall[e] + hbef[e];
-      for (int jj = 0; jj < j; ++jj) s += own_ids[jj] == e;
+      for (int jj = 0; jj < j; ++jj) s += sids[t * k + jj] == e;
     }
     lp.slot_of[(int64_t)t * k + j] = s;
     if (lp.src_of_slot && s >= 0) lp.src_of_slot[s] = t * k + j;
@@ -282,8 +288,8 @@ __device__ void fused_layout(const LayoutParams& lp, int t, const int* own_ids, 
   if (tid < R) {
     bool in = false;
     for (int jj = 0; jj < k; ++jj) {
-      const int e = own_ids[jj];
-      in |= e >= 0 && e < E && e / El == tid;
+      const int e = sids[t * k + jj];
+      in |= e >= 0 && e / El == tid;
     }
     lp.is_token_in_rank[(int64_t)t * R + tid] = in ? 1 : 0;
   }
@@ -353,7 +359,7 @@ __device__ __forceinline__ void dispatch_token(const DispatchParams& p, const La
 
   if (SLOTS == kSlotsFused) {
     const int hist_off = (body + (kQuant ? p.in_row_bytes : 0) + 15) & ~15;
-    fused_layout(*lp, t, s_expert, reinterpret_cast<int*>(img + hist_off), s_slot, p.record_capacity);
+    fused_layout(*lp, t, reinterpret_cast<int*>(img + hist_off), s_slot, p.record_capacity);
   }
 
   cp_async_wait_all();
@@ -583,28 +589,33 @@ cudaError_t launch_dispatch(const DispatchParams& p, int in_kind, int out_kind, 
 }
 
 namespace {
-size_t layout_dispatch_small_smem(const DispatchParams& p, int out_kind, int num_experts, int num_ranks) {
+size_t layout_dispatch_small_smem(const DispatchParams& p, int out_kind, int num_experts) {
   const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16 ||
                      out_kind == MOE_PAYLOAD_FP8_E4M3_UE8M0;
   const size_t hist_off = ((size_t)(p.record_bytes - 16) + (quant ? (size_t)p.in_row_bytes : 0) + 15) & ~(size_t)15;
-  return hist_off + 4 * (size_t)fused_hist_ints(num_experts, num_ranks) + 8 * (size_t)p.num_tokens;
+  return hist_off + 4 * ((size_t)fused_hist_ints(num_experts) + (size_t)p.num_tokens * p.topk);
+}
+// the pair limit: kFusedDefaultPairs, or MOE_FUSED_LAYOUT=n (0 = never, at most kFusedMaxPairs)
+int fused_pair_limit() {
+  static const int limit = [] {
+    const char* v = getenv("MOE_FUSED_LAYOUT");
+    if (!v || !*v) return kFusedDefaultPairs;
+    const long n = strtol(v, nullptr, 10);
+    return (int)(n < 0 ? 0 : n > kFusedMaxPairs ? kFusedMaxPairs : n);
+  }();
+  return limit;
 }
 constexpr size_t kFusedMaxSmem = 200 * 1024;
 }  // namespace
 
-bool layout_dispatch_small_fits(const DispatchParams& p, int out_kind, int num_experts, int num_ranks) {
-  static const bool on = [] {
-    const char* v = getenv("MOE_FUSED_LAYOUT");
-    return !(v && v[0] == '0' && v[1] == '\0');
-  }();
-  return on && p.num_tokens > 0 && (int64_t)p.num_tokens * p.topk <= kFusedMaxPairs &&
-         num_experts <= MOE_MAX_EXPERTS &&
-         layout_dispatch_small_smem(p, out_kind, num_experts, num_ranks) <= kFusedMaxSmem;
+bool layout_dispatch_small_fits(const DispatchParams& p, int out_kind, int num_experts) {
+  return p.num_tokens > 0 && (int64_t)p.num_tokens * p.topk <= fused_pair_limit() &&
+         num_experts <= MOE_MAX_EXPERTS && layout_dispatch_small_smem(p, out_kind, num_experts) <= kFusedMaxSmem;
 }
 
 cudaError_t launch_layout_dispatch_small(const DispatchParams& p, const LayoutParams& lp, int out_kind,
                                          cudaStream_t s) {
-  const size_t smem = layout_dispatch_small_smem(p, out_kind, lp.num_experts, lp.num_ranks);
+  const size_t smem = layout_dispatch_small_smem(p, out_kind, lp.num_experts);
   const void* fn = nullptr;
   switch (out_kind) {
     case MOE_PAYLOAD_BF16: fn = (const void*)k_layout_dispatch_small<MOE_PAYLOAD_BF16>; break;

@@ -341,7 +341,7 @@ int moe_layout_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const f
   int rc = dispatch_params(desc, topk_idx, topk_weights, hidden, scales, slot_of, records,
                            records_bytes, &p, &empty);
   if (rc != MOE_OK) return rc;
-  if (!empty && moe::layout_dispatch_small_fits(p, desc->out_kind, desc->num_experts, desc->num_ranks)) {
+  if (!empty && moe::layout_dispatch_small_fits(p, desc->out_kind, desc->num_experts)) {
     moe::LayoutParams lp;
     rc = layout_params(desc, topk_idx, tokens_per_expert, tokens_per_rank, is_token_in_rank,
                        expert_offset, rank_offset, slot_of, src_of_slot, workspace, ws_bytes, &lp);

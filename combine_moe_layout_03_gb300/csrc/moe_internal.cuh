@@ -166,10 +166,11 @@ cudaError_t launch_slots(bool pack, const void* const* src, void* const* dst,
                          const moe_slot_desc_t* d, const int64_t* offsets, int64_t slot_bytes,
                          cudaStream_t s);
 cudaError_t launch_rank_layout(const RankLayoutParams& p, cudaStream_t s);
-// moe_layout_dispatch of a small routing (at most 512 pairs) as one kernel
+// moe_layout_dispatch of a small routing (at most 2048 pairs) as one kernel
 // that computes the layout in every block; fits() says whether it applies
-// (and MOE_FUSED_LAYOUT=0 in the environment turns it off).
-bool layout_dispatch_small_fits(const DispatchParams& p, int out_kind, int num_experts, int num_ranks);
+// (MOE_FUSED_LAYOUT=n in the environment lowers the pair limit; 0 turns the
+// kernel off).
+bool layout_dispatch_small_fits(const DispatchParams& p, int out_kind, int num_experts);
 cudaError_t launch_layout_dispatch_small(const DispatchParams& p, const LayoutParams& lp, int out_kind,
                                          cudaStream_t s);
 cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const int32_t* send_head,

@@ -213,10 +213,10 @@ int moe_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* t
  * the dispatch's inputs, the dispatch loads and quantises its token rows
  * while the layout still runs and reads only slot_of after it (programmatic
  * dependent launch; with MOE_PDL=0 the two run in plain order). A routing of
- * at most 512 pairs (N*k; decode batches up to 64 tokens of top-8) runs as a
- * single kernel instead, each of whose blocks computes the layout from all
+ * at most 2048 pairs (N*k; decode batches up to 256 tokens of top-8) runs as
+ * a single kernel instead, each of whose blocks computes the layout from all
  * ids while its token row loads (MOE_FUSED_LAYOUT=0 in the environment keeps
- * the two kernels). Arguments are those of the two calls; all of them are
+ * the two kernels; MOE_FUSED_LAYOUT=p lowers the limit to p pairs). Arguments are those of the two calls; all of them are
  * checked before anything is launched. Errors: as moe_layout and
  * moe_dispatch. */
 int moe_layout_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const float* topk_weights,

@@ -56,10 +56,10 @@ def test_workload_bytes_and_launch_counts():
     assert s["bytes_per_token"]["combine"] == k * 2 * h + 12 * k + 2 * h
     assert bench.layout_launches(4096, 8, 256, 8) == 1
     assert bench.layout_launches(100000, 8, 256, 8) == 2  # beyond the cluster's shared memory
-    # layout and dispatch as one kernel up to 512 pairs (tiny, decode N <= 64)
+    # layout and dispatch as one kernel up to 2048 pairs (tiny, decode N <= 256)
     assert bench.single_kernel_layout_dispatch(128, 2, 16)
-    assert bench.single_kernel_layout_dispatch(64, 8, 256)
-    assert not bench.single_kernel_layout_dispatch(65, 8, 256)
+    assert bench.single_kernel_layout_dispatch(256, 8, 256)
+    assert not bench.single_kernel_layout_dispatch(257, 8, 256)
     assert not bench.single_kernel_layout_dispatch(4096, 8, 256)
     sn = bench.workload_spec("prefill_norm")
     assert sn["bytes_per_token"]["combine"] == s["bytes_per_token"]["combine"] + 4 * h

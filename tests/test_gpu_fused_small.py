@@ -1,8 +1,8 @@
-"""moe_layout_dispatch of a small routing (at most 512 pairs: decode up to
-64 tokens of top-8) runs as one kernel that computes the layout inside every
+"""moe_layout_dispatch of a small routing (at most 2048 pairs: decode up to
+256 tokens of top-8) runs as one kernel that computes the layout inside every
 dispatch block. Its outputs -- every layout array including the -1 tail of
 src_of_slot, the status word and the records -- equal the oracle's bit for
-bit, on both sides of the 512-pair limit (above it the call runs the
+bit, on both sides of the 2048-pair limit (above it the call runs the
 cluster layout kernel and the dispatch), for padding, duplicate and invalid
 ids, up to 64 ranks and 1024 experts, and every payload format."""
 import numpy as np
@@ -68,14 +68,15 @@ def test_decode_sweep_raw(n):
 
 
 @pytest.mark.parametrize("n,k,e,r", [
-    (512, 1, 64, 8),      # exactly 512 pairs: one kernel
-    (513, 1, 64, 8),      # one pair more: layout kernel + dispatch
-    (170, 3, 96, 6),      # 510 pairs
-    (171, 3, 96, 6),      # 513 pairs
-    (64, 8, 1024, 64),    # the most experts and ranks
-    (16, 32, 1024, 64),   # the largest k
-    (100, 5, 64, 64),     # one expert per rank
-    (512, 1, 1, 1),       # every pair on one expert
+    (2048, 1, 64, 8),     # exactly 2048 pairs: one kernel, 8 token chunks per block
+    (2049, 1, 64, 8),     # one pair more: layout kernel + dispatch
+    (682, 3, 96, 6),      # 2046 pairs
+    (683, 3, 96, 6),      # 2049 pairs
+    (256, 8, 1024, 64),   # the most experts and ranks
+    (64, 32, 1024, 64),   # the largest k
+    (300, 5, 64, 64),     # one expert per rank
+    (2048, 1, 1, 1),      # every pair on one expert
+    (3, 8, 256, 64),      # fewer tokens than ranks: blocks count several ranks
     (7, 32, 40, 4),
 ])
 def test_limit_and_shapes(n, k, e, r):
@@ -129,10 +130,10 @@ def test_same_as_two_calls():
     """The one-kernel form and moe_layout + moe_dispatch agree bit for bit,
     without src_of_slot as well."""
     from combine_moe_layout_03_gb300 import moe
-    c = synth.decode_case(seed=5, n=60)
+    c = synth.decode_case(seed=5, n=200)
     ids_d, w_d = dev_i32(c["topk_idx"]), dev_f32(c["topk_weights"])
     x, sc = dev_u8(c["payload"]), dev_u8(c["scales"])
-    d = moe.MoeDesc(60, 8, 256, 8, 7168, oracle.RAW, oracle.RAW, c["payload"].shape[1],
+    d = moe.MoeDesc(200, 8, 256, 8, 7168, oracle.RAW, oracle.RAW, c["payload"].shape[1],
                     c["scales"].shape[1])
     lay = moe.moe_layout(d, ids_d)
     rec = moe.moe_dispatch(d, ids_d, w_d, x, sc, lay["slot_of"])
