@@ -388,6 +388,7 @@ namespace {
 struct DeviceInfo {
   int sms = 0;
   int topk_blocks[2] = {0, 0};
+  int rows128_blocks = 0;  // resident 128-thread blocks of the plain row kernel
 };
 DeviceInfo g_info[64];
 std::once_flag g_info_once[64];
@@ -405,6 +406,12 @@ const DeviceInfo* device_info() {
     }
     d.topk_blocks[0] = b0 > 0 ? b0 : 1;
     d.topk_blocks[1] = b1 > 0 ? b1 : 1;
+    int b2 = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, k_combine_rows<false, 128>, 128, 0) != cudaSuccess) {
+      cudaGetLastError();
+      b2 = 0;
+    }
+    d.rows128_blocks = b2;
     d.sms = sms;
   });
   return d.sms > 0 ? &d : nullptr;
@@ -420,12 +427,17 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   // ordering per 64 chunks), keeps every SM busy.
   // The rank-grouped form keeps two fp32 accumulators per element: its
   // 128-thread blocks (twice as many per SM) measured 5% faster at N=4096
-  // and 11% at N=1024 than 256-thread ones; the plain form keeps 256.
+  // and 11% at N=1024 than 256-thread ones.
   if (p.num_tokens >= di->sms * 3) {
     CombineParams q = p;
     void* args[] = {&q};
     if (p.group_by_rank)
       return launch_pdl((const void*)k_combine_rows<true, 128>, dim3((unsigned)p.num_tokens), dim3(128), 0,
+                        s, args);
+    // The plain form takes 128-thread blocks too while that puts every row in
+    // one wave (N=1024: 27.7 -> 27.0 us), else 256.
+    if (p.num_tokens <= (int64_t)di->sms * di->rows128_blocks)
+      return launch_pdl((const void*)k_combine_rows<false, 128>, dim3((unsigned)p.num_tokens), dim3(128), 0,
                         s, args);
     return launch_pdl((const void*)k_combine_rows<false>, dim3((unsigned)p.num_tokens), dim3(kRowThreads),
                       0, s, args);
