@@ -1,9 +1,10 @@
 /* A plain C11 caller of the device path: reads one workload's inputs from
  * files, allocates device memory with the CUDA runtime, runs moe_layout,
  * moe_dispatch (BF16 rows to FP8 records) and moe_combine (grouped by rank)
- * through libmoe.so on the default stream, and writes slot_of, the records
- * and the combined rows back to files for the test that builds and runs it
- * (tests/test_gpu_c_consumer.py) to check against the oracle.
+ * through libmoe.so on the default stream, then moe_layout_dispatch on the
+ * first 128 tokens (layout and dispatch in one kernel), and writes slot_of,
+ * the records and the combined rows back to files for the test that builds
+ * and runs it (tests/test_gpu_c_consumer.py) to check against the oracle.
  *   device_path DIR   with DIR/meta.txt = "N k E R H P" and ids.bin, w.bin,
  *   x.bin (bf16 bits), y.bin (bf16 bits, P rows) */
 #include <cuda_runtime.h>
@@ -83,8 +84,8 @@ int main(int argc, char** argv) {
   const size_t ws_bytes = moe_workspace_size(&d);
   const size_t rec_bytes = pairs * (size_t)lay.record_bytes;
 
-  int32_t *d_ids, *d_tpe, *d_tpr, *d_eo, *d_ro, *d_slot, *d_src;
-  uint8_t *d_mask, *d_rec;
+  int32_t *d_ids, *d_tpe, *d_tpr, *d_eo, *d_ro, *d_slot, *d_slot2, *d_src;
+  uint8_t *d_mask, *d_rec, *d_rec2;
   float* d_w;
   void *d_x, *d_y, *d_out, *d_ws;
   CUDA(cudaMalloc((void**)&d_ids, pairs * 4));
@@ -98,8 +99,10 @@ int main(int argc, char** argv) {
   CUDA(cudaMalloc((void**)&d_eo, (size_t)(e + 1) * 4));
   CUDA(cudaMalloc((void**)&d_ro, (size_t)(r + 1) * 4));
   CUDA(cudaMalloc((void**)&d_slot, pairs * 4));
+  CUDA(cudaMalloc((void**)&d_slot2, pairs * 4));
   CUDA(cudaMalloc((void**)&d_src, pairs * 4));
   CUDA(cudaMalloc((void**)&d_rec, rec_bytes));
+  CUDA(cudaMalloc((void**)&d_rec2, rec_bytes));
   CUDA(cudaMalloc(&d_ws, ws_bytes));
   CUDA(cudaMemcpy(d_ids, ids, pairs * 4, cudaMemcpyHostToDevice));
   CUDA(cudaMemcpy(d_w, w, pairs * 4, cudaMemcpyHostToDevice));
@@ -129,6 +132,25 @@ int main(int argc, char** argv) {
   if (write_file(dir, "slot_of.bin", slot, pairs * 4) ||
       write_file(dir, "records.bin", rec, (size_t)p * lay.record_bytes) ||
       write_file(dir, "out.bin", out, (size_t)n * h * 2))
+    return fail("output files", -1);
+
+  /* The one-call form on the first n_small tokens: at most 2048 pairs, so
+     layout and dispatch run as one kernel. */
+  const int n_small = n < 128 ? n : 128;
+  moe_desc_t ds = d;
+  ds.num_tokens = n_small;
+  const size_t small_pairs = (size_t)n_small * k;
+  const size_t small_rec = (small_pairs < (size_t)p ? small_pairs : (size_t)p) * lay.record_bytes;
+  rc = moe_layout_dispatch(&ds, d_ids, d_w, d_x, NULL, d_tpe, d_tpr, d_mask, d_eo, d_ro, d_slot2, d_src, d_ws,
+                           ws_bytes, d_rec2, rec_bytes, NULL);
+  if (rc) return fail("moe_layout_dispatch", rc);
+  status = -100;
+  rc = moe_layout_status(d_ws, &status, NULL);
+  if (rc || status) return fail("moe_layout_status (one call)", rc ? rc : status);
+  CUDA(cudaMemcpy(slot, d_slot2, small_pairs * 4, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(rec, d_rec2, small_rec, cudaMemcpyDeviceToHost));
+  if (write_file(dir, "slot_of_small.bin", slot, small_pairs * 4) ||
+      write_file(dir, "records_small.bin", rec, small_rec))
     return fail("output files", -1);
   printf("ok records=%d record_bytes=%d\n", p, (int)lay.record_bytes);
   return 0;

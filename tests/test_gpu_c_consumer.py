@@ -57,3 +57,13 @@ def test_c_program_runs_the_device_path(tmp_path):
     np.testing.assert_array_equal(got, want)
     out = np.fromfile(d / "out.bin", dtype=np.uint16).reshape(n, h)
     np.testing.assert_array_equal(out, oracle.combine_topk_ranks(y, ids, w, lay["slot_of"], e, r, h))
+    # the one-call form on the first 128 tokens (layout and dispatch in one kernel)
+    ns = 128
+    lay_s = oracle.layout(ids[:ns], e, r)
+    ps = lay_s["num_pairs"]
+    slot_s = np.fromfile(d / "slot_of_small.bin", dtype=np.int32).reshape(ns, k)
+    np.testing.assert_array_equal(slot_s, lay_s["slot_of"])
+    want_s = oracle.dispatch(ids[:ns], w[:ns], x[:ns], None, lay_s["slot_of"], ps, oracle.BF16,
+                             oracle.FP8_E4M3_B128, h)
+    got_s = np.fromfile(d / "records_small.bin", dtype=np.uint8).reshape(-1, got.shape[1])
+    np.testing.assert_array_equal(got_s[:ps], want_s)
