@@ -819,7 +819,8 @@ def run_ours(args, spec, rank, world):
         gbs = (bpt["layout"] + bpt["dispatch"]) * n / (t1 / 1e3) / 1e9
         single = {"kernel": "k_layout_dispatch_small", "us": round(t1 * 1e3, 2), "gbs": round(gbs, 1),
                   "frac": round(gbs / peaks["hbm_gbs"], 4),
-                  "traffic": recorded_traffic("layout_dispatch_small", spec["name"])}
+                  "traffic": None if spec.get("tokens_overridden")
+                  else recorded_traffic("layout_dispatch_small", spec["name"])}
     # the three timed calls under their own names (the backward step's are
     # the cached handle, combine backward and dispatch backward)
     label = dict(zip(("layout", "dispatch", "combine"),
@@ -849,7 +850,7 @@ def run_ours(args, spec, rank, world):
         "roofline": {"bound": "hbm", "kernel": label[dom], "achieved": round(achieved[dom], 1),
                      "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(achieved[dom] / peaks["hbm_gbs"], 4),
-                     "traffic": recorded_traffic(label[dom], spec["name"]),
+                     "traffic": None if spec.get("tokens_overridden") else recorded_traffic(label[dom], spec["name"]),
                      "algorithmic_bytes_per_launch": bpt[dom] * n},
         "kernels_us": {label[name]: round(v * 1e3, 2) for name, v in kern.items()},
         "kernels_gbs": {label[name]: round(v, 1) for name, v in achieved.items()},
@@ -1192,10 +1193,19 @@ def main(argv=None):
     ap.add_argument("--seeds", type=int, default=5,
                     help="seeded input sets the timed steps cycle through")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override N (a multiple of the workload's ranks; prefill, skewed, decode and "
+                         "rs workloads), e.g. for a smaller profiling case; such a line carries no traffic")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     special = {"ag_slots": run_ag_slots, "decode_sweep": run_decode_sweep, "rs_sweep": run_rs_sweep}
     spec = workload_spec(args.workload) if args.workload not in special else None
+    if args.tokens:
+        if spec is None or spec["name"] in ("tiny", "decode_ll") or args.tokens % spec["num_ranks"]:
+            raise SystemExit("--tokens needs a prefill, skewed, decode or rs workload and a multiple of its ranks")
+        spec["num_tokens"] = args.tokens
+        spec["tokens_overridden"] = True
+        spec["text"] += f" (N overridden to {args.tokens})"
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

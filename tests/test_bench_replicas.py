@@ -111,3 +111,11 @@ def test_routing_stats_from_layout_counts():
                    "tokens_per_rank_max": 6, "tokens_per_rank_mean": 4.0}
     none = bench.routing_stats(torch.zeros(4, dtype=torch.int32), torch.zeros(2, dtype=torch.int32))
     assert none["expert_load_max_over_mean"] is None and none["empty_experts"] == 4
+
+
+def test_tokens_override_is_checked():
+    """--tokens takes only workloads with a free N, and a multiple of their ranks."""
+    with pytest.raises(SystemExit):
+        bench.main(["--workload", "tiny", "--tokens", "64"])
+    with pytest.raises(SystemExit):
+        bench.main(["--workload", "skewed", "--tokens", "1000"])  # R = 16
