@@ -30,7 +30,9 @@ std::mutex g_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_layout_scratch on the current device, looked up once
-// per device (the host-side name of the array is not a device address).
+// per device (the host-side name of the array is not a device address) and
+// kept for the life of the process: a cudaDeviceReset while the library is
+// loaded would leave a stale address here, so it is not supported.
 int scratch_on_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {

@@ -268,7 +268,10 @@ int moe_combine(const moe_desc_t* desc, int mode, const void* expert_out, int64_
  * E = 256, R = 8 that allows N up to about 253,000 tokens.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. Every call shares the one array and overwrites
+ * before any stream capture. The address is kept for the life of the process:
+ * resetting a device (cudaDeviceReset) while the library is loaded is not
+ * supported, since the next call would use the old context's address.
+ * Every call shares the one array and overwrites
  * what it reads, so nothing needs clearing, but calls that overlap on the GPU
  * (different streams, or unordered host threads) race on it.
  * Errors: INVALID_ARG, SHAPE, ALIGNMENT, TOO_LARGE, CUDA. */

@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle
+from format_cases import NVFP4_MIDPOINT_SCALES, nvfp4_midpoint_group
 
 # ---------------------------------------------------------------- BF16 -----
 
@@ -184,3 +185,36 @@ def test_nvfp4_group_special_cases():
     assert q[0] == 0x07            # element 0 in the low nibble, element 1 (0) high
     assert q[1] == (0xB << 4)      # element 3 = -1.5 -> code 8|3 in the high nibble
     assert np.all(q[2:] == 0)
+
+
+@pytest.mark.parametrize("scale_code", NVFP4_MIDPOINT_SCALES)
+def test_nvfp4_divides_by_the_scale(scale_code):
+    """The NVFP4 reading quantises x / d, one IEEE division. With d = 1.875 *
+    2^e the quotient of m*d is exactly the midpoint m, which must go to the
+    even code; multiplying by an fp32 reciprocal 1/d instead lands just off
+    the midpoint and picks the other neighbour for some of these elements,
+    so this group tells the two forms apart."""
+    x, want = nvfp4_midpoint_group(scale_code)
+    q, sc = oracle.nvfp4_group(x)
+    assert sc == scale_code
+    codes = np.empty(16, np.uint8)
+    codes[0::2], codes[1::2] = q & 15, q >> 4
+    for i, c in want.items():
+        assert codes[i] == c, (i, codes[i], c)
+    # the group discriminates: x * fl(1/d) rounds differently at >= 1 midpoint
+    d = np.float32(oracle.e4m3_value(scale_code))
+    inv = np.float32(1.0) / d
+    xf = oracle.bf16_to_f32_array(x)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    differs = 0
+    for i in range(16):
+        v = float(np.float32(xf[i]) * inv)
+        a = abs(v)
+        dist = np.abs(grid - a)
+        nearest = np.flatnonzero(dist == dist.min())
+        code = int(nearest[0] if len(nearest) == 1 else nearest[nearest % 2 == 0][0])
+        if a >= 6.0:
+            code = 7
+        code |= 8 if v < 0 or (v == 0 and np.signbit(v)) else 0
+        differs += code != want[i]
+    assert differs >= 1
