@@ -612,6 +612,33 @@ def _timed_b2b(fns, K, stream):
     return a.elapsed_time(b) * 1e3 / K
 
 
+DECODE_SWEEP_N = (1, 2, 4, 8, 16, 32, 64, 128, 256)
+RS_SWEEP_T = (32, 64, 128, 256, 512)
+
+
+def decode_sweep_rows(dev, K, W, seed_base, flush, flush_read, stream):
+    """The decode step at each N of DECODE_SWEEP_N: eager step time (events at
+    the step's ends, L2 flushed before each step) and CUDA-graph replay time.
+    Returns (rows, kernels launched, eager ms in total, tokens in total)."""
+    rows, launches, total_ms, total_tokens = [], 0, 0.0, 0
+    for n in DECODE_SWEEP_N:
+        spec = workload_spec("decode")
+        spec["num_tokens"] = n
+        st = Step(spec, dev, seed=seed_base + n)
+        for _ in range(W):
+            st.run()
+        eager = _timed(st.run, K, flush, flush_read, stream)
+        graph = measure_graph(st, K, flush, flush_read)
+        rows.append({"num_tokens": n, "eager_step_us": round(eager, 2),
+                     "graph_step_us": graph["step_us_median"],
+                     "graph_tokens_per_s": round(n / (graph["step_us_median"] / 1e6), 1)})
+        launches += st.launches_per_step * (K + graph["replays"])
+        total_ms += eager * K / 1e3
+        total_tokens += n * K
+        del st
+    return rows, launches, total_ms, total_tokens
+
+
 def run_decode_sweep(args, rank, world):
     """The decode step at N = 1, 2, 4, ..., 256 tokens (raw NVFP4 payload,
     top-8 of 256, R=8; the combine grouped by rank where N % R == 0): eager
@@ -624,21 +651,8 @@ def run_decode_sweep(args, rank, world):
     stream = torch.cuda.current_stream()
     K, W = min(args.steps, 100), args.warmup
     clocks = ClockSampler(gpu_uuid())
-    rows, launches, total_ms, total_tokens = [], 0, 0.0, 0
-    for n in (1, 2, 4, 8, 16, 32, 64, 128, 256):
-        spec = workload_spec("decode")
-        spec["num_tokens"] = n
-        st = Step(spec, dev, seed=rank * 1000 + n)
-        for _ in range(W):
-            st.run()
-        eager = _timed(st.run, K, flush, flush_read, stream)
-        graph = measure_graph(st, K, flush, flush_read)
-        rows.append({"num_tokens": n, "eager_step_us": round(eager, 2),
-                     "graph_step_us": graph["step_us_median"],
-                     "graph_tokens_per_s": round(n / (graph["step_us_median"] / 1e6), 1)})
-        launches += st.launches_per_step * K
-        total_ms += eager * K / 1e3
-        total_tokens += n * K
+    rows, launches, total_ms, total_tokens = decode_sweep_rows(dev, K, W, rank * 1000, flush,
+                                                               flush_read, stream)
     clk = clocks.stop()
     total_ms, value = whole_job(total_ms, total_tokens, world, dev)
     last = rows[-1]
@@ -655,25 +669,19 @@ def run_decode_sweep(args, rank, world):
     }
 
 
-def run_rs_sweep(args, rank, world):
-    """The combine as a reduce-scatter, R=4 ranks, H=8192, 32..512 tokens per
-    rank (0.5..8 MiB of output per rank): (i) the cross-rank sum of R BF16
-    partials, (ii) the top-8 weighted reduction grouped by rank. Device time
-    per call."""
+def rs_sweep_rows(dev, K, W, seed_base, flush, flush_read, stream):
+    """The combine as a reduce-scatter, R=4, H=8192, at each T of RS_SWEEP_T
+    tokens per rank: the rank sum of BF16 partials and the top-8 reduction
+    grouped by rank, one call after an L2 flush and calls back to back on
+    copies of the inputs beyond twice the L2. Returns (rows, kernels
+    launched)."""
     import torch
     from combine_moe_layout_03_gb300 import moe, synth
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-    K, W = min(args.steps, 100), args.warmup
     peak = measured_peaks()["hbm_gbs"]
-    clocks = ClockSampler(gpu_uuid())
     r, h, k, e = 4, 8192, 8, 256
     rows, launches = [], 0
-    for t in (32, 64, 128, 256, 512):
-        c = synth.rs_case(seed=rank * 1000 + t, tokens_per_rank=t, hidden=h, r=r, e=e, k=k)
+    for t in RS_SWEEP_T:
+        c = synth.rs_case(seed=seed_base + t, tokens_per_rank=t, hidden=h, r=r, e=e, k=k)
         n = r * t
         d = moe.MoeDesc(n, k, e, r, h)
         part = torch.from_numpy(c["partials_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
@@ -714,7 +722,25 @@ def run_rs_sweep(args, rank, world):
                      "topk_ranks_frac_back_to_back": round(b_f / us_fb / 1e3 / peak, 3)})
         del parts, ys, outs, ranks_b, fused_b
         launches += 4 * K
+    return rows, launches
+
+
+def run_rs_sweep(args, rank, world):
+    """The combine as a reduce-scatter, R=4 ranks, H=8192, 32..512 tokens per
+    rank (0.5..8 MiB of output per rank): (i) the cross-rank sum of R BF16
+    partials, (ii) the top-8 weighted reduction grouped by rank. Device time
+    per call."""
+    import torch
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    K, W = min(args.steps, 100), args.warmup
+    clocks = ClockSampler(gpu_uuid())
+    rows, launches = rs_sweep_rows(dev, K, W, rank * 1000, flush, flush_read, stream)
     clk = clocks.stop()
+    r = 4
     last = rows[-1]
     return {
         "metric": METRIC, "value": round(r * last["tokens_per_rank"] / (last["topk_ranks_us"] / 1e6), 1),
@@ -733,6 +759,103 @@ def run_rs_sweep(args, rank, world):
                              "note": "NCCL symmetric reduce-scatter, staged and direct, 4 GPUs over "
                                      "NVLink: a collective across GPUs, context only"},
     }
+
+
+def step_and_breakdown(st: "Step", K: int, flush, flush_read, stream) -> dict:
+    """Mean device time of K steps (events at each step's ends only, L2
+    flushed between steps) and of each of its three calls (a second loop
+    with an event between calls), in microseconds."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        flush_read.sum()
+        ev[i][0].record(stream)
+        st.run()
+        ev[i][1].record(stream)
+    eb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        flush_read.sum()
+        e = eb[i]
+        e[0].record(stream)
+        st.layout()
+        e[1].record(stream)
+        st.dispatch()
+        e[2].record(stream)
+        st.combine()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    out = {"step": statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3}
+    for name, a, b in (("layout", 0, 1), ("dispatch", 1, 2), ("combine", 2, 3)):
+        out[name] = statistics.mean(eb[i][a].elapsed_time(eb[i][b]) for i in range(K)) * 1e3
+    return out
+
+
+def run_configs(args, dev, flush, flush_read, stream) -> dict:
+    """The other workloads of the pages, measured in the same run as the
+    headline line with fewer steps each: tiny (step and graph replay), the
+    decode sweep N = 1..256 (graph replay), the reduce-scatter sweep 0.5..8
+    MiB per rank (both combine forms) and skewed (dispatch, combine, step)."""
+    K, W = max(3, min(args.steps, 20)), args.warmup
+    peak = measured_peaks()["hbm_gbs"]
+    clocks = ClockSampler(gpu_uuid())
+    t0 = time.perf_counter()
+    out, launches = {}, 0
+
+    st = Step(workload_spec("tiny"), dev, seed=101)
+    for _ in range(W):
+        st.run()
+    eager = _timed(st.run, K, flush, flush_read, stream)
+    graph = measure_graph(st, K, flush, flush_read)
+    launches += st.launches_per_step * (K + graph["replays"])
+    out["tiny"] = {"step_us": round(eager, 2), "graph_us": graph["step_us_median"],
+                   "what": "N=128 H=1024 E=16 top-2 R=2, BF16 dispatch and combine"}
+    del st
+
+    rows, n_l, _, _ = decode_sweep_rows(dev, K, W, 200, flush, flush_read, stream)
+    launches += n_l
+    out["decode_sweep"] = {"num_tokens": [r["num_tokens"] for r in rows],
+                           "graph_us": [r["graph_step_us"] for r in rows],
+                           "eager_us": [r["eager_step_us"] for r in rows],
+                           "what": "top-8 of 256, R=8, raw 3584 B + 448 B payload, BF16 combine "
+                                   "H=7168; one step = layout + dispatch + combine"}
+
+    rows, n_l = rs_sweep_rows(dev, K, W, 300, flush, flush_read, stream)
+    launches += n_l
+    out["rs_sweep"] = {"out_mib_per_rank": [r["out_mib_per_rank"] for r in rows]}
+    for key in ("rank_sum_us", "rank_sum_frac", "topk_ranks_us", "topk_ranks_frac",
+                "rank_sum_us_back_to_back", "rank_sum_frac_back_to_back",
+                "topk_ranks_us_back_to_back", "topk_ranks_frac_back_to_back"):
+        out["rs_sweep"][key] = [r[key] for r in rows]
+    out["rs_sweep"]["what"] = ("R=4, H=8192: rank sum of BF16 partials and top-8 reduction grouped "
+                               "by rank; one call after an L2 flush, and calls back to back")
+
+    spec = workload_spec("skewed")
+    st = Step(spec, dev, seed=400)
+    for _ in range(W):
+        st.run()
+    t = step_and_breakdown(st, K, flush, flush_read, stream)
+    launches += st.launches_per_step * K + 3 * K
+    n, bpt = spec["num_tokens"], spec["bytes_per_token"]
+    sk = {"step_us": round(t["step"], 2), "layout_us": round(t["layout"], 2),
+          "tokens_per_s": round(n / (t["step"] / 1e6), 1)}
+    for name in ("dispatch", "combine"):
+        gbs = bpt[name] * n / (t[name] / 1e6) / 1e9
+        sk[f"{name}_us"] = round(t[name], 2)
+        sk[f"{name}_gbs"] = round(gbs, 1)
+        sk[f"{name}_frac"] = round(gbs / peak, 4)
+    sk["routing"] = routing_stats(st.lay["tokens_per_expert"], st.lay["tokens_per_rank"])
+    sk["what"] = spec["text"]
+    out["skewed"] = sk
+    del st
+
+    out["steps_each"] = K
+    out["gpu_launches"] = launches
+    out["clocks"] = clocks.stop()
+    out["wall_s"] = round(time.perf_counter() - t0, 1)
+    out["l2"] = "flushed before every timed step or call, except the back-to-back columns"
+    return out
 
 
 def run_ours(args, spec, rank, world):
@@ -871,6 +994,10 @@ def run_ours(args, spec, rank, world):
         line["e2e"] = e2e
     if getattr(st, "lay", None) is not None and "tokens_per_expert" in st.lay:
         line["routing"] = routing_stats(st.lay["tokens_per_expert"], st.lay["tokens_per_rank"])
+    if spec["name"] == "prefill" and not spec.get("tokens_overridden") and world == 1 \
+            and not args.no_configs:
+        del sets, st
+        line["configs"] = run_configs(args, dev, flush, flush_read, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, budget_s=args.cpu_seconds)
     return line
@@ -1193,6 +1320,8 @@ def main(argv=None):
     ap.add_argument("--seeds", type=int, default=5,
                     help="seeded input sets the timed steps cycle through")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave out the other workloads' figures from the default (prefill) line")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override N (a multiple of the workload's ranks; prefill, skewed, decode and "
                          "rs workloads), e.g. for a smaller profiling case; such a line carries no traffic")

@@ -1,7 +1,8 @@
 """GPU parity of moe_dispatch (through the C ABI) against the oracle: records
 bit-exact, byte for byte, for BF16 pass-through, raw NVFP4 bytes, FP8 e4m3
 per-128 and NVFP4 per-16 quantisation; full-size workloads on sampled token
-ranges; untouched slots; determinism."""
+ranges; untouched slots; determinism; NVFP4 groups that fall on e2m1
+midpoints; GPU records read back with the host function moe_unpack_record."""
 import numpy as np
 import pytest
 import torch
@@ -9,6 +10,7 @@ import torch
 import oracle
 from combine_moe_layout_03_gb300 import synth
 
+from format_cases import NVFP4_MIDPOINT_SCALES, nvfp4_midpoint_group, quantised_row
 from gpu_helpers import DEV, dev_bf16, dev_f32, dev_i32, dev_u8, host
 
 pytestmark = pytest.mark.gpu
@@ -142,3 +144,77 @@ def test_empty_dispatch_is_a_no_op():
                      None, e, rec)
     torch.cuda.synchronize()
     assert bool((rec == FILL).all())
+
+
+@pytest.mark.parametrize("scale_code", NVFP4_MIDPOINT_SCALES)
+def test_nvfp4_midpoints_divide_by_the_scale(scale_code):
+    """Rows made of groups whose elements divide exactly onto e2m1 midpoints
+    (scale 1.875 * 2^e, an inexact reciprocal): the kernel's codes are the
+    even neighbours, as IEEE division gives, and equal the oracle's."""
+    grp, want = nvfp4_midpoint_group(scale_code)
+    n, h = 8, 256
+    g = np.random.default_rng(scale_code)
+    x = np.tile(grp, (n, h // 16))
+    for t in range(n):  # shuffle within groups so lanes see different positions
+        for gi in range(h // 16):
+            perm = g.permutation(16)
+            x[t, gi * 16:(gi + 1) * 16] = grp[perm]
+    c = synth.prefill_case(seed=scale_code, n=n, hidden=h)
+    c["hidden_bf16"] = x
+    got = compare(c, 256, 8, oracle.BF16, oracle.NVFP4_B16, x, dev_bf16(x))
+    from combine_moe_layout_03_gb300 import moe
+    lay = moe.moe_record_layout(moe.MoeDesc(n, 8, 256, 8, h, oracle.BF16, oracle.NVFP4_B16))
+    slot_of = oracle.layout(c["topk_idx"], 256, 8)["slot_of"]
+    for t in range(n):
+        rec = got[slot_of[t, 0]]
+        pay = rec[lay["off_payload"]:lay["off_payload"] + h // 2]
+        codes = np.empty(h, np.uint8)
+        codes[0::2], codes[1::2] = pay & 15, pay >> 4
+        sc = rec[lay["off_scales"]:lay["off_scales"] + h // 16]
+        assert np.all(sc == scale_code)
+        by_value = {int(v): code for v, code in zip(grp, (want[i] for i in range(16)))}
+        np.testing.assert_array_equal(codes, [by_value[int(v)] for v in x[t]])
+
+
+@pytest.mark.parametrize("in_kind,out_kind,h", [
+    (oracle.BF16, oracle.FP8_E4M3_B128, 7168),
+    (oracle.BF16, oracle.NVFP4_B16, 1024),
+    (oracle.BF16, oracle.FP8_E4M3_UE8M0, 1024),
+    (oracle.BF16, oracle.BF16, 1024),
+    (oracle.RAW, oracle.RAW, 0),
+])
+def test_unpack_gpu_records(in_kind, out_kind, h):
+    """Every record moe_dispatch wrote on the GPU, split by the host function
+    moe_unpack_record: header, id row, weight row, payload and scales agree
+    with the routing and with the oracle's quantisation of the token's row."""
+    from combine_moe_layout_03_gb300 import moe
+    if in_kind == oracle.RAW:
+        c = synth.decode_case(seed=31, n=48)
+        x, sc, rp, rs = c["payload"], c["scales"], 3584, 448
+        got = gpu_dispatch(c, 256, 8, in_kind, out_kind, dev_u8(x), dev_u8(sc), rp, rs)
+    else:
+        c = synth.prefill_case(seed=31, n=48, hidden=h)
+        c["topk_idx"] = c["topk_idx"].copy()
+        c["topk_idx"][5, 2] = -1
+        x, sc, rp, rs = c["hidden_bf16"], None, 0, 0
+        got = gpu_dispatch(c, 256, 8, in_kind, out_kind, dev_bf16(x))
+    ids, w = c["topk_idx"], c["topk_weights"]
+    n, k = ids.shape
+    d = moe.MoeDesc(n, k, 256, 8, c["hidden"], in_kind, out_kind, rp, rs)
+    lay = oracle.layout(ids, 256, 8)
+    rows = {}
+    for s in range(lay["num_pairs"]):
+        u = moe.moe_unpack_record(d, got[s])
+        t, j = u["src_token"], u["slot_j"]
+        assert lay["slot_of"][t, j] == s and u["expert"] == ids[t, j]
+        np.testing.assert_array_equal(u["ids"], ids[t])
+        np.testing.assert_array_equal(u["weights"].view(np.uint32), w[t].view(np.uint32))
+        if in_kind == oracle.RAW:
+            pay, scl = x[t], sc[t]
+        else:
+            if t not in rows:
+                rows[t] = quantised_row(x[t], out_kind)
+            pay, scl = rows[t]
+        np.testing.assert_array_equal(u["payload"], pay)
+        if scl is not None:
+            np.testing.assert_array_equal(u["scales"], scl)

@@ -99,3 +99,47 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     assert rc == moe.MOE_ERR_TOO_LARGE
     ok = moe.MoeDesc(250_000, 8, 256, 8, 8)
     assert moe.moe_workspace_size(ok) <= moe.MOE_NOALLOC_SCRATCH_BYTES
+
+
+def test_noalloc_python_wrapper_with_and_without_status():
+    """The binding's moe_layout_noalloc marshals the same call: with a status
+    tensor and without one, its outputs equal moe_layout's."""
+    from combine_moe_layout_03_gb300 import moe
+    dev = torch.device("cuda:0")
+    c = synth.decode_case(seed=21, n=256)
+    ids = torch.from_numpy(c["topk_idx"]).to(dev)
+    desc = moe.MoeDesc(256, 8, 256, 8, 8)
+    ref = moe.moe_layout(desc, ids)
+    status = torch.full((1,), 777, dtype=torch.int32, device=dev)
+    a = moe.moe_layout_noalloc(desc, ids, status=status)
+    b = moe.moe_layout_noalloc(desc, ids)
+    torch.cuda.synchronize()
+    for key in KEYS:
+        assert torch.equal(a[key], ref[key]), key
+        assert torch.equal(b[key], ref[key]), key
+    assert int(status.item()) == moe.MOE_OK
+
+
+def test_noalloc_at_the_largest_shape_its_scratch_holds():
+    """The largest N (E=256, R=8) whose scratch fits the fixed array runs and
+    matches moe_layout exactly; one more token is rejected before any launch."""
+    from combine_moe_layout_03_gb300 import moe
+    dev = torch.device("cuda:0")
+    lo, hi = 1, 1 << 20
+    while lo < hi:  # the largest N with moe_workspace_size <= the array
+        mid = (lo + hi + 1) // 2
+        if moe.moe_workspace_size(moe.MoeDesc(mid, 8, 256, 8, 8)) <= moe.MOE_NOALLOC_SCRATCH_BYTES:
+            lo = mid
+        else:
+            hi = mid - 1
+    n = lo
+    assert 250_000 <= n < 260_000
+    g = np.random.default_rng(99)
+    ids = g.integers(-1, 256, size=(n, 8)).astype(np.int32)
+    ids[g.random((n, 8)) < 0.25] = -1  # a sparse routing: about a quarter of the pairs empty
+    st, ref_st = _compare(moe, moe.MoeDesc(n, 8, 256, 8, 8), torch.from_numpy(ids).to(dev))
+    assert st == ref_st == moe.MOE_OK
+    over = moe.MoeDesc(n + 1, 8, 256, 8, 8)
+    rc = moe._lib.moe_layout_noalloc(ctypes.byref(over.c()), 16, 16, 16, 16, 16, 16, 16, None,
+                                     None, None)
+    assert rc == moe.MOE_ERR_TOO_LARGE
