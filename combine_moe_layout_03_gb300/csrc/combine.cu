@@ -26,6 +26,7 @@
 // expert row is read exactly once) and runs the fp32 fma chain in the fixed
 // order. The next unit's pair info is fetched while the current unit
 // streams, so its latency is hidden.
+#include <cstdlib>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -340,6 +341,163 @@ __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams
   }
 }
 
+// The same reduction with the expert rows brought into shared memory by the
+// bulk-copy engine, so the bytes in flight per SM are bounded by shared
+// memory, not by registers. A unit is one slice of a token's row (up to 128
+// 16-byte chunks); each block owns a contiguous run of units (mostly several
+// slices of one token, so the token's pair info is loaded once). Warp 0 is
+// the producer: it loads the token's (slot, weight, expert), orders the
+// valid pairs as order_pairs does, writes the weights and the group mask to
+// the stage's header and issues one cp.async.bulk per valid pair, copying
+// the pair's row slice into the stage; the stage's "full" mbarrier counts the
+// bytes. The consumer warps wait on it, run the fp32 chains of combine_chunk
+// from shared memory (same operations in the same order, so the result is
+// the same bit for bit), store the row slice and release the stage on its
+// "empty" mbarrier. kPipeStages stages are in flight per block.
+constexpr int kPipeConsumerWarps = 4;
+constexpr int kPipeThreads = 32 * (1 + kPipeConsumerWarps);
+constexpr int kPipeStages = 4;
+constexpr int kPipeMaxSliceChunks = 32 * kPipeConsumerWarps;  // one chunk per consumer thread
+
+struct PipeHeader {  // one per stage, before its row slices
+  int n;             // valid pairs
+  unsigned lastmask; // bit m: pair m closes its rank group
+  float w[MOE_MAX_TOPK];
+};
+constexpr int kPipeHeaderBytes = (int)((sizeof(PipeHeader) + 127) / 128 * 128);
+
+// Device status word of the kernels with bounded waits: MOE_ERR_TIMEOUT once a
+// wait gave up (read and cleared by moe_device_status).
+__device__ int g_device_status;
+
+__device__ __forceinline__ void record_timeout() { atomicExch(&g_device_status, MOE_ERR_TIMEOUT); }
+
+template <bool GROUP>
+__global__ void __launch_bounds__(kPipeThreads)
+    k_combine_pipe(CombineParams p, int slice_chunks, int slices_per_token, int64_t num_units,
+                   int64_t units_per_block, int stage_bytes) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(128) uint8_t pipe_smem[];
+  __shared__ __align__(8) uint64_t full[kPipeStages];
+  __shared__ __align__(8) uint64_t empty[kPipeStages];
+  const int warp = threadIdx.x >> 5, lane = (int)lane_id();
+  const int k = p.topk;
+  const int chunks = p.hidden_size / 8;
+  const size_t row_bytes = (size_t)p.hidden_size * 2;
+  const int64_t u0 = (int64_t)blockIdx.x * units_per_block;
+  const int64_t u1 = min(u0 + units_per_block, num_units);
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kPipeStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kPipeConsumerWarps);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const int slice_bytes = slice_chunks * 16;
+
+  if (warp == 0) {  // producer
+    const uint64_t pol = l2_evict_first_policy();
+    // pair info of token tt in lanes 0..k-1, fetched one token ahead
+    int nslot = -1, nidx = 0;
+    float nw = 0.0f;
+    auto fetch = [&](int64_t tt) {
+      nslot = -1;
+      if (lane < k && tt * slices_per_token < u1) {
+        const int64_t q = tt * k + lane;
+        nslot = p.slot_of[q];
+        nw = p.topk_weights ? p.topk_weights[q] : 1.0f;
+        if (GROUP) nidx = p.topk_idx[q];
+      }
+    };
+    int64_t cur_t = u0 / slices_per_token;
+    fetch(cur_t);
+    cur_t -= 1;
+    PairList pl;
+    pl.n = 0;
+    pl.slot = -1;
+    pl.w = 0.0f;
+    pl.lastmask = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int64_t u = u0; u < u1; ++u, ++issued) {
+      const int st = issued % kPipeStages;
+      const int64_t t = u / slices_per_token;
+      const int c0 = (int)(u % slices_per_token) * slice_chunks;
+      if (t != cur_t) {  // tokens come in order: the fetched info is t's
+        pl = order_pairs<GROUP>(nslot, nw, nidx, k, p.expert_out_rows, p.experts_per_rank);
+        cur_t = t;
+        fetch(t + 1);
+      }
+      // (the whole warp leaves together if any lane's wait gave up)
+      if (issued >= kPipeStages && !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((issued / kPipeStages) + 1) & 1))) {
+        ok = false;
+        break;
+      }
+      uint8_t* stage = pipe_smem + (size_t)st * stage_bytes;
+      PipeHeader* hdr = reinterpret_cast<PipeHeader*>(stage);
+      if (lane < pl.n) hdr->w[lane] = pl.w;
+      if (lane == 0) {
+        hdr->n = pl.n;
+        hdr->lastmask = pl.lastmask;
+      }
+      const uint32_t bytes = (uint32_t)(min(c0 + slice_chunks, chunks) - c0) * 16u;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes * (uint32_t)pl.n);
+      __syncwarp();
+      if (lane < pl.n)
+        bulk_g2s(stage + kPipeHeaderBytes + (size_t)lane * slice_bytes,
+                 p.expert_out + (size_t)pl.slot * row_bytes + (size_t)c0 * 16, bytes, &full[st], pol);
+    }
+    if (!ok) {
+      if (lane == 0) record_timeout();
+      // no copy may land in shared memory after the block has exited: wait
+      // (bounded) for the phases of the stages still in flight
+      for (int i = max(0, issued - kPipeStages); i < issued; ++i)
+        mbar_wait(&full[i % kPipeStages], (i / kPipeStages) & 1);
+    }
+    return;
+  }
+
+  // consumers: thread ct owns chunk ct of every slice
+  const int ct = threadIdx.x - 32;
+  int done = 0;
+  for (int64_t u = u0; u < u1; ++u, ++done) {
+    const int st = done % kPipeStages;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (done / kPipeStages) & 1))) {
+      if (lane == 0) record_timeout();
+      return;
+    }
+    const uint8_t* stage = pipe_smem + (size_t)st * stage_bytes;
+    const PipeHeader* hdr = reinterpret_cast<const PipeHeader*>(stage);
+    const int n = hdr->n;
+    const unsigned lastmask = hdr->lastmask;
+    const int64_t t = u / slices_per_token;
+    const int c0 = (int)(u % slices_per_token) * slice_chunks;
+    const int c = c0 + ct;
+    if (ct < slice_chunks && c < chunks) {
+      const uint8_t* src = stage + kPipeHeaderBytes + (size_t)ct * 16;
+      float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      float total[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int m = 0; m < n; ++m) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + (size_t)m * slice_bytes);
+        fma8(part, hdr->w[m], v);
+        if (GROUP && ((lastmask >> m) & 1u)) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            total[i] = __fadd_rn(total[i], part[i]);
+            part[i] = 0.0f;
+          }
+        }
+      }
+      st_v4(p.out + (size_t)t * row_bytes + (size_t)c * 16, pack8(GROUP ? total : part));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+}
+
 // Cross-rank sum: out[i] = bf16(sum_r float(P_r[i])), i over 16-byte chunks.
 template <int RB>
 __global__ void __launch_bounds__(256) k_combine_ranks(const uint8_t* partials, uint8_t* out,
@@ -389,6 +547,7 @@ struct DeviceInfo {
   int sms = 0;
   int topk_blocks[2] = {0, 0};
   int rows128_blocks = 0;  // resident 128-thread blocks of the plain row kernel
+  size_t smem_per_sm = 0;  // shared memory an SM offers its blocks
 };
 DeviceInfo g_info[64];
 std::once_flag g_info_once[64];
@@ -412,6 +571,13 @@ const DeviceInfo* device_info() {
       b2 = 0;
     }
     d.rows128_blocks = b2;
+    int dev2 = 0, smem = 0;
+    if (cudaGetDevice(&dev2) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev2) != cudaSuccess) {
+      cudaGetLastError();
+      smem = 0;
+    }
+    d.smem_per_sm = (size_t)smem;
     d.sms = sms;
   });
   return d.sms > 0 ? &d : nullptr;
@@ -419,16 +585,74 @@ const DeviceInfo* device_info() {
 
 }  // namespace
 
+// Which combines take the pipelined kernel: MOE_COMBINE_PIPE unset or 1 the
+// automatic choice of launch_combine_topk, 0 none, 2 all.
+int pipe_policy() {
+  static const int v = [] {
+    const char* e = getenv("MOE_COMBINE_PIPE");
+    if (!e || !*e) return 1;
+    return (int)strtol(e, nullptr, 10);
+  }();
+  return v;
+}
+
+cudaError_t launch_combine_pipe(const CombineParams& p, const DeviceInfo* di, cudaStream_t s) {
+  const int k = p.topk;
+  const int chunks = p.hidden_size / 8;
+  // slices of up to 128 chunks (2 KB), fewer for large k so that a stage
+  // stays within 48 KB
+  int slice = kPipeMaxSliceChunks;
+  while (slice > 8 && (size_t)k * slice * 16 > 48 * 1024) slice /= 2;
+  if (slice > chunks) slice = chunks;
+  const int slices_per_token = (chunks + slice - 1) / slice;
+  const int stage_bytes = (kPipeHeaderBytes + k * slice * 16 + 127) / 128 * 128;
+  const size_t smem = (size_t)kPipeStages * stage_bytes;
+  const void* fn = p.group_by_rank ? (const void*)k_combine_pipe<true> : (const void*)k_combine_pipe<false>;
+  cudaError_t err = ensure_dynamic_smem(fn, smem);
+  if (err != cudaSuccess) return err;
+  // resident blocks per SM from shared memory (1 KB per block is reserved)
+  int per_sm = di->smem_per_sm ? (int)(di->smem_per_sm / (smem + 1024)) : 1;
+  if (per_sm < 1) per_sm = 1;
+  if (per_sm > 8) per_sm = 8;
+  const int64_t num_units = (int64_t)p.num_tokens * slices_per_token;
+  int64_t blocks = (int64_t)di->sms * per_sm;
+  if (blocks > num_units) blocks = num_units;
+  const int64_t per_block = (num_units + blocks - 1) / blocks;
+  blocks = (num_units + per_block - 1) / per_block;
+  CombineParams q = p;
+  int sc = slice, spt = slices_per_token, sb = stage_bytes;
+  int64_t nu = num_units, upb = per_block;
+  void* args[] = {&q, &sc, &spt, &nu, &upb, &sb};
+  return launch_pdl(fn, dim3((unsigned)blocks), dim3(kPipeThreads), smem, s, args);
+}
+
 cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorInvalidDevice;
-  // One block per row from about three rows per SM up; below that the
-  // persistent warp kernel, with units of two 32-chunk steps (one pair
-  // ordering per 64 chunks), keeps every SM busy.
+  const int pipe = pipe_policy();
+  if (pipe >= 2) return launch_combine_pipe(p, di, s);
+  // The choice, from sweeps of the three kernels on GB300 (top-8, hidden
+  // 7168 and 8192, 64 to 4096 tokens, one call after an L2 flush and calls
+  // back to back):
+  //  * one block per row once the rows' loads in flight (a 128-thread block
+  //    keeps min(k, 8) 16-byte loads per thread) reach about 12 MB, enough to
+  //    cover DRAM latency at full bandwidth: from 768 tokens of top-8 up;
+  //  * below that, the persistent warp kernel when every unit of at most two
+  //    32-chunk steps has a resident warp (one round of row loads per warp);
+  //  * otherwise the pipelined kernel, whose bulk copies keep up to 64 KB per
+  //    block in flight without registers (256 and 512 tokens of hidden 8192:
+  //    12.3 -> 10.4 us and 17.1 -> 15.7 us back to back).
+  const int chunks = p.hidden_size / 8;
+  const int steps_per_token = (chunks + 31) / 32;  // warp steps of 32 chunks
+  const int g = p.group_by_rank ? 1 : 0;
+  const int64_t resident_warps = (int64_t)di->sms * di->topk_blocks[g] * kCombineWarps;
+  const bool rows = (int64_t)p.num_tokens * min(p.topk, kBatch) >= 6144;
+  const bool one_round = (int64_t)p.num_tokens * steps_per_token <= 2 * resident_warps;
+  if (!rows && !one_round && pipe == 1) return launch_combine_pipe(p, di, s);
   // The rank-grouped form keeps two fp32 accumulators per element: its
   // 128-thread blocks (twice as many per SM) measured 5% faster at N=4096
   // and 11% at N=1024 than 256-thread ones.
-  if (p.num_tokens >= di->sms * 3) {
+  if (rows || (pipe == 0 && p.num_tokens >= di->sms * 3)) {
     CombineParams q = p;
     void* args[] = {&q};
     if (p.group_by_rank)
@@ -442,12 +666,8 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
     return launch_pdl((const void*)k_combine_rows<false>, dim3((unsigned)p.num_tokens), dim3(kRowThreads),
                       0, s, args);
   }
-  const int chunks = p.hidden_size / 8;
-  const int steps_per_token = (chunks + 31) / 32;  // warp steps of 32 chunks
-  const int g = p.group_by_rank ? 1 : 0;
   // Units of one step when there is a resident warp for every one (each warp
   // then waits on one round of expert-row loads instead of two), else two.
-  const int64_t resident_warps = (int64_t)di->sms * di->topk_blocks[g] * kCombineWarps;
   const int per_unit =
       steps_per_token < 2 || (int64_t)p.num_tokens * steps_per_token <= resident_warps ? 1 : 2;
   const int chunks_per_unit = per_unit * 32;
@@ -462,6 +682,23 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   void* args[] = {&q, &upt, &cpu, &nu};
   const void* fn = p.group_by_rank ? (const void*)k_combine_topk<true> : (const void*)k_combine_topk<false>;
   return launch_pdl(fn, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s, args);
+}
+
+int read_device_status(int32_t* out, bool clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  if (clear && v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+  }
+  *out = v;
+  return MOE_OK;
 }
 
 cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t rows,

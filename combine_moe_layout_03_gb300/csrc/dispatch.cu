@@ -162,11 +162,12 @@ __device__ __forceinline__ void quant_nvfp4(const uint8_t* row, int H, uint8_t* 
 //          + (j' < j of token t with expert e)
 // -- the stable counting sort of the layout, computed per block with no
 // grid-wide exchange. Block 0 writes the expert counts and offsets and the
-// status word; block b counts the tokens of ranks b, b + N, ... (one barrier
-// count per rank); each block writes its token's slot_of row,
-// is_token_in_rank row and src_of_slot entries, and a share of the
-// src_of_slot tail (-1 beyond P). Ids outside [-1, E) count as -1 and raise
-// the status word, as in the layout kernels.
+// status word; block b counts the tokens of ranks b, b + N, ..., one warp per
+// rank over the staged ids; each block writes its token's slot_of row,
+// is_token_in_rank row (one rank per lane, OR-reduced over the warp) and
+// src_of_slot entries, and a share of the src_of_slot tail (-1 beyond P).
+// Ids outside [-1, E) count as -1 and raise the status word, as in the
+// layout kernels.
 constexpr int kFusedMaxPairs = 2048;      // what the kernel can take
 constexpr int kFusedDefaultPairs = 2048;  // where the host sends it by default
 constexpr int kFusedPairsPerThread = kFusedMaxPairs / kDispatchThreads;
@@ -216,28 +217,26 @@ __device__ void fused_layout(const LayoutParams& lp, int t, int* hist, int* s_sl
   if (bad) scratch[kFusedScratch - 1] = 1;
   __syncthreads();
 
-  // ranks b, b + N, ...: tokens with a pair on the rank. With more tokens
-  // than threads N > NT > R, so such a block has one rank.
-  if ((int)blockIdx.x < R) {
-    int total = 0;
-    for (int ub = 0; ub < N; ub += NT) {
-      const int u = ub + tid;
-      unsigned long long mask = 0ull;
-      if (u < N)
+  // ranks b, b + N, ...: tokens with a pair on the rank, one warp each over
+  // the staged ids (from the last warp down)
+  {
+    const int warp = tid >> 5, lane = (int)lane_id();
+    const int owned_r = (int)blockIdx.x < R ? (R - (int)blockIdx.x + N - 1) / N : 0;
+    for (int m = NT / 32 - 1 - warp; m < owned_r; m += NT / 32) {
+      const int r = blockIdx.x + m * N;
+      const int lo = r * El, hi = lo + El;
+      int cnt = 0;
+      for (int u = lane; u < N; u += 32) {
+        bool hit = false;
         for (int j = 0; j < k; ++j) {
-          const int e = sids[u * k + j];
-          if (e >= 0) mask |= 1ull << (e / El);
+          const int x = sids[u * k + j];
+          hit |= x >= lo && x < hi;
         }
-      for (int r = blockIdx.x; r < R; r += N) {
-        const int c = __syncthreads_count((int)((mask >> r) & 1ull));
-        if (N <= NT) {
-          if (tid == 0) lp.tokens_per_rank[r] = c;
-        } else {
-          total += c;
-        }
+        cnt += hit ? 1 : 0;
       }
+      cnt = __reduce_add_sync(0xffffffffu, cnt);
+      if (lane == 0) lp.tokens_per_rank[r] = cnt;
     }
-    if (N > NT && tid == 0) lp.tokens_per_rank[blockIdx.x] = total;
   }
 
   // expert offsets: thread tid owns experts [tid*m, tid*m + m)
@@ -285,13 +284,13 @@ __device__ void fused_layout(const LayoutParams& lp, int t, int* hist, int* s_sl
     if (lp.src_of_slot && s >= 0) lp.src_of_slot[s] = t * k + j;
     s_slot[j] = (s >= 0 && (int64_t)s < capacity) ? s : -1;
   }
-  if (tid < R) {
-    bool in = false;
-    for (int jj = 0; jj < k; ++jj) {
-      const int e = sids[t * k + jj];
-      in |= e >= 0 && e / El == tid;
-    }
-    lp.is_token_in_rank[(int64_t)t * R + tid] = in ? 1 : 0;
+  if (tid < 32) {  // the token's rank row: one division per lane, OR over the warp
+    const int e = tid < k ? sids[t * k + tid] : -1;
+    const int r = e >= 0 ? e / El : -1;
+    const unsigned m0 = __reduce_or_sync(0xffffffffu, (r >= 0 && r < 32) ? 1u << r : 0u);
+    const unsigned m1 = __reduce_or_sync(0xffffffffu, r >= 32 ? 1u << (r - 32) : 0u);
+    for (int rr = tid; rr < R; rr += 32)
+      lp.is_token_in_rank[(int64_t)t * R + rr] = (uint8_t)(((rr < 32 ? m0 >> rr : m1 >> (rr - 32))) & 1u);
   }
   if (lp.src_of_slot)
     for (int s = P + blockIdx.x * NT + tid; s < NK; s += gridDim.x * NT) lp.src_of_slot[s] = -1;
@@ -340,17 +339,23 @@ __device__ __forceinline__ void dispatch_token(const DispatchParams& p, const La
       copy_g2s_async(img + os, p.scales + (size_t)t * p.in_scale_bytes, p.scale_bytes / 16);
   }
 
-  // slots, ids and weights of this token
+  // slots, ids and weights of this token (the fused form keeps the loads in
+  // flight through its layout and stores them after it)
+  int own_e = -1;
+  uint32_t own_w = 0;
   if (threadIdx.x < k) {
     const int64_t q = (int64_t)t * k + threadIdx.x;
     if (SLOTS == kSlotsAfterWait) {
       const int s = p.slot_of[q];
       s_slot[threadIdx.x] = (s >= 0 && (int64_t)s < p.record_capacity) ? s : -1;
     }
-    const int e = p.topk_idx[q];
-    s_expert[threadIdx.x] = e;
-    reinterpret_cast<int32_t*>(img + oi)[threadIdx.x] = e;
-    reinterpret_cast<uint32_t*>(img + ow)[threadIdx.x] = __float_as_uint(p.topk_weights[q]);
+    own_e = p.topk_idx[q];
+    own_w = __float_as_uint(p.topk_weights[q]);
+    if (SLOTS != kSlotsFused) {
+      s_expert[threadIdx.x] = own_e;
+      reinterpret_cast<int32_t*>(img + oi)[threadIdx.x] = own_e;
+      reinterpret_cast<uint32_t*>(img + ow)[threadIdx.x] = own_w;
+    }
   }
   zero_bytes(img, oi + 4 * k, ow);
   zero_bytes(img, ow + 4 * k, op);
@@ -360,6 +365,11 @@ __device__ __forceinline__ void dispatch_token(const DispatchParams& p, const La
   if (SLOTS == kSlotsFused) {
     const int hist_off = (body + (kQuant ? p.in_row_bytes : 0) + 15) & ~15;
     fused_layout(*lp, t, reinterpret_cast<int*>(img + hist_off), s_slot, p.record_capacity);
+    if (threadIdx.x < k) {
+      s_expert[threadIdx.x] = own_e;
+      reinterpret_cast<int32_t*>(img + oi)[threadIdx.x] = own_e;
+      reinterpret_cast<uint32_t*>(img + ow)[threadIdx.x] = own_w;
+    }
   }
 
   cp_async_wait_all();

@@ -224,6 +224,7 @@ const char* moe_strerror(int status) {
     case MOE_ERR_CUDA: return "a CUDA launch or copy failed";
     case MOE_ERR_DEVICE_IDS: return "an expert id was outside [-1, num_experts)";
     case MOE_ERR_TOO_LARGE: return "shape needs more scratch than moe_layout_noalloc's fixed array";
+    case MOE_ERR_TIMEOUT: return "a bounded device wait gave up";
     default: return "unknown status";
   }
 }
@@ -268,6 +269,15 @@ int moe_layout_status(const void* workspace, int32_t* status, moe_stream_t strea
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   *status = v;
   return MOE_OK;
+}
+
+int moe_device_status(int32_t* status, int clear) {
+  if (!status) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return moe::read_device_status(status, clear != 0);
 }
 
 }  // extern "C"

@@ -162,6 +162,9 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_combine_ranks(const uint8_t* partials, uint8_t* out, int64_t rows,
                                  int hidden_size, int num_ranks, cudaStream_t s);
 cudaError_t launch_combine_norm(const CombineNormParams& p, cudaStream_t s);
+// The device status word of the kernels with bounded waits (MOE_OK, or
+// MOE_ERR_TIMEOUT once a wait gave up); synchronous. clear: reset it to MOE_OK.
+int read_device_status(int32_t* out, bool clear);
 cudaError_t launch_slots(bool pack, const void* const* src, void* const* dst,
                          const moe_slot_desc_t* d, const int64_t* offsets, int64_t slot_bytes,
                          cudaStream_t s);
@@ -282,6 +285,69 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // Make generic-proxy writes to shared memory visible to the async proxy.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- mbarriers and bulk copies global -> shared -----------------------------
+// An mbarrier in shared memory counts thread arrivals and the bytes of bulk
+// copies (transaction count) of its current phase; waiting on the phase's
+// parity returns once both are complete.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Makes initialised barriers visible to the bulk-copy (async) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// One arrival that also announces `bytes` of bulk copies for this phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Every wait on an mbarrier in this library is bounded: it gives up after
+// kWaitLimitNs of wall time (far beyond any legitimate wait: the copies it
+// waits for are reads of this GPU's own memory) and returns false, and the
+// caller records MOE_ERR_TIMEOUT in the library's device status word.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+// Bulk copy global -> shared of `bytes` (16-byte aligned addresses, a
+// multiple of 16 bytes) whose completion is counted on `bar`, with an L2
+// cache policy (e.g. evict-first for data read once).
+__device__ __forceinline__ void bulk_g2s(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                         uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
 }
 
 // Inclusive warp scan of an int.

@@ -24,6 +24,7 @@ MOE_ERR_CAPACITY = -4
 MOE_ERR_CUDA = -5
 MOE_ERR_DEVICE_IDS = -6
 MOE_ERR_TOO_LARGE = -7
+MOE_ERR_TIMEOUT = -8
 MOE_NOALLOC_SCRATCH_BYTES = 2 << 20
 
 MOE_PAYLOAD_BF16 = 0
@@ -110,6 +111,8 @@ _lib.moe_combine_gather_ranks_backward.restype = ctypes.c_int
 _lib.moe_combine_gather_ranks_backward.argtypes = [_D, _vp, _vp, _vp, _i64, _vp]
 _lib.moe_mask_topk_ids.restype = ctypes.c_int
 _lib.moe_mask_topk_ids.argtypes = [_vp, _i32, _i32, _vp, _vp]
+_lib.moe_device_status.restype = ctypes.c_int
+_lib.moe_device_status.argtypes = [_vp, ctypes.c_int]
 _lib.moe_pack_record.restype = ctypes.c_int
 _lib.moe_pack_record.argtypes = [_D, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
 _lib.moe_unpack_record.restype = ctypes.c_int
@@ -223,6 +226,14 @@ def moe_layout_noalloc(desc: MoeDesc, topk_idx: torch.Tensor, out: dict | None =
                                  _ptr(out.get("src_of_slot")), _ptr(status), _stream(stream))
     _check(rc, "moe_layout_noalloc")
     return out
+
+
+def moe_device_status(clear: bool = True) -> int:
+    """Status of the kernels with bounded waits on this device since the last
+    clearing call: MOE_OK or MOE_ERR_TIMEOUT (synchronises the device)."""
+    v = _i32(0)
+    _check(_lib.moe_device_status(ctypes.byref(v), 1 if clear else 0), "moe_device_status")
+    return v.value
 
 
 def moe_layout_status(workspace: torch.Tensor, stream=None) -> int:
@@ -667,4 +678,4 @@ def exported_symbols() -> list[str]:
             "moe_pack_slots", "moe_unpack_slots", "moe_mask_topk_ids", "moe_rank_layout",
             "moe_dispatch_ranks", "moe_combine_gather_ranks", "moe_ll_layout",
             "moe_dispatch_ll", "moe_combine_backward", "moe_dispatch_backward",
-            "moe_combine_gather_ranks_backward", "moe_layout_dispatch"]
+            "moe_combine_gather_ranks_backward", "moe_layout_dispatch", "moe_device_status"]

@@ -67,6 +67,7 @@ extern "C" {
 #define MOE_ERR_CUDA (-5)        /* a CUDA launch or copy failed */
 #define MOE_ERR_DEVICE_IDS (-6)  /* (from moe_layout_status) an id was outside [-1, E) */
 #define MOE_ERR_TOO_LARGE (-7)   /* moe_layout_noalloc: the shape needs more scratch than it has */
+#define MOE_ERR_TIMEOUT (-8)     /* (from moe_device_status) a bounded device wait gave up */
 
 typedef void* moe_stream_t;
 
@@ -184,6 +185,17 @@ int moe_layout(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* tokens_
  * *status (MOE_OK or MOE_ERR_DEVICE_IDS) after synchronising the stream.
  * This is the only call that waits for the device. Errors: INVALID_ARG, CUDA. */
 int moe_layout_status(const void* workspace, int32_t* status, moe_stream_t stream);
+
+/* Status of the kernels that wait on shared-memory barriers (the pipelined
+ * combine: expert rows brought into shared memory by bulk copies). Every
+ * such wait is bounded: after 1 s it gives up, the kernel records
+ * MOE_ERR_TIMEOUT in a device word of the library and returns, leaving the
+ * context usable. No legitimate run reaches that limit, since the copies are
+ * reads of the GPU's own memory. *status receives MOE_OK or MOE_ERR_TIMEOUT
+ * for all launches on the current device since the last call with clear != 0
+ * (which resets the word). It synchronises the device; it is not for a hot
+ * loop. Errors: INVALID_ARG, CUDA. */
+int moe_device_status(int32_t* status, int clear);
 
 /* Permute and pack (dispatch). For every pair (t, j) with slot_of[t, j] >= 0
  * writes one record (moe_record_layout) to

@@ -151,6 +151,6 @@ def test_argument_errors_return_codes_without_launch(moe):
 
 
 def test_strerror_covers_codes(moe):
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         assert moe.moe_strerror(code) != "unknown status"
     assert moe.moe_strerror(-99) == "unknown status"
