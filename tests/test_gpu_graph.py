@@ -138,3 +138,45 @@ def test_fixed_capacity_forward_and_backward_graph():
         ref_gy, _ = oracle.combine_backward(gg, c["topk_weights"], so, y_ref, rows, h)
         np.testing.assert_array_equal(host_bf16(gy)[pos], ref_gy[pos])
         np.testing.assert_array_equal(host_bf16(gx), oracle.dispatch_backward(ref_gy, so, h))
+
+
+def test_pipelined_combine_graph_replays_on_new_inputs():
+    # 4 ranks x 64 tokens of hidden 8192, top-8 of 256 grouped by rank: the
+    # shape moe_combine sends to its pipelined kernel (bulk copies into
+    # shared-memory stages); layout + combine captured once, replayed twice
+    from combine_moe_layout_03_gb300 import moe
+    r, t_per, k, e, h = 4, 64, 8, 256, 8192
+    n = r * t_per
+    d = moe.MoeDesc(n, k, e, r, h)
+    ids = torch.empty((n, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((n, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((n * k, h), dtype=torch.bfloat16, device=DEV)
+    lay = moe.layout_outputs(d, DEV)
+    ws = torch.empty(max(moe.moe_workspace_size(d), 256), dtype=torch.uint8, device=DEV)
+    out = torch.empty((n, h), dtype=torch.bfloat16, device=DEV)
+
+    def fill(seed):
+        c = synth.rs_case(seed=seed, tokens_per_rank=t_per, hidden=h, r=r, e=e, k=k, with_partials=False)
+        ids.copy_(torch.from_numpy(c["topk_idx"]))
+        w.copy_(torch.from_numpy(c["topk_weights"]))
+        y.copy_(dev_bf16(c["expert_out_bf16"]))
+        return c
+
+    fill(20)
+    calls = [
+        lambda s: moe.prepare_layout(d, ids, lay, ws, s.cuda_stream)(),
+        lambda s: moe.prepare_combine(d, moe.MOE_COMBINE_TOPK_RANKS, y, ids, w, lay["slot_of"], out,
+                                      s.cuda_stream)(),
+    ]
+    g = _capture(calls)
+    for seed in (21, 22):
+        c = fill(seed)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.layout(c["topk_idx"], e, r)
+        np.testing.assert_array_equal(host(lay["slot_of"]), ref["slot_of"])
+        np.testing.assert_array_equal(
+            host_bf16(out), oracle.combine_topk_ranks(c["expert_out_bf16"], c["topk_idx"], c["topk_weights"],
+                                                      ref["slot_of"], e, r, h))
+    assert moe.moe_device_status(clear=False) == moe.MOE_OK

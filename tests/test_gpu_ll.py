@@ -189,3 +189,42 @@ def test_ll_combine(case, hidden):
     torch.cuda.synchronize()
     ref = oracle.combine_topk(y_used, w, compact, hidden)
     assert_combine_close(host_bf16(out), ref, case)
+
+
+@pytest.mark.parametrize("out_kind,n,hidden,r,max_t", [
+    (oracle.FP8_E4M3_B128, 1216, 512, 8, 160),
+    (oracle.NVFP4_B16, 704, 1024, 4, 200),
+    (oracle.FP8_E4M3_UE8M0, 1000, 256, 8, 125),
+])
+def test_dispatch_ll_persistent_every_token(out_kind, n, hidden, r, max_t):
+    """Every token of a larger routing in each quantising format (the full-size
+    case above samples tokens): every used row equals the oracle's, unused
+    rows are untouched, with padding pairs in the routing."""
+    from combine_moe_layout_03_gb300 import moe
+    c = synth.prefill_case(seed=n, n=n, hidden=hidden)
+    ids = c["topk_idx"].copy()
+    ids[::13, 5] = -1  # padding pairs
+    e, k = 256, 8
+    d = moe.MoeDesc(n, k, e, r, hidden, in_kind=oracle.BF16, out_kind=out_kind)
+    ids_d = dev_i32(ids)
+    lay = moe.moe_layout(d, ids_d)
+    ll = moe.moe_ll_layout(d, max_t, ids_d, lay)
+    cap = ll["capacity"]
+    rows = e * cap
+    lay_rec = moe.moe_record_layout(d)
+    pb, sbp = lay_rec["payload_bytes"], (lay_rec["scale_bytes"] + 15) // 16 * 16
+    xo = torch.full((rows, pb), 0x5A, dtype=torch.uint8, device=DEV)
+    so = torch.full((rows, sbp), 0x5A, dtype=torch.uint8, device=DEV)
+    moe.moe_dispatch_ll(d, dev_bf16(c["hidden_bf16"]), None, ll["ll_slot_of"], cap, x_out=xo, scales_out=so)
+    torch.cuda.synchronize()
+    ll_h = oracle.ll_layout(ids, e, r, max_t)
+    np.testing.assert_array_equal(host(ll["ll_slot_of"]), ll_h["ll_slot_of"])
+    ref_x, ref_s = oracle.dispatch_ll(c["hidden_bf16"], None, ll_h["ll_slot_of"], rows, oracle.BF16,
+                                      out_kind, hidden)
+    so_h = ll_h["ll_slot_of"]
+    used = np.zeros(rows, bool)
+    used[so_h[so_h >= 0]] = True
+    gx, gs = host(xo), host(so)
+    np.testing.assert_array_equal(gx[used], ref_x[used])
+    np.testing.assert_array_equal(gs[used], ref_s[used])
+    assert (gx[~used] == 0x5A).all() and (gs[~used] == 0x5A).all()
