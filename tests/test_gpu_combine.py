@@ -58,6 +58,14 @@ def test_decode_shapes(n):
     check_topk(c["topk_idx"], c["topk_weights"], 256, 8, 7168, seed=n)
 
 
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 32, 64, 128, 256])
+def test_decode_sweep_in_the_bench_mode(n):
+    # every N of the decode sweep, in the mode the benchmark's step runs: the
+    # top-k reduction grouped by rank where N % R == 0, else the plain one
+    c = synth.decode_case(seed=300 + n, n=n)
+    check_topk(c["topk_idx"], c["topk_weights"], 256, 8, 7168, seed=300 + n, mode=2 if n % 8 == 0 else 0)
+
+
 @pytest.mark.parametrize("mode", [0, 2])
 def test_prefill_full_size_sampled(mode):
     c = synth.prefill_case(seed=0)
