@@ -344,9 +344,10 @@ class Step:
                                                self.ids, self.w, self.lay["slot_of"], self.out)
 
     def _setup_per_rank(self, spec, dev, seed):
-        """One record per (token, rank): the rank layout runs after the layout
-        (both timed as 'layout'); the expert of rank r returns, per received
-        token, the sum of its local pairs' weight times the dequantised row."""
+        """One record per (token, rank): the layout and the receive layout in
+        one call (moe_layout_ranks, timed as 'layout'); the expert of rank r
+        returns, per received token, the sum of its local pairs' weight times
+        the dequantised row."""
         import torch
         moe = self.moe
         n, h = spec["num_tokens"], spec["hidden"]
@@ -365,11 +366,13 @@ class Step:
         self.y = (q.float() * sc.repeat_interleave(128, dim=1) * lw.sum(1, keepdim=True)).to(torch.bfloat16)
         self.recv_records = recv
         import torch
-        lp, rp, dp, cp = self._rank_calls_on(torch.cuda.current_stream())
-        self.layout = lambda: (lp(), rp())
+        lp, dp, cp = self._rank_calls_on(torch.cuda.current_stream())
+        self.layout = lp
         self.dispatch, self.combine = dp, cp
-        self.launches_per_step = layout_launches(n, spec["topk"], spec["num_experts"],
-                                                 spec["num_ranks"]) + 1 + 1 + 1
+        # the receive layout runs inside the cluster layout launch, or as a
+        # third kernel after the two-kernel layout
+        nl = layout_launches(n, spec["topk"], spec["num_experts"], spec["num_ranks"])
+        self.launches_per_step = nl + (0 if nl == 1 else 1) + 1 + 1
         # algorithmic bytes per token from the actual (token, rank) records
         per = recv / n
         r = spec["num_ranks"]
@@ -455,8 +458,7 @@ class Step:
     def _rank_calls_on(self, stream):
         moe = self.moe
         h = stream.cuda_stream
-        return [moe.prepare_layout(self.desc, self.ids, self.lay, self.ws, h),
-                moe.prepare_rank_layout(self.desc, self.lay, 1, self.rlay, h),
+        return [moe.prepare_layout_ranks(self.desc, self.ids, 1, self.lay, self.rlay, self.ws, h),
                 moe.prepare_dispatch_ranks(self.desc, self.ids, self.w, self.x, self.sc,
                                            self.rlay["send_head"], self.records, h),
                 moe.prepare_combine_gather_ranks(self.cdesc, self.y, self.rlay["send_head"],

@@ -564,13 +564,15 @@ __device__ __forceinline__ void st_cluster_s32(int* local_addr, unsigned rank, i
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
 }
 
-// Shared memory of k_layout_cluster, in ints (MASK words rounded to ints).
+// Shared memory of k_layout_cluster, in ints (MASK words rounded to ints),
+// plus the per-chunk rank counts of the receive layout when it is computed.
 __host__ __device__ inline size_t cluster_smem_ints(int tpb, int k, int E, int R, int G, bool inv,
-                                                    size_t mask_bytes, bool peer_masks) {
+                                                    size_t mask_bytes, bool peer_masks, bool ranks = false) {
   const size_t E4 = (size_t)((E + 3) & ~3);
   return (size_t)kClusterWarps * E4 * (peer_masks ? 2 : 1) + (size_t)tpb * k * (inv ? 2 : 1) +
          tpb * mask_bytes / 4 +
-         (size_t)G * E + (size_t)G * (R + 1) + (size_t)kClusterWarps * R + 4 * (size_t)E + 80;
+         (size_t)G * E + (size_t)G * (R + 1) + (size_t)kClusterWarps * R + 4 * (size_t)E + 80 +
+         (ranks ? (size_t)((tpb + 31) / 32) * R + 2 * (size_t)R : 0);
 }
 
 // Everything in one launch: a cluster of G blocks (G <= 16), block c owning a
@@ -597,6 +599,10 @@ __host__ __device__ inline size_t cluster_smem_ints(int tpb, int k, int E, int R
 //  6. slot_of in pair order and the block's pairs in slot order in shared
 //     memory (inv), then src_of_slot from inv, so both are coalesced stores
 //     (without room for inv, src_of_slot is scattered from step 6).
+//  7. With p.send_head set (moe_layout_ranks), the per-rank receive layout:
+//     every block has received all blocks' tokens-per-rank counts in step 4,
+//     which give each rank's base and this block's prefix; warp ballots over
+//     32-token chunks of the rank masks give the positions inside the block.
 // No workspace is used except the status word.
 template <typename MASK, int L>
 __global__ void __launch_bounds__(kClusterThreads)
@@ -700,10 +706,15 @@ __global__ void __launch_bounds__(kClusterThreads)
     } else {
       s = s_bad;
     }
-    if (multi)
-      st_cluster_s32(allr + c * (R + 1) + r, 0u, s);
-    else
+    if (multi) {
+      if (p.send_head) {
+        for (int b = 0; b < G; ++b) st_cluster_s32(allr + c * (R + 1) + r, (unsigned)b, s);
+      } else {
+        st_cluster_s32(allr + c * (R + 1) + r, 0u, s);
+      }
+    } else {
       allr[r] = s;
+    }
   }
   if (multi)
     cluster.sync();  // every block's counts are in the shared memory of the blocks that need them
@@ -739,6 +750,10 @@ __global__ void __launch_bounds__(kClusterThreads)
         p.tokens_per_expert[e] = tot[i];
         p.expert_offset[e] = ex.x;
         if (e % p.experts_per_rank == 0) p.rank_offset[e / p.experts_per_rank] = ex.x;
+        if (p.send_head) {  // the receive layout's per-expert counts, aligned
+          const int a = p.expert_alignment;
+          p.recv_tokens_per_expert[e] = (tot[i] + a - 1) / a * a;
+        }
       }
       ex.x += tot[i];
       ex.y += own[i];
@@ -809,6 +824,73 @@ __global__ void __launch_bounds__(kClusterThreads)
     }
   }
   clear_src_tail(p, total);
+
+  // 7.
+  if (p.send_head) {
+    const int warp = threadIdx.x >> 5, lane = (int)lane_id();
+    const int nt = t1 - t0;
+    const int nch = (tpb + 31) / 32;
+    int* chc = scratch + 80;  // [nch][R] tokens per rank in each 32-token chunk, then their prefix
+    int* rbase = chc + nch * R;  // [R] slot of the block's first token on each rank
+    int* rall = rbase + R;       // [R] tokens per rank over all blocks
+    for (int ch = warp; ch < nch; ch += NW) {
+      const int tt = ch * 32 + lane;
+      const MASK m = tt < nt ? masks[tt] : (MASK)0;
+      for (int r = 0; r < R; ++r) {
+        const unsigned bits = __ballot_sync(0xffffffffu, ((m >> r) & 1) != 0);
+        if (lane == 0) chc[ch * R + r] = __popc(bits);
+      }
+    }
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+      int all = 0, before = 0;
+      for (int b = 0; b < G; ++b) {
+        const int v = allr[b * (R + 1) + r];
+        all += v;
+        before += b < c ? v : 0;
+      }
+      rall[r] = all;
+      rbase[r] = before;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // rank bases: exclusive scan over ranks
+      int run = 0;
+      for (int r = 0; r < R; ++r) {
+        rbase[r] += run;
+        if (c == 0) p.recv_offset[r] = run;
+        run += rall[r];
+      }
+      if (c == 0) p.recv_offset[R] = run;
+      rall[0] = run;  // total receive slots, for the recv_src_idx tail
+    }
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {  // chunk prefixes per rank
+      int run = 0;
+      for (int ch = 0; ch < nch; ++ch) {
+        const int v = chc[ch * R + r];
+        chc[ch * R + r] = run;
+        run += v;
+      }
+    }
+    __syncthreads();
+    for (int ch = warp; ch < nch; ch += NW) {
+      const int tt = ch * 32 + lane;
+      const MASK m = tt < nt ? masks[tt] : (MASK)0;
+      for (int r = 0; r < R; ++r) {
+        const bool in = ((m >> r) & 1) != 0;
+        const unsigned bits = __ballot_sync(0xffffffffu, in);
+        if (tt < nt) {
+          const int slot = in ? rbase[r] + chc[ch * R + r] + __popc(bits & ((1u << lane) - 1u)) : -1;
+          p.send_head[(int64_t)(t0 + tt) * R + r] = slot;
+          if (in && p.recv_src_idx) p.recv_src_idx[slot] = t0 + tt;
+        }
+      }
+    }
+    if (p.recv_src_idx) {
+      const int64_t cap = (int64_t)p.num_tokens * R;
+      for (int64_t q = (int64_t)rall[0] + (int64_t)c * blockDim.x + threadIdx.x; q < cap;
+           q += (int64_t)G * blockDim.x)
+        p.recv_src_idx[q] = -1;
+    }
+  }
 }
 
 }  // namespace
@@ -889,7 +971,7 @@ static int max_cluster_blocks() {
 }
 
 static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int num_ranks, bool want_inv,
-                                int gmax) {
+                                int gmax, bool ranks = false) {
   // about kPairsPerClusterBlock pairs per block, but small inputs still
   // spread over up to gmax blocks of at least kMinPairsPerClusterBlock
   const int64_t pairs = (int64_t)num_tokens * topk;
@@ -910,17 +992,20 @@ static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int n
   const size_t mb = cp.wide ? 8 : 4;
   // peer masks in shared memory when they fit, then the inverse map for
   // coalesced src_of_slot stores when that fits too
-  cp.use_or = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, false, mb, true) * 4 <= kClusterMaxSmem;
-  cp.use_inv = want_inv && cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, true, mb, cp.use_or) * 4 <=
+  cp.use_or = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, false, mb, true, ranks) * 4 <= kClusterMaxSmem;
+  cp.use_inv = want_inv && cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, true, mb, cp.use_or, ranks) * 4 <=
                                kClusterMaxSmem;
-  cp.smem = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, cp.use_inv, mb, cp.use_or) * 4;
+  cp.smem = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, cp.use_inv, mb, cp.use_or, ranks) * 4;
   return cp;
 }
 
-cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s) {
+cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s, bool* ranks_done) {
   const int E = p.num_experts, R = p.num_ranks;
-  const ClusterPlan cp = cluster_plan(p.num_tokens, p.topk, E, R, p.src_of_slot != nullptr, max_cluster_blocks());
+  const ClusterPlan cp = cluster_plan(p.num_tokens, p.topk, E, R, p.src_of_slot != nullptr, max_cluster_blocks(),
+                                      p.send_head != nullptr);
+  if (ranks_done) *ranks_done = false;
   if (cp.smem <= kClusterMaxSmem) {
+    if (ranks_done) *ranks_done = p.send_head != nullptr;
     const void* fn = cluster_kernel(cp.wide, cp.lanes);
     cudaError_t err = set_smem(fn, cp.smem);
     if (err != cudaSuccess) return err;
@@ -935,6 +1020,7 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s) {
   cudaError_t err = set_smem((const void*)k_layout_count, smem_count);
   if (err != cudaSuccess) return err;
   LayoutParams q = p;
+  q.send_head = nullptr;  // the two-kernel path leaves the receive layout to the caller
   void* args[] = {&q};
   err = launch_pdl((const void*)k_layout_count, dim3(p.num_chunks), dim3(kCountThreads), smem_count, s,
                    args);

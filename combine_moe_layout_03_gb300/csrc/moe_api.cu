@@ -207,6 +207,11 @@ int layout_params(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* toke
   p->chunk_hist = (int32_t*)(ws + 256);
   p->chunk_rank = p->chunk_hist + (size_t)p->num_chunks * E;
   p->chunk_flag = p->chunk_rank + (size_t)p->num_chunks * R;
+  p->send_head = nullptr;  // no receive layout unless moe_layout_ranks asks for it
+  p->recv_src_idx = nullptr;
+  p->recv_offset = nullptr;
+  p->recv_tokens_per_expert = nullptr;
+  p->expert_alignment = 1;
   return MOE_OK;
 }
 
@@ -258,6 +263,52 @@ int moe_layout(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* tokens_
     return cuda_status(e);
   }
   return cuda_status(moe::launch_layout(p, s));
+}
+
+int moe_layout_ranks(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* tokens_per_expert,
+                     int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
+                     int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot, int32_t expert_alignment,
+                     int32_t* send_head, int32_t* recv_src_idx, int32_t* recv_offset,
+                     int32_t* recv_tokens_per_expert, void* workspace, size_t ws_bytes, moe_stream_t stream) {
+  moe::LayoutParams p;
+  int rc = layout_params(desc, topk_idx, tokens_per_expert, tokens_per_rank, is_token_in_rank,
+                         expert_offset, rank_offset, slot_of, src_of_slot, workspace, ws_bytes, &p);
+  if (rc != MOE_OK) return rc;
+  const int N = p.num_tokens;
+  if (expert_alignment < 1 || !recv_offset || !recv_tokens_per_expert) return MOE_ERR_INVALID_ARG;
+  if (N > 0 && !send_head) return MOE_ERR_INVALID_ARG;
+  const void* ints[] = {send_head, recv_src_idx, recv_offset, recv_tokens_per_expert};
+  for (const void* q : ints)
+    if (!aligned(q, 4)) return MOE_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  bool done = false;
+  if (N > 0) {
+    p.send_head = send_head;
+    p.recv_src_idx = recv_src_idx;
+    p.recv_offset = recv_offset;
+    p.recv_tokens_per_expert = recv_tokens_per_expert;
+    p.expert_alignment = expert_alignment;
+    if (moe::launch_layout(p, s, &done) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    rc = moe_layout(desc, topk_idx, tokens_per_expert, tokens_per_rank, is_token_in_rank, expert_offset,
+                    rank_offset, slot_of, src_of_slot, workspace, ws_bytes, stream);
+    if (rc != MOE_OK) return rc;
+  }
+  if (done) return MOE_OK;
+  // the layout ran as two kernels: the receive layout follows as its own kernel
+  moe::RankLayoutParams rp;
+  rp.is_token_in_rank = is_token_in_rank;
+  rp.tokens_per_rank = tokens_per_rank;
+  rp.tokens_per_expert = tokens_per_expert;
+  rp.send_head = send_head;
+  rp.recv_src_idx = recv_src_idx;
+  rp.recv_offset = recv_offset;
+  rp.recv_tokens_per_expert = recv_tokens_per_expert;
+  rp.num_tokens = N;
+  rp.num_ranks = p.num_ranks;
+  rp.num_experts = p.num_experts;
+  rp.expert_alignment = expert_alignment;
+  return cuda_status(moe::launch_rank_layout(rp, s));
 }
 
 int moe_layout_status(const void* workspace, int32_t* status, moe_stream_t stream) {

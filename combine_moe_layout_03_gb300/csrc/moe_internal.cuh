@@ -28,6 +28,13 @@ struct LayoutParams {
   int32_t* chunk_flag;   // [chunks] invalid-id flags
   int num_tokens, topk, num_experts, num_ranks, experts_per_rank;
   int tokens_per_chunk, num_chunks;
+  // The per-rank receive layout (moe_layout_ranks), computed by the cluster
+  // kernel when send_head is set; null otherwise.
+  int32_t* send_head = nullptr;               // [N, R]
+  int32_t* recv_src_idx = nullptr;            // [N * R], may be null
+  int32_t* recv_offset = nullptr;             // [R + 1]
+  int32_t* recv_tokens_per_expert = nullptr;  // [E]
+  int expert_alignment = 1;
 };
 
 struct DispatchParams {
@@ -152,7 +159,9 @@ constexpr int kLayoutTokensPerChunk = 128;
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 
 // Launchers (return cudaError_t of the launch).
-cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s);
+// ranks_done (may be null) is set when the launch also computed the receive
+// layout of p.send_head; otherwise the caller runs launch_rank_layout.
+cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s, bool* ranks_done = nullptr);
 // after_layout: the previous kernel on s is this library's layout kernel,
 // launched by the same call (moe_layout_dispatch), so the row work may start
 // before it ends.

@@ -95,6 +95,8 @@ _lib.moe_unpack_slots.restype = ctypes.c_int
 _lib.moe_unpack_slots.argtypes = [_SD, _vp, ctypes.POINTER(_vp), _vp]
 _lib.moe_rank_layout.restype = ctypes.c_int
 _lib.moe_rank_layout.argtypes = [_D, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]
+_lib.moe_layout_ranks.restype = ctypes.c_int
+_lib.moe_layout_ranks.argtypes = [_D] + [_vp] * 8 + [_i32] + [_vp] * 5 + [_sz, _vp]
 _lib.moe_dispatch_ranks.restype = ctypes.c_int
 _lib.moe_dispatch_ranks.argtypes = [_D] + [_vp] * 6 + [_sz, _vp]
 _lib.moe_combine_gather_ranks.restype = ctypes.c_int
@@ -315,6 +317,43 @@ def moe_rank_layout(desc: MoeDesc, lay: dict, expert_alignment: int = 1, out: di
                               _ptr(out["recv_tokens_per_expert"]), _stream(stream))
     _check(rc, "moe_rank_layout")
     return out
+
+
+def rank_layout_outputs(desc: MoeDesc, device) -> dict:
+    """Fresh receive-layout output tensors of one call (int32, on device)."""
+    n, r, e = desc.num_tokens, desc.num_ranks, desc.num_experts
+    i32 = dict(dtype=torch.int32, device=device)
+    return dict(send_head=torch.empty((n, r), **i32), recv_src_idx=torch.empty(n * r, **i32),
+                recv_offset=torch.empty(r + 1, **i32), recv_tokens_per_expert=torch.empty(e, **i32))
+
+
+def moe_layout_ranks(desc: MoeDesc, topk_idx: torch.Tensor, expert_alignment: int = 1,
+                     out: dict | None = None, rank_out: dict | None = None, workspace=None,
+                     stream=None) -> tuple[dict, dict]:
+    """moe_layout and moe_rank_layout in one call (see include/moe.h).
+    Returns (layout outputs with the workspace, receive-layout outputs)."""
+    if out is None:
+        out = layout_outputs(desc, topk_idx.device)
+    if rank_out is None:
+        rank_out = rank_layout_outputs(desc, topk_idx.device)
+    if workspace is None:
+        workspace = torch.empty(max(moe_workspace_size(desc), 256), dtype=torch.uint8, device=topk_idx.device)
+    prepare_layout_ranks(desc, topk_idx, expert_alignment, out, rank_out, workspace, stream)()
+    out["workspace"] = workspace
+    return out, rank_out
+
+
+def prepare_layout_ranks(desc: MoeDesc, topk_idx, expert_alignment: int, out: dict, rank_out: dict,
+                         workspace, stream=None) -> Prepared:
+    d = desc.c()
+    args = (ctypes.byref(d),
+            *_vps(topk_idx, out["tokens_per_expert"], out["tokens_per_rank"], out["is_token_in_rank"],
+                  out["expert_offset"], out["rank_offset"], out["slot_of"], out.get("src_of_slot")),
+            ctypes.c_int32(expert_alignment),
+            *_vps(rank_out["send_head"], rank_out.get("recv_src_idx"), rank_out["recv_offset"],
+                  rank_out["recv_tokens_per_expert"], workspace),
+            ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_layout_ranks", args, (d, topk_idx, out, rank_out, workspace))
 
 
 def moe_dispatch_ranks(desc: MoeDesc, topk_idx, topk_weights, hidden, scales, send_head,
@@ -678,4 +717,5 @@ def exported_symbols() -> list[str]:
             "moe_pack_slots", "moe_unpack_slots", "moe_mask_topk_ids", "moe_rank_layout",
             "moe_dispatch_ranks", "moe_combine_gather_ranks", "moe_ll_layout",
             "moe_dispatch_ll", "moe_combine_backward", "moe_dispatch_backward",
-            "moe_combine_gather_ranks_backward", "moe_layout_dispatch", "moe_device_status"]
+            "moe_combine_gather_ranks_backward", "moe_layout_dispatch", "moe_device_status",
+            "moe_layout_ranks"]

@@ -341,6 +341,21 @@ int moe_rank_layout(const moe_desc_t* desc, const uint8_t* is_token_in_rank,
                     int32_t expert_alignment, int32_t* send_head, int32_t* recv_src_idx,
                     int32_t* recv_offset, int32_t* recv_tokens_per_expert, moe_stream_t stream);
 
+/* moe_layout and moe_rank_layout in one call (DeepEP repository,
+ * csrc/deep_ep.cpp Buffer::get_dispatch_layout, then the receive layout of
+ * Buffer::intranode_dispatch). Arguments are those of moe_layout, then
+ * expert_alignment and the receive-layout outputs of moe_rank_layout (which
+ * it computes from this call's layout); every output is the one the two
+ * calls give. Where the layout runs as one cluster launch (every workload of
+ * the pages), the receive layout is computed in that launch from the rank
+ * masks and the per-block rank counts the cluster already exchanges; larger
+ * shapes take the two kernels. Errors: those of the two calls. */
+int moe_layout_ranks(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* tokens_per_expert,
+                     int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
+                     int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot, int32_t expert_alignment,
+                     int32_t* send_head, int32_t* recv_src_idx, int32_t* recv_offset,
+                     int32_t* recv_tokens_per_expert, void* workspace, size_t ws_bytes, moe_stream_t stream);
+
 /* Dispatch with one record per (token, rank) at records + send_head[t, r] *
  * record_bytes (moe_record_layout's format and sizes). The payload and
  * scales are those of moe_dispatch. The first segment differs (reading: the
