@@ -572,7 +572,7 @@ __host__ __device__ inline size_t cluster_smem_ints(int tpb, int k, int E, int R
   return (size_t)kClusterWarps * E4 * (peer_masks ? 2 : 1) + (size_t)tpb * k * (inv ? 2 : 1) +
          tpb * mask_bytes / 4 +
          (size_t)G * E + (size_t)G * (R + 1) + (size_t)kClusterWarps * R + 4 * (size_t)E + 80 +
-         (ranks ? (size_t)((tpb + 31) / 32) * R + 2 * (size_t)R : 0);
+         (ranks ? 2 * (size_t)((tpb + 31) / 32) * R + 3 * (size_t)R + 1 : 0);
 }
 
 // Everything in one launch: a cluster of G blocks (G <= 16), block c owning a
@@ -830,63 +830,83 @@ __global__ void __launch_bounds__(kClusterThreads)
     const int warp = threadIdx.x >> 5, lane = (int)lane_id();
     const int nt = t1 - t0;
     const int nch = (tpb + 31) / 32;
-    int* chc = scratch + 80;  // [nch][R] tokens per rank in each 32-token chunk, then their prefix
-    int* rbase = chc + nch * R;  // [R] slot of the block's first token on each rank
-    int* rall = rbase + R;       // [R] tokens per rank over all blocks
+    unsigned* cbits = reinterpret_cast<unsigned*>(scratch + 80);  // [nch][R] rank-r bits of 32 tokens
+    int* cpre = scratch + 80 + nch * R;  // [nch][R] the block's rank-r tokens before the chunk
+    int* rtot = cpre + nch * R;          // [R] tokens on rank r over all blocks
+    int* rbef = rtot + R;                // [R] ... of the blocks before this one
+    int* rbase = rbef + R;               // [R] slot of the block's first token on rank r
+    int* rtotal = rbase + R;             // [1] receive slots over all ranks
     for (int ch = warp; ch < nch; ch += NW) {
       const int tt = ch * 32 + lane;
       const MASK m = tt < nt ? masks[tt] : (MASK)0;
       for (int r = 0; r < R; ++r) {
         const unsigned bits = __ballot_sync(0xffffffffu, ((m >> r) & 1) != 0);
-        if (lane == 0) chc[ch * R + r] = __popc(bits);
-      }
-    }
-    for (int r = threadIdx.x; r < R; r += blockDim.x) {
-      int all = 0, before = 0;
-      for (int b = 0; b < G; ++b) {
-        const int v = allr[b * (R + 1) + r];
-        all += v;
-        before += b < c ? v : 0;
-      }
-      rall[r] = all;
-      rbase[r] = before;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {  // rank bases: exclusive scan over ranks
-      int run = 0;
-      for (int r = 0; r < R; ++r) {
-        rbase[r] += run;
-        if (c == 0) p.recv_offset[r] = run;
-        run += rall[r];
-      }
-      if (c == 0) p.recv_offset[R] = run;
-      rall[0] = run;  // total receive slots, for the recv_src_idx tail
-    }
-    for (int r = threadIdx.x; r < R; r += blockDim.x) {  // chunk prefixes per rank
-      int run = 0;
-      for (int ch = 0; ch < nch; ++ch) {
-        const int v = chc[ch * R + r];
-        chc[ch * R + r] = run;
-        run += v;
+        if (lane == 0) cbits[ch * R + r] = bits;
       }
     }
     __syncthreads();
-    for (int ch = warp; ch < nch; ch += NW) {
-      const int tt = ch * 32 + lane;
-      const MASK m = tt < nt ? masks[tt] : (MASK)0;
-      for (int r = 0; r < R; ++r) {
-        const bool in = ((m >> r) & 1) != 0;
-        const unsigned bits = __ballot_sync(0xffffffffu, in);
-        if (tt < nt) {
-          const int slot = in ? rbase[r] + chc[ch * R + r] + __popc(bits & ((1u << lane) - 1u)) : -1;
-          p.send_head[(int64_t)(t0 + tt) * R + r] = slot;
-          if (in && p.recv_src_idx) p.recv_src_idx[slot] = t0 + tt;
-        }
+    // one warp per rank: prefix over the chunks (lanes = chunks), and the
+    // rank's totals over all blocks and over the earlier ones (lanes = blocks)
+    for (int r = warp; r < R; r += NW) {
+      int carry = 0;
+      for (int ch0 = 0; ch0 < nch; ch0 += 32) {
+        const int ch = ch0 + lane;
+        const int v = ch < nch ? __popc(cbits[ch * R + r]) : 0;
+        const int inc = warp_inclusive_scan(v);
+        if (ch < nch) cpre[ch * R + r] = carry + inc - v;
+        carry += __shfl_sync(0xffffffffu, inc, 31);
       }
+      const int a = lane < G ? allr[lane * (R + 1) + r] : 0;  // G <= 16
+      const int tot = __reduce_add_sync(0xffffffffu, a);
+      const int bef = __reduce_add_sync(0xffffffffu, lane < c ? a : 0);
+      if (lane == 0) {
+        rtot[r] = tot;
+        rbef[r] = bef;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {  // rank bases: exclusive scan of the rank totals (R <= 64)
+      const int v0 = lane < R ? rtot[lane] : 0, v1 = lane + 32 < R ? rtot[lane + 32] : 0;
+      const int i0 = warp_inclusive_scan(v0), i1 = warp_inclusive_scan(v1);
+      const int s0 = __shfl_sync(0xffffffffu, i0, 31);
+      const int e0 = i0 - v0, e1 = s0 + i1 - v1;
+      if (lane < R) {
+        rbase[lane] = e0 + rbef[lane];
+        if (c == 0) p.recv_offset[lane] = e0;
+      }
+      if (lane + 32 < R) {
+        rbase[lane + 32] = e1 + rbef[lane + 32];
+        if (c == 0) p.recv_offset[lane + 32] = e1;
+      }
+      const int total = s0 + __shfl_sync(0xffffffffu, i1, 31);
+      if (lane == 0) {
+        *rtotal = total;
+        if (c == 0) p.recv_offset[R] = total;
+      }
+    }
+    __syncthreads();
+    // send_head rows of the block's tokens: one contiguous run, coalesced
+    const bool pow2 = (R & (R - 1)) == 0;
+    const int sh_r = 31 - __clz(R);
+    int32_t* shd = p.send_head + (int64_t)t0 * R;
+    for (int i = threadIdx.x; i < nt * R; i += blockDim.x) {
+      const int tt = pow2 ? (i >> sh_r) : (i / R), r = i - tt * R;
+      const unsigned w = cbits[(tt >> 5) * R + r];
+      const int l = tt & 31;
+      shd[i] = ((w >> l) & 1u) ? rbase[r] + cpre[(tt >> 5) * R + r] + __popc(w & ((1u << l) - 1u)) : -1;
     }
     if (p.recv_src_idx) {
+      // rank by rank, so each rank's run of slots is written in order
+      for (int r = 0; r < R; ++r) {
+        for (int tt = threadIdx.x; tt < nt; tt += blockDim.x) {
+          const unsigned w = cbits[(tt >> 5) * R + r];
+          const int l = tt & 31;
+          if ((w >> l) & 1u)
+            p.recv_src_idx[rbase[r] + cpre[(tt >> 5) * R + r] + __popc(w & ((1u << l) - 1u))] = t0 + tt;
+        }
+      }
       const int64_t cap = (int64_t)p.num_tokens * R;
-      for (int64_t q = (int64_t)rall[0] + (int64_t)c * blockDim.x + threadIdx.x; q < cap;
+      for (int64_t q = (int64_t)*rtotal + (int64_t)c * blockDim.x + threadIdx.x; q < cap;
            q += (int64_t)G * blockDim.x)
         p.recv_src_idx[q] = -1;
     }
