@@ -383,8 +383,8 @@ class Step:
         )
 
     def _setup_ll(self, spec, dev):
-        """Fixed-capacity, expert-major buffers: the LL layout runs after the
-        layout (both timed as 'layout'), the payload and scales go to
+        """Fixed-capacity, expert-major buffers: the layout and the fixed-capacity
+        layout in one call (moe_layout_ll, timed as 'layout'), the payload and scales go to
         [E * capacity] rows, and the expert of each position returns its
         dequantised row; the combine is the top-k reduction over those rows."""
         import torch
@@ -408,11 +408,13 @@ class Step:
         self.y[pos] = (q.float() * sc.repeat_interleave(128, dim=1)).to(torch.bfloat16)
         self.max_t = max_t
         self.calls_on = self._ll_calls_on
-        lp, llp, dp, cp = self._ll_calls_on(torch.cuda.current_stream())
-        self.layout = lambda: (lp(), llp())
+        lp, dp, cp = self._ll_calls_on(torch.cuda.current_stream())
+        self.layout = lp
         self.dispatch, self.combine = dp, cp
-        self.launches_per_step = layout_launches(spec["num_tokens"], spec["topk"],
-                                                 spec["num_experts"], spec["num_ranks"]) + 3
+        # the fixed-capacity layout runs inside the cluster layout launch (this
+        # workload's source ranks are whole blocks), or after the two-kernel one
+        nl = layout_launches(spec["num_tokens"], spec["topk"], spec["num_experts"], spec["num_ranks"])
+        self.launches_per_step = nl + (0 if nl == 1 else 1) + 2
 
     def _setup_bwd(self, spec, dev, seed):
         """The backward step with the forward's slot map cached: the upstream
@@ -448,8 +450,7 @@ class Step:
     def _ll_calls_on(self, stream):
         moe = self.moe
         h = stream.cuda_stream
-        return [moe.prepare_layout(self.desc, self.ids, self.lay, self.ws, h),
-                moe.prepare_ll_layout(self.desc, self.max_t, self.ids, self.lay, self.ll, h),
+        return [moe.prepare_layout_ll(self.desc, self.max_t, self.ids, self.lay, self.ll, self.ws, h),
                 moe.prepare_dispatch_ll(self.desc, self.x, self.sc, self.ll["ll_slot_of"],
                                         self.x_ll, self.s_ll, h),
                 moe.prepare_combine(self.cdesc, moe.MOE_COMBINE_TOPK, self.y, self.ids, self.w,

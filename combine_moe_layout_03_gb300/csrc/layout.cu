@@ -566,13 +566,17 @@ __device__ __forceinline__ void st_cluster_s32(int* local_addr, unsigned rank, i
 
 // Shared memory of k_layout_cluster, in ints (MASK words rounded to ints),
 // plus the per-chunk rank counts of the receive layout when it is computed.
+__host__ __device__ inline size_t cluster_rank_ints(int tpb, int R) {
+  return 2 * (size_t)((tpb + 31) / 32) * R + 3 * (size_t)R + 1;
+}
 __host__ __device__ inline size_t cluster_smem_ints(int tpb, int k, int E, int R, int G, bool inv,
-                                                    size_t mask_bytes, bool peer_masks, bool ranks = false) {
+                                                    size_t mask_bytes, bool peer_masks, bool ranks = false,
+                                                    bool ll = false) {
   const size_t E4 = (size_t)((E + 3) & ~3);
   return (size_t)kClusterWarps * E4 * (peer_masks ? 2 : 1) + (size_t)tpb * k * (inv ? 2 : 1) +
          tpb * mask_bytes / 4 +
          (size_t)G * E + (size_t)G * (R + 1) + (size_t)kClusterWarps * R + 4 * (size_t)E + 80 +
-         (ranks ? 2 * (size_t)((tpb + 31) / 32) * R + 3 * (size_t)R + 1 : 0);
+         (ranks ? cluster_rank_ints(tpb, R) : 0) + (ll ? (size_t)E : 0);
 }
 
 // Everything in one launch: a cluster of G blocks (G <= 16), block c owning a
@@ -603,6 +607,13 @@ __host__ __device__ inline size_t cluster_smem_ints(int tpb, int k, int E, int R
 //     every block has received all blocks' tokens-per-rank counts in step 4,
 //     which give each rank's base and this block's prefix; warp ballots over
 //     32-token chunks of the rank masks give the positions inside the block.
+//  8. With p.ll_slot_of set (moe_layout_ll; the plan then makes every source
+//     rank's T tokens a whole number of blocks), the fixed-capacity layout:
+//     step 6 writes each pair's position slot - expert_offset[e] (if inside
+//     the capacity) and src_info; every block holds all blocks' expert counts,
+//     so one warp per owned expert scans them over the blocks into the
+//     (source rank) ranges and the receive count, and clears the expert's
+//     unused positions.
 // No workspace is used except the status word.
 template <typename MASK, int L>
 __global__ void __launch_bounds__(kClusterThreads)
@@ -637,6 +648,8 @@ __global__ void __launch_bounds__(kClusterThreads)
   int* delta = loff + E;              // [E] slot = delta[e] + position
   int* rank_of = delta + E;           // [E]
   int* scratch = rank_of + E;         // [80]
+  // [E] expert offsets (fixed-capacity layout), after the receive-layout area
+  int* eoff = scratch + 80 + (p.send_head ? (int)cluster_rank_ints(tpb, R) : 0);
   __shared__ int s_bad;
   const int t0 = min(c * tpb, p.num_tokens);
   const int t1 = min(t0 + tpb, p.num_tokens);
@@ -746,6 +759,7 @@ __global__ void __launch_bounds__(kClusterThreads)
     if (i < ept && e < E) {
       loff[e] = ex.y;
       delta[e] = ex.x + pre[i] - ex.y;
+      if (p.ll_slot_of) eoff[e] = ex.x;
       if (c == 0) {
         p.tokens_per_expert[e] = tot[i];
         p.expert_offset[e] = ex.x;
@@ -792,6 +806,18 @@ __global__ void __launch_bounds__(kClusterThreads)
         else if (p.src_of_slot) p.src_of_slot[slot] = (int32_t)(p0 + q);
       }
       p.slot_of[p0 + q] = slot;
+      if (p.ll_slot_of) {  // fixed-capacity position, in source-rank then token order
+        int32_t pos = -1;
+        if (e >= 0) {
+          const int within = slot - eoff[e];
+          if (within < p.ll_capacity) {
+            pos = (int32_t)((int64_t)e * p.ll_capacity + within);
+            const int t = t0 + q / k;
+            p.src_info[pos] = t % p.ll_tokens_per_rank;
+          }
+        }
+        p.ll_slot_of[p0 + q] = pos;
+      }
     }
   }
   {  // is_token_in_rank rows of the block's tokens
@@ -911,6 +937,35 @@ __global__ void __launch_bounds__(kClusterThreads)
         p.recv_src_idx[q] = -1;
     }
   }
+
+  // 8.
+  if (p.ll_slot_of) {
+    const int warp = threadIdx.x >> 5, lane = (int)lane_id();
+    const int64_t cap = p.ll_capacity;
+    const int bps = p.ll_tokens_per_rank / tpb;  // blocks per source rank
+    for (int e = c + warp * G; e < E; e += NW * G) {
+      // lane b: expert e's pairs in blocks before b (G <= 16 lanes)
+      const int v = lane < G ? allcnt[lane * E + e] : 0;
+      const int inc = warp_inclusive_scan(v);
+      const int total = __shfl_sync(0xffffffffu, inc, 31);
+      const int excl = inc - v;
+      // ranks lane and lane + 32: begin at block s * bps, end at block (s + 1) * bps
+      for (int h = 0; h < 2; ++h) {
+        const int sr = lane + 32 * h;
+        const int bb = sr * bps, be = (sr + 1) * bps;
+        const int b0 = __shfl_sync(0xffffffffu, excl, bb < G ? bb : 0);
+        const int b1 = __shfl_sync(0xffffffffu, excl, be < G ? be : 0);
+        if (sr < R) {
+          const int64_t lo = bb < G ? b0 : total, hi = be < G ? b1 : total;
+          const int64_t c0 = lo < cap ? lo : cap, c1 = hi < cap ? hi : cap;
+          p.layout_range[(int64_t)e * R + sr] = (c0 << 32) | (c1 - c0);
+        }
+      }
+      const int64_t used = total < cap ? total : cap;
+      if (lane == 0) p.recv_count[e] = (int32_t)used;
+      for (int64_t i = used + lane; i < cap; i += 32) p.src_info[(int64_t)e * cap + i] = -1;
+    }
+  }
 }
 
 }  // namespace
@@ -945,7 +1000,7 @@ static const void* cluster_kernel(bool wide, int lanes) {
 // non-portable cluster of 16 (looked up once per device), else 8.
 struct ClusterPlan {
   int blocks, tokens_per_block, lanes;
-  bool wide, use_inv, use_or;
+  bool wide, use_inv, use_or, ll;
   size_t smem;
 };
 
@@ -990,8 +1045,12 @@ static int max_cluster_blocks() {
   return g_cluster_blocks[dev];
 }
 
+// ll_T > 0 (the fixed-capacity layout, T tokens per source rank): tokens per
+// block become a divisor of T, so every source rank is a whole number of
+// blocks; cp.ll stays false (and the plan is the plain one) if no divisor
+// fits the cluster.
 static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int num_ranks, bool want_inv,
-                                int gmax, bool ranks = false) {
+                                int gmax, bool ranks = false, int ll_T = 0) {
   // about kPairsPerClusterBlock pairs per block, but small inputs still
   // spread over up to gmax blocks of at least kMinPairsPerClusterBlock
   const int64_t pairs = (int64_t)num_tokens * topk;
@@ -1002,7 +1061,20 @@ static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int n
   g = g < 1 ? 1 : (g > gmax ? gmax : g);
   int tpb = (num_tokens + g - 1) / g;
   tpb = (tpb + 3) / 4 * 4;  // 16-byte aligned id runs per block
+  bool ll = false;
+  if (ll_T > 0) {
+    const int lo = tpb > (num_tokens + gmax - 1) / gmax ? tpb : (num_tokens + gmax - 1) / gmax;
+    for (int d = lo; d <= ll_T; ++d) {
+      if (ll_T % d == 0 && (d * topk) % 4 == 0) {
+        tpb = d;
+        g = num_tokens / d;
+        ll = true;
+        break;
+      }
+    }
+  }
   ClusterPlan cp;
+  cp.ll = ll;
   cp.blocks = g;
   cp.tokens_per_block = tpb;
   cp.wide = num_ranks > 32;
@@ -1012,24 +1084,29 @@ static ClusterPlan cluster_plan(int num_tokens, int topk, int num_experts, int n
   const size_t mb = cp.wide ? 8 : 4;
   // peer masks in shared memory when they fit, then the inverse map for
   // coalesced src_of_slot stores when that fits too
-  cp.use_or = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, false, mb, true, ranks) * 4 <= kClusterMaxSmem;
-  cp.use_inv = want_inv && cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, true, mb, cp.use_or, ranks) * 4 <=
-                               kClusterMaxSmem;
-  cp.smem = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, cp.use_inv, mb, cp.use_or, ranks) * 4;
+  cp.use_or = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, false, mb, true, ranks, ll) * 4 <=
+              kClusterMaxSmem;
+  cp.use_inv = want_inv && cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, true, mb, cp.use_or, ranks,
+                                             ll) * 4 <= kClusterMaxSmem;
+  cp.smem = cluster_smem_ints(tpb, topk, num_experts, num_ranks, g, cp.use_inv, mb, cp.use_or, ranks, ll) * 4;
   return cp;
 }
 
-cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s, bool* ranks_done) {
+cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s, bool* extra_done) {
   const int E = p.num_experts, R = p.num_ranks;
-  const ClusterPlan cp = cluster_plan(p.num_tokens, p.topk, E, R, p.src_of_slot != nullptr, max_cluster_blocks(),
-                                      p.send_head != nullptr);
-  if (ranks_done) *ranks_done = false;
+  ClusterPlan cp = cluster_plan(p.num_tokens, p.topk, E, R, p.src_of_slot != nullptr, max_cluster_blocks(),
+                                p.send_head != nullptr, p.ll_slot_of ? p.ll_tokens_per_rank : 0);
+  if (p.ll_slot_of && (!cp.ll || cp.smem > kClusterMaxSmem))  // the plain plan; the caller adds the kernel
+    cp = cluster_plan(p.num_tokens, p.topk, E, R, p.src_of_slot != nullptr, max_cluster_blocks(),
+                      p.send_head != nullptr);
+  if (extra_done) *extra_done = false;
   if (cp.smem <= kClusterMaxSmem) {
-    if (ranks_done) *ranks_done = p.send_head != nullptr;
     const void* fn = cluster_kernel(cp.wide, cp.lanes);
     cudaError_t err = set_smem(fn, cp.smem);
     if (err != cudaSuccess) return err;
     LayoutParams q = p;
+    if (!cp.ll) q.ll_slot_of = nullptr;
+    if (extra_done) *extra_done = q.send_head != nullptr || q.ll_slot_of != nullptr;
     int tpb = cp.tokens_per_block;
     int use_inv = cp.use_inv ? 1 : 0, use_or = cp.use_or ? 1 : 0;
     void* args[] = {&q, &tpb, &use_inv, &use_or};
@@ -1040,7 +1117,8 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s, bool* ranks_don
   cudaError_t err = set_smem((const void*)k_layout_count, smem_count);
   if (err != cudaSuccess) return err;
   LayoutParams q = p;
-  q.send_head = nullptr;  // the two-kernel path leaves the receive layout to the caller
+  q.send_head = nullptr;  // the two-kernel path leaves the receive layouts to the caller
+  q.ll_slot_of = nullptr;
   void* args[] = {&q};
   err = launch_pdl((const void*)k_layout_count, dim3(p.num_chunks), dim3(kCountThreads), smem_count, s,
                    args);

@@ -311,6 +311,46 @@ int moe_layout_ranks(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* t
   return cuda_status(moe::launch_rank_layout(rp, s));
 }
 
+int moe_layout_ll(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* tokens_per_expert,
+                  int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
+                  int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot, int32_t max_tokens_per_rank,
+                  int32_t* ll_slot_of, int32_t* src_info, int64_t* layout_range, int32_t* recv_count,
+                  void* workspace, size_t ws_bytes, moe_stream_t stream) {
+  moe::LayoutParams p;
+  int rc = layout_params(desc, topk_idx, tokens_per_expert, tokens_per_rank, is_token_in_rank,
+                         expert_offset, rank_offset, slot_of, src_of_slot, workspace, ws_bytes, &p);
+  if (rc != MOE_OK) return rc;
+  const int N = p.num_tokens, R = p.num_ranks;
+  if (max_tokens_per_rank < 1 || N % R || N / R > max_tokens_per_rank) return MOE_ERR_SHAPE;
+  const int64_t cap = (int64_t)R * max_tokens_per_rank;
+  if ((int64_t)p.num_experts * cap >= ((int64_t)1 << 31)) return MOE_ERR_SHAPE;
+  if (!src_info || !layout_range || !recv_count) return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!ll_slot_of || !src_of_slot)) return MOE_ERR_INVALID_ARG;
+  const void* ints[] = {ll_slot_of, src_info, recv_count};
+  for (const void* q : ints)
+    if (!aligned(q, 4)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(layout_range, 8)) return MOE_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  bool done = false;
+  if (N > 0) {
+    p.ll_slot_of = ll_slot_of;
+    p.src_info = src_info;
+    p.layout_range = layout_range;
+    p.recv_count = recv_count;
+    p.ll_capacity = cap;
+    p.ll_tokens_per_rank = N / R;
+    if (moe::launch_layout(p, s, &done) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    rc = moe_layout(desc, topk_idx, tokens_per_expert, tokens_per_rank, is_token_in_rank, expert_offset,
+                    rank_offset, slot_of, src_of_slot, workspace, ws_bytes, stream);
+    if (rc != MOE_OK) return rc;
+  }
+  if (done) return MOE_OK;
+  // the cluster launch did not take it: the fixed-capacity layout as its own kernel
+  return moe_ll_layout(desc, max_tokens_per_rank, topk_idx, slot_of, expert_offset, src_of_slot, ll_slot_of,
+                       src_info, layout_range, recv_count, stream);
+}
+
 int moe_layout_status(const void* workspace, int32_t* status, moe_stream_t stream) {
   if (!workspace || !status) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;

@@ -35,6 +35,14 @@ struct LayoutParams {
   int32_t* recv_offset = nullptr;             // [R + 1]
   int32_t* recv_tokens_per_expert = nullptr;  // [E]
   int expert_alignment = 1;
+  // The fixed-capacity, expert-major layout (moe_layout_ll), computed by the
+  // cluster kernel when ll_slot_of is set; null otherwise.
+  int32_t* ll_slot_of = nullptr;    // [N, k]
+  int32_t* src_info = nullptr;      // [E, ll_capacity]
+  int64_t* layout_range = nullptr;  // [E, R]
+  int32_t* recv_count = nullptr;    // [E]
+  int64_t ll_capacity = 0;          // R * max_tokens_per_rank
+  int ll_tokens_per_rank = 0;       // T = N / R
 };
 
 struct DispatchParams {
@@ -159,9 +167,10 @@ constexpr int kLayoutTokensPerChunk = 128;
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 
 // Launchers (return cudaError_t of the launch).
-// ranks_done (may be null) is set when the launch also computed the receive
-// layout of p.send_head; otherwise the caller runs launch_rank_layout.
-cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s, bool* ranks_done = nullptr);
+// extra_done (may be null) is set when the launch also computed the receive
+// layout of p.send_head or the fixed-capacity layout of p.ll_slot_of;
+// otherwise the caller runs launch_rank_layout or launch_ll_layout.
+cudaError_t launch_layout(const LayoutParams& p, cudaStream_t s, bool* extra_done = nullptr);
 // after_layout: the previous kernel on s is this library's layout kernel,
 // launched by the same call (moe_layout_dispatch), so the row work may start
 // before it ends.

@@ -95,6 +95,8 @@ _lib.moe_unpack_slots.restype = ctypes.c_int
 _lib.moe_unpack_slots.argtypes = [_SD, _vp, ctypes.POINTER(_vp), _vp]
 _lib.moe_rank_layout.restype = ctypes.c_int
 _lib.moe_rank_layout.argtypes = [_D, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]
+_lib.moe_layout_ll.restype = ctypes.c_int
+_lib.moe_layout_ll.argtypes = [_D] + [_vp] * 8 + [_i32] + [_vp] * 5 + [_sz, _vp]
 _lib.moe_layout_ranks.restype = ctypes.c_int
 _lib.moe_layout_ranks.argtypes = [_D] + [_vp] * 8 + [_i32] + [_vp] * 5 + [_sz, _vp]
 _lib.moe_dispatch_ranks.restype = ctypes.c_int
@@ -448,6 +450,44 @@ def moe_ll_layout(desc: MoeDesc, max_tokens_per_rank: int, topk_idx, lay: dict,
     return out
 
 
+def ll_layout_outputs(desc: MoeDesc, max_tokens_per_rank: int, device) -> dict:
+    """Fresh fixed-capacity layout output tensors of one call (on device)."""
+    n, k, e, r = desc.num_tokens, desc.topk, desc.num_experts, desc.num_ranks
+    cap = r * max_tokens_per_rank
+    return dict(ll_slot_of=torch.empty((n, k), dtype=torch.int32, device=device),
+                src_info=torch.empty((e, cap), dtype=torch.int32, device=device),
+                layout_range=torch.empty((e, r), dtype=torch.int64, device=device),
+                recv_count=torch.empty(e, dtype=torch.int32, device=device), capacity=cap)
+
+
+def moe_layout_ll(desc: MoeDesc, max_tokens_per_rank: int, topk_idx: torch.Tensor, out: dict | None = None,
+                  ll_out: dict | None = None, workspace=None, stream=None) -> tuple[dict, dict]:
+    """moe_layout and moe_ll_layout in one call (see include/moe.h).
+    Returns (layout outputs with the workspace, fixed-capacity outputs)."""
+    if out is None:
+        out = layout_outputs(desc, topk_idx.device)
+    if ll_out is None:
+        ll_out = ll_layout_outputs(desc, max_tokens_per_rank, topk_idx.device)
+    if workspace is None:
+        workspace = torch.empty(max(moe_workspace_size(desc), 256), dtype=torch.uint8, device=topk_idx.device)
+    prepare_layout_ll(desc, max_tokens_per_rank, topk_idx, out, ll_out, workspace, stream)()
+    out["workspace"] = workspace
+    return out, ll_out
+
+
+def prepare_layout_ll(desc: MoeDesc, max_tokens_per_rank: int, topk_idx, out: dict, ll_out: dict, workspace,
+                      stream=None) -> Prepared:
+    d = desc.c()
+    args = (ctypes.byref(d),
+            *_vps(topk_idx, out["tokens_per_expert"], out["tokens_per_rank"], out["is_token_in_rank"],
+                  out["expert_offset"], out["rank_offset"], out["slot_of"], out.get("src_of_slot")),
+            ctypes.c_int32(max_tokens_per_rank),
+            *_vps(ll_out["ll_slot_of"], ll_out["src_info"], ll_out["layout_range"], ll_out["recv_count"],
+                  workspace),
+            ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_layout_ll", args, (d, topk_idx, out, ll_out, workspace))
+
+
 def moe_dispatch_ll(desc: MoeDesc, hidden, scales, ll_slot_of, capacity: int,
                     x_out=None, scales_out=None, stream=None):
     """Payload and scales into [E * capacity, ...] buffers; returns (x_out, scales_out)."""
@@ -718,4 +758,4 @@ def exported_symbols() -> list[str]:
             "moe_dispatch_ranks", "moe_combine_gather_ranks", "moe_ll_layout",
             "moe_dispatch_ll", "moe_combine_backward", "moe_dispatch_backward",
             "moe_combine_gather_ranks_backward", "moe_layout_dispatch", "moe_device_status",
-            "moe_layout_ranks"]
+            "moe_layout_ranks", "moe_layout_ll"]

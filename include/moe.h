@@ -408,6 +408,21 @@ int moe_ll_layout(const moe_desc_t* desc, int32_t max_tokens_per_rank, const int
                   const int32_t* src_of_slot, int32_t* ll_slot_of, int32_t* src_info,
                   int64_t* layout_range, int32_t* recv_count, moe_stream_t stream);
 
+/* moe_layout and moe_ll_layout in one call. Arguments are those of moe_layout
+ * (src_of_slot required), then max_tokens_per_rank and the outputs of
+ * moe_ll_layout, which it computes from this call's layout; every output is
+ * the one the two calls give. Where the layout runs as one cluster launch and
+ * a source rank's T = N / R tokens can be a whole number of its blocks (the
+ * low-latency decode workload of the pages: 8 x 128 tokens), the fixed-capacity
+ * layout is computed in that launch from the expert counts every block of the
+ * cluster already holds; otherwise the two calls' kernels run in turn. Needs
+ * N % R == 0 and N / R <= max_tokens_per_rank. Errors: those of the two calls. */
+int moe_layout_ll(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* tokens_per_expert,
+                  int32_t* tokens_per_rank, uint8_t* is_token_in_rank, int32_t* expert_offset,
+                  int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot, int32_t max_tokens_per_rank,
+                  int32_t* ll_slot_of, int32_t* src_info, int64_t* layout_range, int32_t* recv_count,
+                  void* workspace, size_t ws_bytes, moe_stream_t stream);
+
 /* Dispatch into the fixed-capacity buffers: the payload of moe_dispatch
  * (quantised once per token) goes to row ll_slot_of[t, j] of x_out
  * [E * capacity, payload_bytes] and its scales to the same row of scales_out
