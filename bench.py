@@ -366,9 +366,7 @@ class Step:
         self.y = (q.float() * sc.repeat_interleave(128, dim=1) * lw.sum(1, keepdim=True)).to(torch.bfloat16)
         self.recv_records = recv
         import torch
-        lp, dp, cp = self._rank_calls_on(torch.cuda.current_stream())
-        self.layout = lp
-        self.dispatch, self.combine = dp, cp
+        self.layout, self.dispatch, self.combine = self._rank_calls_on(torch.cuda.current_stream())
         # the receive layout runs inside the cluster layout launch, or as a
         # third kernel after the two-kernel layout
         nl = layout_launches(n, spec["topk"], spec["num_experts"], spec["num_ranks"])
@@ -408,9 +406,13 @@ class Step:
         self.y[pos] = (q.float() * sc.repeat_interleave(128, dim=1)).to(torch.bfloat16)
         self.max_t = max_t
         self.calls_on = self._ll_calls_on
-        lp, dp, cp = self._ll_calls_on(torch.cuda.current_stream())
-        self.layout = lp
-        self.dispatch, self.combine = dp, cp
+        h = torch.cuda.current_stream().cuda_stream
+        self.layout = moe.prepare_layout_ll(self.desc, self.max_t, self.ids, self.lay, self.ll, self.ws, h)
+        self.dispatch = moe.prepare_dispatch_ll(self.desc, self.x, self.sc, self.ll["ll_slot_of"],
+                                                self.x_ll, self.s_ll, h)
+        # the step runs layout and dispatch as one call (the breakdown times
+        # them apart)
+        self.layout_dispatch, self.combine = self._ll_calls_on(torch.cuda.current_stream())
         # the fixed-capacity layout runs inside the cluster layout launch (this
         # workload's source ranks are whole blocks), or after the two-kernel one
         nl = layout_launches(spec["num_tokens"], spec["topk"], spec["num_experts"], spec["num_ranks"])
@@ -450,9 +452,8 @@ class Step:
     def _ll_calls_on(self, stream):
         moe = self.moe
         h = stream.cuda_stream
-        return [moe.prepare_layout_ll(self.desc, self.max_t, self.ids, self.lay, self.ll, self.ws, h),
-                moe.prepare_dispatch_ll(self.desc, self.x, self.sc, self.ll["ll_slot_of"],
-                                        self.x_ll, self.s_ll, h),
+        return [moe.prepare_layout_ll_dispatch(self.desc, self.max_t, self.ids, self.x, self.sc, self.lay,
+                                               self.ll, self.ws, self.x_ll, self.s_ll, h),
                 moe.prepare_combine(self.cdesc, moe.MOE_COMBINE_TOPK, self.y, self.ids, self.w,
                                     self.ll["ll_slot_of"], self.out, h)]
 

@@ -518,11 +518,15 @@ __global__ void __launch_bounds__(kDispatchThreads)
 // pair (t, j) goes to row pos = slot_of[t, j] of x_out [rows, payload_bytes]
 // and of scales_out [rows, scale_bytes rounded up to 16] (pad bytes zero). The payload is built once per token
 // in shared memory as above; thread j issues the two bulk stores.
-template <int OUT_KIND>
+// EARLY (moe_layout_ll_dispatch only): as in k_dispatch_ranks, the payload is
+// built before griddepcontrol.wait and the positions read after it.
+template <int OUT_KIND, bool EARLY = false>
 __global__ void __launch_bounds__(kDispatchThreads)
     k_dispatch_packed(DispatchParams p, uint8_t* x_out, uint8_t* scales_out, int64_t rows) {
-  pdl_wait();
-  pdl_trigger();
+  if (!EARLY) {
+    pdl_wait();
+    pdl_trigger();
+  }
   extern __shared__ __align__(128) uint8_t img[];  // payload | scales | staged row
   __shared__ int s_pos[MOE_MAX_TOPK];
   const int t = blockIdx.x;
@@ -540,7 +544,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
     if (OUT_KIND == MOE_PAYLOAD_RAW && sb > 0)
       copy_g2s_async(img + pb, p.scales + (size_t)t * p.in_scale_bytes, sb / 16);
   }
-  if (threadIdx.x < k) {
+  if (!EARLY && threadIdx.x < k) {
     const int pos = p.slot_of[(int64_t)t * k + threadIdx.x];
     s_pos[threadIdx.x] = (pos >= 0 && (int64_t)pos < rows) ? pos : -1;
   }
@@ -555,6 +559,14 @@ __global__ void __launch_bounds__(kDispatchThreads)
     quant_fp8_ue8m0(stage, p.hidden_size, img, img + pb);
   }
   fence_proxy_async_smem();
+  if (EARLY) {
+    pdl_wait();  // the layout has completed: the positions are final
+    pdl_trigger();
+    if (threadIdx.x < k) {
+      const int pos = p.slot_of[(int64_t)t * k + threadIdx.x];
+      s_pos[threadIdx.x] = (pos >= 0 && (int64_t)pos < rows) ? pos : -1;
+    }
+  }
   __syncthreads();
   if (threadIdx.x < k) {
     const int pos = s_pos[threadIdx.x];
@@ -642,6 +654,17 @@ cudaError_t launch_layout_dispatch_small(const DispatchParams& p, const LayoutPa
   return launch_pdl(fn, dim3((unsigned)p.num_tokens), dim3(kDispatchThreads), smem, s, args);
 }
 
+template <bool EARLY>
+const void* dispatch_packed_kernel(int out_kind) {
+  switch (out_kind) {
+    case MOE_PAYLOAD_BF16: return (const void*)k_dispatch_packed<MOE_PAYLOAD_BF16, EARLY>;
+    case MOE_PAYLOAD_FP8_E4M3_B128: return (const void*)k_dispatch_packed<MOE_PAYLOAD_FP8_E4M3_B128, EARLY>;
+    case MOE_PAYLOAD_NVFP4_B16: return (const void*)k_dispatch_packed<MOE_PAYLOAD_NVFP4_B16, EARLY>;
+    case MOE_PAYLOAD_FP8_E4M3_UE8M0: return (const void*)k_dispatch_packed<MOE_PAYLOAD_FP8_E4M3_UE8M0, EARLY>;
+    default: return (const void*)k_dispatch_packed<MOE_PAYLOAD_RAW, EARLY>;
+  }
+}
+
 cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const int32_t* send_head,
                                   int num_ranks, int experts_per_rank, cudaStream_t s) {
   const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16 ||
@@ -665,19 +688,13 @@ cudaError_t launch_dispatch_ranks(const DispatchParams& p, int out_kind, const i
 }
 
 cudaError_t launch_dispatch_packed(const DispatchParams& p, int out_kind, uint8_t* x_out,
-                                   uint8_t* scales_out, int64_t rows, cudaStream_t s) {
+                                   uint8_t* scales_out, int64_t rows, cudaStream_t s, bool after_layout) {
   const bool quant = out_kind == MOE_PAYLOAD_FP8_E4M3_B128 || out_kind == MOE_PAYLOAD_NVFP4_B16 ||
                      out_kind == MOE_PAYLOAD_FP8_E4M3_UE8M0;
   const size_t smem = (size_t)p.payload_bytes + (size_t)((p.scale_bytes + 15) & ~15) +
                       (quant ? (size_t)p.in_row_bytes : 0);
-  const void* fn = nullptr;
-  switch (out_kind) {
-    case MOE_PAYLOAD_BF16: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_BF16>; break;
-    case MOE_PAYLOAD_FP8_E4M3_B128: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_FP8_E4M3_B128>; break;
-    case MOE_PAYLOAD_NVFP4_B16: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_NVFP4_B16>; break;
-    case MOE_PAYLOAD_FP8_E4M3_UE8M0: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_FP8_E4M3_UE8M0>; break;
-    default: fn = (const void*)k_dispatch_packed<MOE_PAYLOAD_RAW>; break;
-  }
+  const void* fn = after_layout && pdl_enabled() ? dispatch_packed_kernel<true>(out_kind)
+                                                 : dispatch_packed_kernel<false>(out_kind);
   cudaError_t err = ensure_dynamic_smem(fn, smem);
   if (err != cudaSuccess) return err;
   DispatchParams q = p;

@@ -575,14 +575,20 @@ int moe_rank_layout(const moe_desc_t* desc, const uint8_t* is_token_in_rank,
   return cuda_status(moe::launch_rank_layout(p, (cudaStream_t)stream));
 }
 
-int moe_dispatch_ranks(const moe_desc_t* desc, const int32_t* topk_idx,
-                       const float* topk_weights, const void* hidden, const void* scales,
-                       const int32_t* send_head, void* records, size_t records_bytes,
-                       moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates moe_dispatch_ranks' arguments and fills its launch parameters;
+// *empty is set when there is no work.
+int dispatch_ranks_params(const moe_desc_t* desc, const int32_t* topk_idx, const float* topk_weights,
+                          const void* hidden, const void* scales, const int32_t* send_head, void* records,
+                          size_t records_bytes, moe::DispatchParams* p, bool* empty) {
   moe_record_layout_t lay;
   int rc = record_layout(desc, &lay);
   if (rc != MOE_OK) return rc;
   const int N = desc->num_tokens;
+  *empty = N == 0;
   if (N == 0) return MOE_OK;
   const bool raw = desc->out_kind == MOE_PAYLOAD_RAW;
   if (!topk_idx || !topk_weights || !hidden || !send_head || !records) return MOE_ERR_INVALID_ARG;
@@ -592,26 +598,41 @@ int moe_dispatch_ranks(const moe_desc_t* desc, const int32_t* topk_idx,
   if (!aligned(hidden, 16) || !aligned(records, 16) || (raw && scales && !aligned(scales, 16)))
     return MOE_ERR_ALIGNMENT;
   if (records_bytes < (size_t)lay.record_bytes) return MOE_ERR_CAPACITY;
+  p->topk_idx = topk_idx;
+  p->topk_weights = topk_weights;
+  p->hidden = (const uint8_t*)hidden;
+  p->scales = (const uint8_t*)scales;
+  p->slot_of = nullptr;
+  p->records = (uint8_t*)records;
+  p->record_capacity = (int64_t)(records_bytes / (size_t)lay.record_bytes);
+  p->num_tokens = N;
+  p->topk = desc->topk;
+  p->hidden_size = desc->hidden;
+  p->in_row_bytes = raw ? desc->raw_payload_bytes : 2 * desc->hidden;
+  p->in_scale_bytes = raw ? desc->raw_scale_bytes : 0;
+  p->record_bytes = lay.record_bytes;
+  p->off_ids = lay.off_ids;
+  p->off_weights = lay.off_weights;
+  p->off_payload = lay.off_payload;
+  p->off_scales = lay.off_scales;
+  p->payload_bytes = lay.payload_bytes;
+  p->scale_bytes = lay.scale_bytes;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_dispatch_ranks(const moe_desc_t* desc, const int32_t* topk_idx,
+                       const float* topk_weights, const void* hidden, const void* scales,
+                       const int32_t* send_head, void* records, size_t records_bytes,
+                       moe_stream_t stream) {
   moe::DispatchParams p;
-  p.topk_idx = topk_idx;
-  p.topk_weights = topk_weights;
-  p.hidden = (const uint8_t*)hidden;
-  p.scales = (const uint8_t*)scales;
-  p.slot_of = nullptr;
-  p.records = (uint8_t*)records;
-  p.record_capacity = (int64_t)(records_bytes / (size_t)lay.record_bytes);
-  p.num_tokens = N;
-  p.topk = desc->topk;
-  p.hidden_size = desc->hidden;
-  p.in_row_bytes = raw ? desc->raw_payload_bytes : 2 * desc->hidden;
-  p.in_scale_bytes = raw ? desc->raw_scale_bytes : 0;
-  p.record_bytes = lay.record_bytes;
-  p.off_ids = lay.off_ids;
-  p.off_weights = lay.off_weights;
-  p.off_payload = lay.off_payload;
-  p.off_scales = lay.off_scales;
-  p.payload_bytes = lay.payload_bytes;
-  p.scale_bytes = lay.scale_bytes;
+  bool empty = false;
+  int rc = dispatch_ranks_params(desc, topk_idx, topk_weights, hidden, scales, send_head, records,
+                                 records_bytes, &p, &empty);
+  if (rc != MOE_OK || empty) return rc;
   return cuda_status(moe::launch_dispatch_ranks(p, desc->out_kind, send_head, desc->num_ranks,
                                                 desc->num_experts / desc->num_ranks,
                                                 (cudaStream_t)stream));
@@ -672,15 +693,22 @@ int moe_ll_layout(const moe_desc_t* desc, int32_t max_tokens_per_rank, const int
   return cuda_status(moe::launch_ll_layout(p, (cudaStream_t)stream));
 }
 
-int moe_dispatch_ll(const moe_desc_t* desc, const void* hidden, const void* scales,
-                    const int32_t* ll_slot_of, void* x_out, size_t x_out_bytes, void* scales_out,
-                    size_t scales_out_bytes, moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates moe_dispatch_ll's arguments and fills its launch parameters and
+// the rows the output buffers hold; *empty is set when there is no work.
+int dispatch_ll_params(const moe_desc_t* desc, const void* hidden, const void* scales,
+                       const int32_t* ll_slot_of, void* x_out, size_t x_out_bytes, void* scales_out,
+                       size_t scales_out_bytes, moe::DispatchParams* p, int64_t* rows_out, bool* empty) {
   moe_record_layout_t lay;
   int rc = record_layout(desc, &lay);
   if (rc != MOE_OK) return rc;
   if (lay.payload_bytes % 16) return MOE_ERR_SHAPE;
   const int64_t scale_row = (lay.scale_bytes + 15) / 16 * 16;  // padded scale rows
   const int N = desc->num_tokens;
+  *empty = N == 0;
   if (N == 0) return MOE_OK;
   const bool raw = desc->out_kind == MOE_PAYLOAD_RAW;
   if (!hidden || !ll_slot_of || !x_out) return MOE_ERR_INVALID_ARG;
@@ -695,19 +723,58 @@ int moe_dispatch_ll(const moe_desc_t* desc, const void* hidden, const void* scal
     const int64_t srows = (int64_t)(scales_out_bytes / (size_t)scale_row);
     if (srows < rows) rows = srows;
   }
-  moe::DispatchParams p = {};
-  p.hidden = (const uint8_t*)hidden;
-  p.scales = (const uint8_t*)scales;
-  p.slot_of = ll_slot_of;
-  p.num_tokens = N;
-  p.topk = desc->topk;
-  p.hidden_size = desc->hidden;
-  p.in_row_bytes = raw ? desc->raw_payload_bytes : 2 * desc->hidden;
-  p.in_scale_bytes = raw ? desc->raw_scale_bytes : 0;
-  p.payload_bytes = lay.payload_bytes;
-  p.scale_bytes = lay.scale_bytes;
+  *p = moe::DispatchParams{};
+  p->hidden = (const uint8_t*)hidden;
+  p->scales = (const uint8_t*)scales;
+  p->slot_of = ll_slot_of;
+  p->num_tokens = N;
+  p->topk = desc->topk;
+  p->hidden_size = desc->hidden;
+  p->in_row_bytes = raw ? desc->raw_payload_bytes : 2 * desc->hidden;
+  p->in_scale_bytes = raw ? desc->raw_scale_bytes : 0;
+  p->payload_bytes = lay.payload_bytes;
+  p->scale_bytes = lay.scale_bytes;
+  *rows_out = rows;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_dispatch_ll(const moe_desc_t* desc, const void* hidden, const void* scales,
+                    const int32_t* ll_slot_of, void* x_out, size_t x_out_bytes, void* scales_out,
+                    size_t scales_out_bytes, moe_stream_t stream) {
+  moe::DispatchParams p;
+  int64_t rows = 0;
+  bool empty = false;
+  int rc = dispatch_ll_params(desc, hidden, scales, ll_slot_of, x_out, x_out_bytes, scales_out,
+                              scales_out_bytes, &p, &rows, &empty);
+  if (rc != MOE_OK || empty) return rc;
   return cuda_status(moe::launch_dispatch_packed(p, desc->out_kind, (uint8_t*)x_out,
                                                  (uint8_t*)scales_out, rows, (cudaStream_t)stream));
+}
+
+int moe_layout_ll_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const void* hidden,
+                           const void* scales, int32_t* tokens_per_expert, int32_t* tokens_per_rank,
+                           uint8_t* is_token_in_rank, int32_t* expert_offset, int32_t* rank_offset,
+                           int32_t* slot_of, int32_t* src_of_slot, int32_t max_tokens_per_rank,
+                           int32_t* ll_slot_of, int32_t* src_info, int64_t* layout_range, int32_t* recv_count,
+                           void* workspace, size_t ws_bytes, void* x_out, size_t x_out_bytes, void* scales_out,
+                           size_t scales_out_bytes, moe_stream_t stream) {
+  moe::DispatchParams p;
+  int64_t rows = 0;
+  bool empty = false;
+  int rc = dispatch_ll_params(desc, hidden, scales, ll_slot_of, x_out, x_out_bytes, scales_out,
+                              scales_out_bytes, &p, &rows, &empty);
+  if (rc != MOE_OK) return rc;
+  rc = moe_layout_ll(desc, topk_idx, tokens_per_expert, tokens_per_rank, is_token_in_rank, expert_offset,
+                     rank_offset, slot_of, src_of_slot, max_tokens_per_rank, ll_slot_of, src_info, layout_range,
+                     recv_count, workspace, ws_bytes, stream);
+  if (rc != MOE_OK || empty) return rc;
+  // the previous kernel is this call's own (layout or fixed-capacity layout)
+  return cuda_status(moe::launch_dispatch_packed(p, desc->out_kind, (uint8_t*)x_out, (uint8_t*)scales_out,
+                                                 rows, (cudaStream_t)stream, true));
 }
 
 int moe_combine_backward(const moe_desc_t* desc, const void* grad_out, const float* topk_weights,

@@ -200,8 +200,10 @@ cudaError_t launch_combine_gather_ranks(const RankCombineParams& p, cudaStream_t
 cudaError_t launch_ll_layout(const LlLayoutParams& p, cudaStream_t s);
 cudaError_t launch_combine_backward(const CombineBwdParams& p, cudaStream_t s);
 cudaError_t launch_gather_ranks_backward(const RankCombineBwdParams& p, cudaStream_t s);
+// after_layout (as in launch_dispatch): the previous kernel on s is the same
+// call's layout, so the payload may be built before it ends.
 cudaError_t launch_dispatch_packed(const DispatchParams& p, int out_kind, uint8_t* x_out,
-                                   uint8_t* scales_out, int64_t rows, cudaStream_t s);
+                                   uint8_t* scales_out, int64_t rows, cudaStream_t s, bool after_layout = false);
 cudaError_t launch_mask_topk_ids(int32_t* ids, int64_t total, int topk, const int32_t* num_actual,
                                  cudaStream_t s);
 constexpr int kMaxHiddenNorm = 16384;

@@ -95,6 +95,8 @@ _lib.moe_unpack_slots.restype = ctypes.c_int
 _lib.moe_unpack_slots.argtypes = [_SD, _vp, ctypes.POINTER(_vp), _vp]
 _lib.moe_rank_layout.restype = ctypes.c_int
 _lib.moe_rank_layout.argtypes = [_D, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]
+_lib.moe_layout_ll_dispatch.restype = ctypes.c_int
+_lib.moe_layout_ll_dispatch.argtypes = [_D] + [_vp] * 10 + [_i32] + [_vp] * 5 + [_sz, _vp, _sz, _vp, _sz, _vp]
 _lib.moe_layout_ll.restype = ctypes.c_int
 _lib.moe_layout_ll.argtypes = [_D] + [_vp] * 8 + [_i32] + [_vp] * 5 + [_sz, _vp]
 _lib.moe_layout_ranks.restype = ctypes.c_int
@@ -702,6 +704,25 @@ def prepare_dispatch_ranks(desc: MoeDesc, topk_idx, topk_weights, hidden, scales
                                                  send_head, records))
 
 
+def prepare_layout_ll_dispatch(desc: MoeDesc, max_tokens_per_rank: int, topk_idx, hidden, scales, out: dict,
+                               ll_out: dict, workspace, x_out, scales_out, stream=None) -> Prepared:
+    """moe_layout_ll and moe_dispatch_ll in one call (see include/moe.h)."""
+    d = desc.c()
+    sb = scales_out.numel() * scales_out.element_size() if scales_out is not None else 0
+    args = (ctypes.byref(d),
+            *_vps(topk_idx, hidden, scales, out["tokens_per_expert"], out["tokens_per_rank"],
+                  out["is_token_in_rank"], out["expert_offset"], out["rank_offset"], out["slot_of"],
+                  out.get("src_of_slot")),
+            ctypes.c_int32(max_tokens_per_rank),
+            *_vps(ll_out["ll_slot_of"], ll_out["src_info"], ll_out["layout_range"], ll_out["recv_count"],
+                  workspace),
+            ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(_ptr(x_out)),
+            ctypes.c_size_t(x_out.numel() * x_out.element_size()), ctypes.c_void_p(_ptr(scales_out)),
+            ctypes.c_size_t(sb), ctypes.c_void_p(_stream(stream)))
+    return Prepared("moe_layout_ll_dispatch", args, (d, topk_idx, hidden, scales, out, ll_out, workspace,
+                                                     x_out, scales_out))
+
+
 def prepare_combine_gather_ranks(desc: MoeDesc, recv_out, send_head, out, stream=None) -> Prepared:
     d = desc.c()
     rows = recv_out.numel() // max(desc.hidden, 1)
@@ -758,4 +779,4 @@ def exported_symbols() -> list[str]:
             "moe_dispatch_ranks", "moe_combine_gather_ranks", "moe_ll_layout",
             "moe_dispatch_ll", "moe_combine_backward", "moe_dispatch_backward",
             "moe_combine_gather_ranks_backward", "moe_layout_dispatch", "moe_device_status",
-            "moe_layout_ranks", "moe_layout_ll"]
+            "moe_layout_ranks", "moe_layout_ll", "moe_layout_ll_dispatch"]

@@ -356,6 +356,7 @@ int moe_layout_ranks(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* t
                      int32_t* send_head, int32_t* recv_src_idx, int32_t* recv_offset,
                      int32_t* recv_tokens_per_expert, void* workspace, size_t ws_bytes, moe_stream_t stream);
 
+
 /* Dispatch with one record per (token, rank) at records + send_head[t, r] *
  * record_bytes (moe_record_layout's format and sizes). The payload and
  * scales are those of moe_dispatch. The first segment differs (reading: the
@@ -422,6 +423,21 @@ int moe_layout_ll(const moe_desc_t* desc, const int32_t* topk_idx, int32_t* toke
                   int32_t* rank_offset, int32_t* slot_of, int32_t* src_of_slot, int32_t max_tokens_per_rank,
                   int32_t* ll_slot_of, int32_t* src_info, int64_t* layout_range, int32_t* recv_count,
                   void* workspace, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_layout_ll then moe_dispatch_ll in one call: arguments are those of
+ * moe_layout_ll followed by x_out, x_out_bytes, scales_out and
+ * scales_out_bytes of moe_dispatch_ll (hidden and scales as there). The
+ * dispatch's blocks load and quantise their rows while the layout kernels
+ * still run (they write none of the rows) and read ll_slot_of once they have
+ * completed. Every dispatch argument is checked before anything is launched.
+ * Outputs and errors: those of the two calls. */
+int moe_layout_ll_dispatch(const moe_desc_t* desc, const int32_t* topk_idx, const void* hidden,
+                           const void* scales, int32_t* tokens_per_expert, int32_t* tokens_per_rank,
+                           uint8_t* is_token_in_rank, int32_t* expert_offset, int32_t* rank_offset,
+                           int32_t* slot_of, int32_t* src_of_slot, int32_t max_tokens_per_rank,
+                           int32_t* ll_slot_of, int32_t* src_info, int64_t* layout_range, int32_t* recv_count,
+                           void* workspace, size_t ws_bytes, void* x_out, size_t x_out_bytes, void* scales_out,
+                           size_t scales_out_bytes, moe_stream_t stream);
 
 /* Dispatch into the fixed-capacity buffers: the payload of moe_dispatch
  * (quantised once per token) goes to row ll_slot_of[t, j] of x_out

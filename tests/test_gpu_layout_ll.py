@@ -81,3 +81,45 @@ def test_layout_ll_on_the_two_kernel_layout():
     n, k, e, r = 90000, 8, 512, 16
     ids = np.stack([g.permutation(e)[:k] for _ in range(n)]).astype(np.int32)
     _check(ids, e, r, n // r)
+
+
+@pytest.mark.parametrize("out_kind,n,hidden,r,max_t", [
+    (oracle.FP8_E4M3_B128, 1024, 7168, 8, 128),   # the low-latency workload
+    (oracle.NVFP4_B16, 1000, 1024, 8, 125),
+    (oracle.BF16, 2018, 256, 2, 1009),            # the separate fixed-capacity kernel
+])
+def test_layout_ll_dispatch_one_call(out_kind, n, hidden, r, max_t):
+    """Layout, fixed-capacity layout and the packed payload rows in one call, the
+    dispatch building its rows while the layout runs: all equal the oracle."""
+    from combine_moe_layout_03_gb300 import moe
+    from gpu_helpers import dev_bf16
+    e = 256
+    k = 8 if n != 2018 else 3
+    g = np.random.default_rng(n)
+    ids = np.stack([g.permutation(e)[:k] for _ in range(n)]).astype(np.int32)
+    x = synth.bf16_normal(g, (n, hidden))
+    d = moe.MoeDesc(n, k, e, r, hidden, moe.MOE_PAYLOAD_BF16, out_kind)
+    ids_d = dev_i32(ids)
+    out = moe.layout_outputs(d, ids_d.device)
+    llo = moe.ll_layout_outputs(d, max_t, ids_d.device)
+    ws = torch.empty(max(moe.moe_workspace_size(d), 256), dtype=torch.uint8, device=ids_d.device)
+    lay_rec = moe.moe_record_layout(d)
+    rows = e * llo["capacity"]
+    pb, sbp = lay_rec["payload_bytes"], (lay_rec["scale_bytes"] + 15) // 16 * 16
+    xo = torch.full((rows, pb), 0x5A, dtype=torch.uint8, device=ids_d.device)
+    so = torch.full((rows, max(sbp, 16)), 0x5A, dtype=torch.uint8, device=ids_d.device) if sbp else None
+    moe.prepare_layout_ll_dispatch(d, max_t, ids_d, dev_bf16(x), None, out, llo, ws, xo, so)()
+    torch.cuda.synchronize()
+    lref = oracle.ll_layout(ids, e, r, max_t)
+    for key in LLKEYS:
+        np.testing.assert_array_equal(host(llo[key]).reshape(lref[key].shape), lref[key], err_msg=key)
+    ref_x, ref_s = oracle.dispatch_ll(x, None, lref["ll_slot_of"], rows, oracle.BF16, out_kind, hidden)
+    so_h = lref["ll_slot_of"]
+    used = np.zeros(rows, bool)
+    used[so_h[so_h >= 0]] = True
+    gx = host(xo)
+    np.testing.assert_array_equal(gx[used], ref_x[used])
+    assert (gx[~used] == 0x5A).all()
+    if so is not None:
+        gs = host(so)
+        np.testing.assert_array_equal(gs[used], ref_s[used])

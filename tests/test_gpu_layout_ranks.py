@@ -81,3 +81,4 @@ def test_layout_ranks_on_the_two_kernel_path():
     n, k, e, r = 90000, 8, 512, 16
     ids = np.stack([g.permutation(e)[:k] for _ in range(n)]).astype(np.int32)
     _check(ids, e, r, 8)
+
