@@ -353,10 +353,13 @@ __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams
 // bytes. The consumer warps wait on it, run the fp32 chains of combine_chunk
 // from shared memory (same operations in the same order, so the result is
 // the same bit for bit), store the row slice and release the stage on its
-// "empty" mbarrier. kPipeStages stages are in flight per block.
+// "empty" mbarrier. kPipeStages stages are in flight per block. Two stages of
+// up to 16 KB (top-8) let about six blocks share an SM: more producers
+// issuing copies at once beat deeper pipelines in fewer blocks (a sweep of
+// 2/4/8 stages and 2/4/8/16 consumer warps at hidden 7168 and 8192).
 constexpr int kPipeConsumerWarps = 4;
 constexpr int kPipeThreads = 32 * (1 + kPipeConsumerWarps);
-constexpr int kPipeStages = 4;
+constexpr int kPipeStages = 2;
 constexpr int kPipeMaxSliceChunks = 32 * kPipeConsumerWarps;  // one chunk per consumer thread
 
 struct PipeHeader {  // one per stage, before its row slices
@@ -639,9 +642,9 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   //    cover DRAM latency at full bandwidth: from 768 tokens of top-8 up;
   //  * below that, the persistent warp kernel when every unit of at most two
   //    32-chunk steps has a resident warp (one round of row loads per warp);
-  //  * otherwise the pipelined kernel, whose bulk copies keep up to 64 KB per
+  //  * otherwise the pipelined kernel, whose bulk copies keep up to 32 KB per
   //    block in flight without registers (256 and 512 tokens of hidden 8192:
-  //    12.3 -> 10.4 us and 17.1 -> 15.7 us back to back).
+  //    12.3 -> 10.0 us and 17.1 -> 14.9 us back to back).
   const int chunks = p.hidden_size / 8;
   const int steps_per_token = (chunks + 31) / 32;  // warp steps of 32 chunks
   const int g = p.group_by_rank ? 1 : 0;
