@@ -669,7 +669,7 @@ def run_decode_sweep(args, rank, world):
         "config": {"workload": "decode sweep: N = 1..256 tokens, top-8 of 256 R=8, raw 3584 B + 448 B "
                                "payload per token, BF16 combine H=7168 (value and ms_per_step at N=256)",
                    "l2": "flushed before every timed step"},
-        "sweep": rows, "gpu_launches": launches, "clocks": clk,
+        "sweep": rows, "floor": floor, "gpu_launches": launches, "clocks": clk,
     }
 
 
@@ -678,12 +678,25 @@ def rs_sweep_rows(dev, K, W, seed_base, flush, flush_read, stream):
     tokens per rank: the rank sum of BF16 partials and the top-8 reduction
     grouped by rank, one call after an L2 flush and calls back to back on
     copies of the inputs beyond twice the L2. Returns (rows, kernels
-    launched)."""
+    launched, floor): floor times the rank sum of one token per rank (80 KB
+    moved) both ways, the fixed cost every call of the sweep carries."""
     import torch
     from combine_moe_layout_03_gb300 import moe, synth
     peak = measured_peaks()["hbm_gbs"]
     r, h, k, e = 4, 8192, 8, 256
     rows, launches = [], 0
+    c = synth.rs_case(seed=seed_base, tokens_per_rank=1, hidden=h, r=r, e=e, k=k, with_expert_out=False)
+    part = torch.from_numpy(c["partials_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+    outs = [torch.empty((r, h), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    tiny = [moe.prepare_combine(moe.MoeDesc(r, k, e, r, h), moe.MOE_COMBINE_RANKS, part, None, None,
+                                None, o) for o in outs]
+    for _ in range(W):
+        tiny[0]()
+    floor = {"rank_sum_us": round(_timed(tiny[0], K, flush, flush_read, stream), 2),
+             "rank_sum_us_back_to_back": round(_timed_b2b(tiny, K, stream), 2),
+             "what": "rank sum of one token per rank (80 KB moved): the fixed cost of a call"}
+    launches += W + 2 * K
+    del tiny, outs, part
     for t in RS_SWEEP_T:
         c = synth.rs_case(seed=seed_base + t, tokens_per_rank=t, hidden=h, r=r, e=e, k=k)
         n = r * t
@@ -726,7 +739,7 @@ def rs_sweep_rows(dev, K, W, seed_base, flush, flush_read, stream):
                      "topk_ranks_frac_back_to_back": round(b_f / us_fb / 1e3 / peak, 3)})
         del parts, ys, outs, ranks_b, fused_b
         launches += 4 * K
-    return rows, launches
+    return rows, launches, floor
 
 
 def run_rs_sweep(args, rank, world):
@@ -742,7 +755,7 @@ def run_rs_sweep(args, rank, world):
     stream = torch.cuda.current_stream()
     K, W = min(args.steps, 100), args.warmup
     clocks = ClockSampler(gpu_uuid())
-    rows, launches = rs_sweep_rows(dev, K, W, rank * 1000, flush, flush_read, stream)
+    rows, launches, floor = rs_sweep_rows(dev, K, W, rank * 1000, flush, flush_read, stream)
     clk = clocks.stop()
     r = 4
     last = rows[-1]
@@ -825,13 +838,14 @@ def run_configs(args, dev, flush, flush_read, stream) -> dict:
                            "what": "top-8 of 256, R=8, raw 3584 B + 448 B payload, BF16 combine "
                                    "H=7168; one step = layout + dispatch + combine"}
 
-    rows, n_l = rs_sweep_rows(dev, K, W, 300, flush, flush_read, stream)
+    rows, n_l, floor = rs_sweep_rows(dev, K, W, 300, flush, flush_read, stream)
     launches += n_l
     out["rs_sweep"] = {"out_mib_per_rank": [r["out_mib_per_rank"] for r in rows]}
     for key in ("rank_sum_us", "rank_sum_frac", "topk_ranks_us", "topk_ranks_frac",
                 "rank_sum_us_back_to_back", "rank_sum_frac_back_to_back",
                 "topk_ranks_us_back_to_back", "topk_ranks_frac_back_to_back"):
         out["rs_sweep"][key] = [r[key] for r in rows]
+    out["rs_sweep"]["floor_us"] = [floor["rank_sum_us"], floor["rank_sum_us_back_to_back"]]
     out["rs_sweep"]["what"] = ("R=4, H=8192: rank sum of BF16 partials and top-8 reduction grouped "
                                "by rank; one call after an L2 flush, and calls back to back")
 
