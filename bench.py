@@ -669,7 +669,7 @@ def run_decode_sweep(args, rank, world):
         "config": {"workload": "decode sweep: N = 1..256 tokens, top-8 of 256 R=8, raw 3584 B + 448 B "
                                "payload per token, BF16 combine H=7168 (value and ms_per_step at N=256)",
                    "l2": "flushed before every timed step"},
-        "sweep": rows, "floor": floor, "gpu_launches": launches, "clocks": clk,
+        "sweep": rows, "gpu_launches": launches, "clocks": clk,
     }
 
 
@@ -770,7 +770,7 @@ def run_rs_sweep(args, rank, world):
                                "(value at 512 tokens per rank, grouped form)",
                    "l2": "flushed before every timed call; the back-to-back columns cycle through "
                          "copies of the inputs larger than twice the L2 instead"},
-        "sweep": rows, "gpu_launches": launches, "clocks": clk,
+        "sweep": rows, "floor": floor, "gpu_launches": launches, "clocks": clk,
         "pages_context_us": {"0.5": [42.4, 35.6], "1": [43.1, 37.1], "2": [42.3, 37.4],
                              "4": [51.6, 43.5], "8": [84.8, 76.7],
                              "note": "NCCL symmetric reduce-scatter, staged and direct, 4 GPUs over "
