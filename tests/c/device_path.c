@@ -2,9 +2,11 @@
  * files, allocates device memory with the CUDA runtime, runs moe_layout,
  * moe_dispatch (BF16 rows to FP8 records) and moe_combine (grouped by rank)
  * through libmoe.so on the default stream, then moe_layout_dispatch on the
- * first 128 tokens (layout and dispatch in one kernel), and writes slot_of,
- * the records and the combined rows back to files for the test that builds
- * and runs it (tests/test_gpu_c_consumer.py) to check against the oracle.
+ * first 128 tokens (layout and dispatch in one kernel), then the
+ * fixed-capacity path (moe_layout_ll_dispatch) on the first R * 16 tokens,
+ * and writes slot_of, the records, the combined rows and the fixed-capacity
+ * outputs back to files for the test that builds and runs it
+ * (tests/test_gpu_c_consumer.py) to check against the oracle.
  *   device_path DIR   with DIR/meta.txt = "N k E R H P" and ids.bin, w.bin,
  *   x.bin (bf16 bits), y.bin (bf16 bits, P rows) */
 #include <cuda_runtime.h>
@@ -152,6 +154,54 @@ int main(int argc, char** argv) {
   if (write_file(dir, "slot_of_small.bin", slot, small_pairs * 4) ||
       write_file(dir, "records_small.bin", rec, small_rec))
     return fail("output files", -1);
-  printf("ok records=%d record_bytes=%d\n", p, (int)lay.record_bytes);
+  /* The fixed-capacity path on the first R * T tokens: positions
+     [E * R * T] rows, then the payload and scales of every pair gathered in
+     pair order (zero rows for pairs past the capacity or without an expert). */
+  const int T = 16;
+  const int n_ll = r * T <= n ? r * T : n - n % r;
+  moe_desc_t dl = d;
+  dl.num_tokens = n_ll;
+  const size_t ll_pairs = (size_t)n_ll * k;
+  const size_t cap = (size_t)r * T, rows_ll = (size_t)e * cap;
+  const size_t pb = (size_t)lay.payload_bytes, sb = ((size_t)lay.scale_bytes + 15) & ~(size_t)15;
+  int32_t *d_llslot, *d_info, *d_cnt;
+  int64_t* d_range;
+  uint8_t *d_xo, *d_so;
+  CUDA(cudaMalloc((void**)&d_llslot, ll_pairs * 4));
+  CUDA(cudaMalloc((void**)&d_info, rows_ll * 4));
+  CUDA(cudaMalloc((void**)&d_range, (size_t)e * r * 8));
+  CUDA(cudaMalloc((void**)&d_cnt, (size_t)e * 4));
+  CUDA(cudaMalloc((void**)&d_xo, rows_ll * pb));
+  CUDA(cudaMalloc((void**)&d_so, rows_ll * sb));
+  rc = moe_layout_ll_dispatch(&dl, d_ids, d_x, NULL, d_tpe, d_tpr, d_mask, d_eo, d_ro, d_slot2, d_src, T, d_llslot,
+                              d_info, d_range, d_cnt, d_ws, ws_bytes, d_xo, rows_ll * pb, d_so, rows_ll * sb, NULL);
+  if (rc) return fail("moe_layout_ll_dispatch", rc);
+  status = -100;
+  rc = moe_layout_status(d_ws, &status, NULL);
+  if (rc || status) return fail("moe_layout_status (fixed capacity)", rc ? rc : status);
+  int32_t* llslot = malloc(ll_pairs * 4);
+  int32_t* info = malloc(rows_ll * 4);
+  int64_t* range = malloc((size_t)e * r * 8);
+  int32_t* cnt = malloc((size_t)e * 4);
+  uint8_t* xg = calloc(ll_pairs, pb);
+  uint8_t* sg = calloc(ll_pairs, sb);
+  if (!llslot || !info || !range || !cnt || !xg || !sg) return fail("host memory", -1);
+  CUDA(cudaMemcpy(llslot, d_llslot, ll_pairs * 4, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(info, d_info, rows_ll * 4, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(range, d_range, (size_t)e * r * 8, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(cnt, d_cnt, (size_t)e * 4, cudaMemcpyDeviceToHost));
+  for (size_t q = 0; q < ll_pairs; ++q) {
+    const int32_t pos = llslot[q];
+    if (pos < 0 || (size_t)pos >= rows_ll) continue;
+    CUDA(cudaMemcpy(xg + q * pb, d_xo + (size_t)pos * pb, pb, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(sg + q * sb, d_so + (size_t)pos * sb, sb, cudaMemcpyDeviceToHost));
+  }
+  if (write_file(dir, "ll_slot_of.bin", llslot, ll_pairs * 4) ||
+      write_file(dir, "ll_src_info.bin", info, rows_ll * 4) ||
+      write_file(dir, "ll_layout_range.bin", range, (size_t)e * r * 8) ||
+      write_file(dir, "ll_recv_count.bin", cnt, (size_t)e * 4) ||
+      write_file(dir, "ll_x_pairs.bin", xg, ll_pairs * pb) || write_file(dir, "ll_s_pairs.bin", sg, ll_pairs * sb))
+    return fail("output files", -1);
+  printf("ok records=%d record_bytes=%d ll_tokens=%d\n", p, (int)lay.record_bytes, n_ll);
   return 0;
 }

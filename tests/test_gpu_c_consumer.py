@@ -1,8 +1,10 @@
 """The device path from a plain C program: tests/c/device_path.c, built with
 the CUDA toolkit's compiler against include/moe.h and libmoe.so, allocates
 its own device memory, runs moe_layout, moe_dispatch (FP8 records) and
-moe_combine (grouped by rank) on inputs this test writes, and its slot map,
-records and combined rows equal the oracle's."""
+moe_combine (grouped by rank) on inputs this test writes, then the one-call
+layout + dispatch and the one-call fixed-capacity layout + dispatch
+(moe_layout_ll_dispatch); its slot maps, records, combined rows, positions,
+ranges and packed rows equal the oracle's."""
 import os
 import shutil
 import subprocess
@@ -67,3 +69,25 @@ def test_c_program_runs_the_device_path(tmp_path):
                              oracle.FP8_E4M3_B128, h)
     got_s = np.fromfile(d / "records_small.bin", dtype=np.uint8).reshape(-1, got.shape[1])
     np.testing.assert_array_equal(got_s[:ps], want_s)
+
+    # the fixed-capacity path on the first R * 16 tokens
+    T = 16
+    nl = r * T
+    ll = oracle.ll_layout(ids[:nl], e, r, T)
+    cap = r * T
+    rows = e * cap
+    np.testing.assert_array_equal(np.fromfile(d / "ll_slot_of.bin", dtype=np.int32).reshape(nl, k),
+                                  ll["ll_slot_of"])
+    np.testing.assert_array_equal(np.fromfile(d / "ll_src_info.bin", dtype=np.int32).reshape(e, cap),
+                                  ll["src_info"])
+    np.testing.assert_array_equal(np.fromfile(d / "ll_layout_range.bin", dtype=np.int64).reshape(e, r),
+                                  ll["layout_range"])
+    np.testing.assert_array_equal(np.fromfile(d / "ll_recv_count.bin", dtype=np.int32), ll["recv_count"])
+    xo, so = oracle.dispatch_ll(x[:nl], None, ll["ll_slot_of"], rows, oracle.BF16, oracle.FP8_E4M3_B128, h)
+    pos = ll["ll_slot_of"].ravel()
+    used = pos >= 0
+    assert used.all()                    # no pair past the capacity or without an expert here
+    got_x = np.fromfile(d / "ll_x_pairs.bin", dtype=np.uint8).reshape(nl * k, xo.shape[1])
+    got_s = np.fromfile(d / "ll_s_pairs.bin", dtype=np.uint8).reshape(nl * k, so.shape[1])
+    np.testing.assert_array_equal(got_x, xo[pos])
+    np.testing.assert_array_equal(got_s, so[pos])
