@@ -27,6 +27,7 @@
 // order. The next unit's pair info is fetched while the current unit
 // streams, so its latency is hidden.
 #include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -378,7 +379,7 @@ __device__ __forceinline__ void record_timeout() { atomicExch(&g_device_status, 
 template <bool GROUP>
 __global__ void __launch_bounds__(kPipeThreads)
     k_combine_pipe(CombineParams p, int slice_chunks, int slices_per_token, int64_t num_units,
-                   int64_t units_per_block, int stage_bytes) {
+                   int64_t units_per_block, int stage_bytes, uint64_t wait_ns) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(128) uint8_t pipe_smem[];
@@ -434,7 +435,8 @@ __global__ void __launch_bounds__(kPipeThreads)
         fetch(t + 1);
       }
       // (the whole warp leaves together if any lane's wait gave up)
-      if (issued >= kPipeStages && !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((issued / kPipeStages) + 1) & 1))) {
+      if (issued >= kPipeStages &&
+          !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((issued / kPipeStages) + 1) & 1, wait_ns))) {
         ok = false;
         break;
       }
@@ -453,13 +455,13 @@ __global__ void __launch_bounds__(kPipeThreads)
         bulk_g2s(stage + kPipeHeaderBytes + (size_t)lane * slice_bytes,
                  p.expert_out + (size_t)pl.slot * row_bytes + (size_t)c0 * 16, bytes, &full[st], pol);
     }
-    if (!ok) {
-      if (lane == 0) record_timeout();
-      // no copy may land in shared memory after the block has exited: wait
-      // (bounded) for the phases of the stages still in flight
-      for (int i = max(0, issued - kPipeStages); i < issued; ++i)
-        mbar_wait(&full[i % kPipeStages], (i / kPipeStages) & 1);
-    }
+    if (!ok && lane == 0) record_timeout();
+    // No copy may land in shared memory after the block has exited, and the
+    // consumers that would otherwise hold the block until the last stage has
+    // landed may have given up: wait (bounded, always with the full budget)
+    // for the last phase of every stage in use.
+    for (int i = max(0, issued - kPipeStages); i < issued; ++i)
+      mbar_wait(&full[i % kPipeStages], (i / kPipeStages) & 1);
     return;
   }
 
@@ -468,7 +470,7 @@ __global__ void __launch_bounds__(kPipeThreads)
   int done = 0;
   for (int64_t u = u0; u < u1; ++u, ++done) {
     const int st = done % kPipeStages;
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (done / kPipeStages) & 1))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (done / kPipeStages) & 1, wait_ns))) {
       if (lane == 0) record_timeout();
       return;
     }
@@ -588,6 +590,9 @@ const DeviceInfo* device_info() {
 
 }  // namespace
 
+// The bounded waits' budget passed to each launch of the pipelined combine.
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
+
 // Which combines take the pipelined kernel: MOE_COMBINE_PIPE unset or 1 the
 // automatic choice of launch_combine_topk, 0 none, 2 all.
 int pipe_policy() {
@@ -625,7 +630,8 @@ cudaError_t launch_combine_pipe(const CombineParams& p, const DeviceInfo* di, cu
   CombineParams q = p;
   int sc = slice, spt = slices_per_token, sb = stage_bytes;
   int64_t nu = num_units, upb = per_block;
-  void* args[] = {&q, &sc, &spt, &nu, &upb, &sb};
+  uint64_t wns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  void* args[] = {&q, &sc, &spt, &nu, &upb, &sb, &wns};
   return launch_pdl(fn, dim3((unsigned)blocks), dim3(kPipeThreads), smem, s, args);
 }
 
@@ -685,6 +691,10 @@ cudaError_t launch_combine_topk(const CombineParams& p, cudaStream_t s) {
   void* args[] = {&q, &upt, &cpu, &nu};
   const void* fn = p.group_by_rank ? (const void*)k_combine_topk<true> : (const void*)k_combine_topk<false>;
   return launch_pdl(fn, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s, args);
+}
+
+void set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns == 0 || ns > kWaitLimitNs ? kWaitLimitNs : ns, std::memory_order_relaxed);
 }
 
 int read_device_status(int32_t* out, bool clear) {

@@ -371,6 +371,11 @@ int moe_device_status(int32_t* status, int clear) {
   return moe::read_device_status(status, clear != 0);
 }
 
+int moe_set_wait_limit_ns(uint64_t ns) {
+  moe::set_wait_limit_ns(ns);
+  return MOE_OK;
+}
+
 }  // extern "C"
 
 namespace {

@@ -183,6 +183,9 @@ cudaError_t launch_combine_norm(const CombineNormParams& p, cudaStream_t s);
 // The device status word of the kernels with bounded waits (MOE_OK, or
 // MOE_ERR_TIMEOUT once a wait gave up); synchronous. clear: reset it to MOE_OK.
 int read_device_status(int32_t* out, bool clear);
+// The budget of the bounded waits for launches from now on (ns; 0 = the
+// default kWaitLimitNs; clamped to it).
+void set_wait_limit_ns(uint64_t ns);
 cudaError_t launch_slots(bool pack, const void* const* src, void* const* dst,
                          const moe_slot_desc_t* d, const int64_t* offsets, int64_t slot_bytes,
                          cudaStream_t s);
@@ -340,21 +343,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking form: true once the phase with this parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
 // Every wait on an mbarrier in this library is bounded: it gives up after
-// kWaitLimitNs of wall time (far beyond any legitimate wait: the copies it
-// waits for are reads of this GPU's own memory) and returns false, and the
-// caller records MOE_ERR_TIMEOUT in the library's device status word.
+// limit_ns of wall time (kWaitLimitNs unless moe_set_wait_limit_ns lowered it
+// for a test; far beyond any legitimate wait: the copies it waits for are
+// reads of this GPU's own memory) and returns false, and the caller records
+// MOE_ERR_TIMEOUT in the library's device status word.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+  if (limit_ns < kWaitLimitNs) {
+    // a lowered budget (test hook): poll without suspending, since try_wait
+    // may sleep longer than the budget before it reports
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_test_wait(bar, parity)) {
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }

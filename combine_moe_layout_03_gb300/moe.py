@@ -119,6 +119,8 @@ _lib.moe_mask_topk_ids.restype = ctypes.c_int
 _lib.moe_mask_topk_ids.argtypes = [_vp, _i32, _i32, _vp, _vp]
 _lib.moe_device_status.restype = ctypes.c_int
 _lib.moe_device_status.argtypes = [_vp, ctypes.c_int]
+_lib.moe_set_wait_limit_ns.restype = ctypes.c_int
+_lib.moe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
 _lib.moe_pack_record.restype = ctypes.c_int
 _lib.moe_pack_record.argtypes = [_D, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
 _lib.moe_unpack_record.restype = ctypes.c_int
@@ -240,6 +242,12 @@ def moe_device_status(clear: bool = True) -> int:
     v = _i32(0)
     _check(_lib.moe_device_status(ctypes.byref(v), 1 if clear else 0), "moe_device_status")
     return v.value
+
+
+def moe_set_wait_limit_ns(ns: int) -> None:
+    """Budget of the bounded waits for later launches (0 = the default one
+    second; a test hook, see include/moe.h)."""
+    _check(_lib.moe_set_wait_limit_ns(int(ns)), "moe_set_wait_limit_ns")
 
 
 def moe_layout_status(workspace: torch.Tensor, stream=None) -> int:
@@ -779,4 +787,4 @@ def exported_symbols() -> list[str]:
             "moe_dispatch_ranks", "moe_combine_gather_ranks", "moe_ll_layout",
             "moe_dispatch_ll", "moe_combine_backward", "moe_dispatch_backward",
             "moe_combine_gather_ranks_backward", "moe_layout_dispatch", "moe_device_status",
-            "moe_layout_ranks", "moe_layout_ll", "moe_layout_ll_dispatch"]
+            "moe_layout_ranks", "moe_layout_ll", "moe_layout_ll_dispatch", "moe_set_wait_limit_ns"]

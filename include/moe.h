@@ -197,6 +197,17 @@ int moe_layout_status(const void* workspace, int32_t* status, moe_stream_t strea
  * loop. Errors: INVALID_ARG, CUDA. */
 int moe_device_status(int32_t* status, int clear);
 
+/* Test hook for the bounded waits above. Sets, for launches made after the
+ * call, how long each such wait may last before it gives up: ns of wall time
+ * (%globaltimer), clamped to the default of one second; ns = 0 restores the
+ * default. With a budget far below a copy's latency (e.g. 1 ns) the waits
+ * give up at once: the kernel records MOE_ERR_TIMEOUT for moe_device_status,
+ * leaves the output rows it did not finish unwritten and returns, with the
+ * context still usable. A block always waits, with the full second, for the
+ * copies it issued before it exits, so no copy lands after it. Process-wide
+ * (every device), host only, does not synchronise. Always returns MOE_OK. */
+int moe_set_wait_limit_ns(uint64_t ns);
+
 /* Permute and pack (dispatch). For every pair (t, j) with slot_of[t, j] >= 0
  * writes one record (moe_record_layout) to
  * records + slot_of[t, j] * record_bytes. The payload of a token is computed
