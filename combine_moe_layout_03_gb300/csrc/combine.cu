@@ -275,6 +275,9 @@ __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams
   for (int cb = 0; cb < chunks; cb += kNormThreads) {  // uniform trip count per warp
     const int c = cb + (int)threadIdx.x;
     const bool on = c < chunks;
+    // the residual chunk's load goes out with the expert rows' loads
+    uint4 rv = make_uint4(0, 0, 0, 0);
+    if (on) rv = ld_stream_v4(q.residual_in + (size_t)t * row_bytes + (size_t)c * 16);
     float x[8];
     if (MODE == MOE_COMBINE_RANKS) {
 #pragma unroll
@@ -306,7 +309,6 @@ __global__ void __launch_bounds__(kNormThreads) k_combine_norm(CombineNormParams
       combine_chunk<GROUP>(pl, p.expert_out + (size_t)c * 16, row_bytes, on, x);
     }
     if (on) {
-      const uint4 rv = ld_stream_v4(q.residual_in + (size_t)t * row_bytes + (size_t)c * 16);
       x[0] = __fadd_rn(x[0], bf16_lo(rv.x));
       x[1] = __fadd_rn(x[1], bf16_hi(rv.x));
       x[2] = __fadd_rn(x[2], bf16_lo(rv.y));
