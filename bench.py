@@ -1036,22 +1036,27 @@ def routing_stats(tokens_per_expert, tokens_per_rank) -> dict:
             "tokens_per_rank_mean": round(float(tpr.mean()), 2) if tpr.size else 0.0}
 
 
+E2E_SETS = 3  # buffer sets of the end-to-end pipeline
+
+
 def measure_e2e(st: Step, spec: dict, dev, K: int, W: int, seed: int = 0) -> dict:
     """The same step through the public API with the inputs copied from pinned
     host memory every step and the combined output read back every step.
 
-    Pipelined as a serving loop would run it: two buffer sets; step i's inputs
-    are copied on one stream while step i-1 computes and step i-2's output is
-    read back on another, with events ordering each buffer's reuse. The serial
-    form (copy in, compute, copy out, one stream) is reported beside it."""
+    Pipelined as a serving loop would run it: E2E_SETS buffer sets; step i's
+    inputs are copied on one stream while earlier steps compute and are read
+    back on another, with events ordering each buffer set's reuse (step i
+    reuses the set of step i - E2E_SETS). The serial form (copy in, compute,
+    copy out, one stream) is reported beside it."""
     import torch
     n = spec["num_tokens"]
-    sets = [st, Step(spec, dev, seed)]
+    NB = E2E_SETS
+    sets = [st] + [Step(spec, dev, seed) for _ in range(NB - 1)]
     h_ids = st.ids.cpu().pin_memory()
     h_w = st.w.cpu().pin_memory()
     h_x = st.x.cpu().pin_memory()
     h_sc = st.sc.cpu().pin_memory() if st.sc is not None else None
-    h_out = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(2)]
+    h_out = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(NB)]
     h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_w, h_x))
     if h_sc is not None:
         h2d += h_sc.numel()
@@ -1072,22 +1077,22 @@ def measure_e2e(st: Step, spec: dict, dev, K: int, W: int, seed: int = 0) -> dic
         h_out[0].copy_(S.out, non_blocking=True)
 
     def pipelined(steps, comp=comp, s_in=s_in, s_out=s_out, runs=None):
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_comp = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
+        ev_in = [torch.cuda.Event() for _ in range(NB)]
+        ev_comp = [torch.cuda.Event() for _ in range(NB)]
+        ev_out = [torch.cuda.Event() for _ in range(NB)]
         s_in.wait_stream(comp)
         s_out.wait_stream(comp)
         for i in range(steps):
-            bset = i % 2
+            bset = i % NB
             S = sets[bset]
             with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(ev_comp[bset])  # step i-2 is done with these inputs
+                if i >= NB:
+                    s_in.wait_event(ev_comp[bset])  # step i-NB is done with these inputs
                 copy_in(S)
                 ev_in[bset].record(s_in)
             comp.wait_event(ev_in[bset])
-            if i >= 2:
-                comp.wait_event(ev_out[bset])  # step i-2's output has been read back
+            if i >= NB:
+                comp.wait_event(ev_out[bset])  # step i-NB's output has been read back
             if runs is None:
                 S.run()
             else:
@@ -1104,7 +1109,7 @@ def measure_e2e(st: Step, spec: dict, dev, K: int, W: int, seed: int = 0) -> dic
     # the same pipeline of G steps captured once in a CUDA graph (copies,
     # library calls and the event edges between the three streams) and
     # replayed: the host issues one launch per G steps
-    G = 16
+    G = 8 * NB
     g_comp, g_in, g_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     runs = [S.calls_on(g_comp) for S in sets]
     g_comp.wait_stream(comp)
@@ -1144,8 +1149,8 @@ def measure_e2e(st: Step, spec: dict, dev, K: int, W: int, seed: int = 0) -> dic
         b.record(comp)
         torch.cuda.synchronize()
         res[name] = a.elapsed_time(b) / steps
-    pipe = ("the inputs of step i copied in while step i-1 computes and step i-2 is read back "
-            "(two buffer sets, three streams)")
+    pipe = (f"the inputs of step i copied in while earlier steps compute and are read back "
+            f"({NB} buffer sets, three streams)")
     # the faster of the two ways of issuing the same pipeline: the graph wins
     # where the host's issue rate bounds a small step, eager issue where the
     # host link does (each graph replay drains the pipeline once)
