@@ -269,15 +269,35 @@ class Step:
         n, k, e, r, h = (spec["num_tokens"], spec["topk"], spec["num_experts"],
                          spec["num_ranks"], spec["hidden"])
         self.host = c
-        self.ids = torch.from_numpy(c["topk_idx"]).to(dev)
-        self.w = torch.from_numpy(c["topk_weights"]).to(dev)
+        # the step's inputs (ids, weights, the row, raw scales) as 256-byte-
+        # aligned views of one device buffer, so that a step's host copy is a
+        # single transfer (the end-to-end measurement)
         if spec["out_kind"] == "raw":
-            self.x = torch.from_numpy(c["payload"]).to(dev)
-            self.sc = torch.from_numpy(c["scales"]).to(dev)
+            parts = [c["topk_idx"], c["topk_weights"], c["payload"], c["scales"]]
+        else:
+            parts = [c["topk_idx"], c["topk_weights"], c["hidden_bf16"].view(np.int16)]
+        offs, total = [], 0
+        for a in parts:
+            offs.append(total)
+            total += (a.nbytes + 255) // 256 * 256
+        staged = np.zeros(total, np.uint8)
+        for a, o in zip(parts, offs):
+            staged[o:o + a.nbytes] = np.ascontiguousarray(a).reshape(-1).view(np.uint8)
+        self.inputs = torch.from_numpy(staged).to(dev)
+
+        def view(i, dtype):
+            a = parts[i]
+            return self.inputs[offs[i]:offs[i] + a.nbytes].view(dtype).view(a.shape)
+
+        self.ids = view(0, torch.int32)
+        self.w = view(1, torch.float32)
+        if spec["out_kind"] == "raw":
+            self.x = view(2, torch.uint8)
+            self.sc = view(3, torch.uint8)
             self.desc = moe.MoeDesc(n, k, e, r, h, moe.MOE_PAYLOAD_RAW, moe.MOE_PAYLOAD_RAW,
                                     3584, 448)
         else:
-            self.x = torch.from_numpy(c["hidden_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+            self.x = view(2, torch.bfloat16)
             self.sc = None
             kind = moe.MOE_PAYLOAD_FP8_E4M3_B128 if spec["out_kind"] == "fp8" else moe.MOE_PAYLOAD_BF16
             self.desc = moe.MoeDesc(n, k, e, r, h, moe.MOE_PAYLOAD_BF16, kind)
@@ -429,8 +449,9 @@ class Step:
         moe = self.moe
         n, k, h = spec["num_tokens"], spec["topk"], spec["hidden"]
         P = self.y.shape[0]
-        self.x = torch.from_numpy(synth.bf16_normal(synth.rng_for(seed, 14), (n, h))
-                                  .view(np.int16)).to(dev).view(torch.bfloat16)
+        # g goes into the packed input buffer in place of the row
+        self.x.copy_(torch.from_numpy(synth.bf16_normal(synth.rng_for(seed, 14), (n, h))
+                                      .view(np.int16)).to(dev).view(torch.bfloat16))
         self.sc = None
         self.records = None
         self.grad_y = torch.empty((P, h), dtype=torch.bfloat16, device=dev)
@@ -1052,24 +1073,17 @@ def measure_e2e(st: Step, spec: dict, dev, K: int, W: int, seed: int = 0) -> dic
     n = spec["num_tokens"]
     NB = E2E_SETS
     sets = [st] + [Step(spec, dev, seed) for _ in range(NB - 1)]
-    h_ids = st.ids.cpu().pin_memory()
-    h_w = st.w.cpu().pin_memory()
-    h_x = st.x.cpu().pin_memory()
-    h_sc = st.sc.cpu().pin_memory() if st.sc is not None else None
+    # the step's inputs in pinned host memory, laid out as Step.inputs (ids,
+    # weights, the row and raw scales at 256-byte-aligned offsets): one copy
+    h_in = st.inputs.cpu().pin_memory()
     h_out = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(NB)]
-    h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_w, h_x))
-    if h_sc is not None:
-        h2d += h_sc.numel()
+    h2d = h_in.numel()
     d2h = h_out[0].numel() * h_out[0].element_size()
     comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def copy_in(S):
-        S.ids.copy_(h_ids, non_blocking=True)
-        S.w.copy_(h_w, non_blocking=True)
-        S.x.copy_(h_x, non_blocking=True)
-        if h_sc is not None:
-            S.sc.copy_(h_sc, non_blocking=True)
+        S.inputs.copy_(h_in, non_blocking=True)
 
     def serial(S):
         copy_in(S)
